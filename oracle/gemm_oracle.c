@@ -1,0 +1,263 @@
+/*
+ * gemm_oracle.c -- CPU oracle for dense GEMM.  TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline leg may
+ * load this code.  The product (the CUDA library) never calls it, and it
+ * shares no source, header or helper with the CUDA path.
+ *
+ * What it computes, for every 0 <= i < M, 0 <= j < N:
+ *
+ *     ref(i,j) = alpha * sum_{k<K} a(i,k) * b(k,j) + beta * c(i,j)
+ *
+ * This is the BLAS GEMM update C <- alpha*A*B + beta*C given in
+ * "AI Programming: Matrix Product" (elainafan.one), section "Dense matrix
+ * multiplication" (the text after the stripped formula says that alpha and
+ * beta let one call scale and accumulate).  The loop follows the CPU triple
+ * loop of the same page, section "Row-major order", with two changes that
+ * only widen precision: the accumulator is fp64 (int64 for INT8 inputs), and
+ * every stored operand is first decoded exactly to fp64.
+ *
+ * Layout (same page, section "Row-major order": offset = row*ld + col):
+ *   A(i,k) = A[i*lda + k]                   (row-major)
+ *   B(k,j) = B[k*ldb + j]   if layout_b==0  (row-major, K x N)
+ *          = B[j*ldb + k]   if layout_b==1  (column-major, i.e. stored N x K)
+ *   C(i,j) = C[i*ldc + j]                   (row-major)
+ *
+ * BLAS conventions (readings where the pages are silent):
+ *   beta == 0  -> C is not read (NaN/Inf in C do not reach the result);
+ *   alpha == 0 -> A and B are not read; ref = beta*c.
+ *
+ * The k order of every sum is ascending, so the result does not depend on
+ * the OpenMP thread count.
+ *
+ * Error bound returned beside ref (fp64):
+ *   bound(i,j) = 1e-4 * sum_k |alpha*a(i,k)*b(k,j)| + |beta*c(i,j)| * 2^-22
+ * The bf16-output ulp term is a separate function (oracle_ulp_bf16).
+ *
+ * Parity pins: every function here is pinned by tests/test_oracle.py
+ * (identity, permutation, alpha/beta semantics, exact small integers against
+ * Python integers, tiny shapes against exact rationals, MAC count = M*N*K,
+ * bf16 rounding against IEEE round-to-nearest-even).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#ifdef ORACLE_COUNT_MACS
+static int64_t g_mac_count = 0;
+#define COUNT_MAC() __atomic_fetch_add(&g_mac_count, 1, __ATOMIC_RELAXED)
+#else
+#define COUNT_MAC() ((void)0)
+#endif
+
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2, OR_I8 = 3, OR_I32 = 4 };
+enum { OR_ROW_MAJOR = 0, OR_COL_MAJOR = 1 };
+
+/* ---- exact decoding of stored elements ---------------------------------- */
+
+/* bfloat16: the upper 16 bits of an IEEE binary32. */
+static double decode_bf16(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double decode_f16(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0) {
+        v = ldexp((double)m, -24);              /* subnormal: m * 2^-14 * 2^-10 */
+    } else if (e == 31) {
+        v = m ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + m), e - 25);  /* (1 + m/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+static double load_fp(int dtype, const void* p, int64_t idx) {
+    switch (dtype) {
+    case OR_F32: return (double)((const float*)p)[idx];
+    case OR_BF16: return decode_bf16(((const uint16_t*)p)[idx]);
+    case OR_F16: return decode_f16(((const uint16_t*)p)[idx]);
+    default: return NAN;
+    }
+}
+
+static int64_t b_index(int layout_b, int64_t k, int64_t j, int64_t ldb) {
+    return layout_b == OR_COL_MAJOR ? j * ldb + k : k * ldb + j;
+}
+
+/* ---- one output element, floating point --------------------------------- */
+
+static void fp_element(int in_dtype, int out_dtype, int layout_b, int64_t K,
+                       double alpha, const void* A, int64_t lda, const void* B,
+                       int64_t ldb, double beta, const void* C, int64_t ldc,
+                       int64_t i, int64_t j, double* ref, double* bound) {
+    double sum = 0.0, abs_sum = 0.0;
+    if (alpha != 0.0) {
+        for (int64_t k = 0; k < K; ++k) {
+            double a = load_fp(in_dtype, A, i * lda + k);
+            double b = load_fp(in_dtype, B, b_index(layout_b, k, j, ldb));
+            sum += a * b;            /* exact product for fp32/bf16/fp16 inputs */
+            abs_sum += fabs(a * b);
+            COUNT_MAC();
+        }
+    }
+    double cterm = 0.0;
+    if (beta != 0.0) cterm = beta * load_fp(out_dtype, C, i * ldc + j);
+    *ref = alpha * sum + cterm;
+    *bound = 1e-4 * fabs(alpha) * abs_sum + fabs(cterm) * ldexp(1.0, -22);
+}
+
+/* ---- one output element, INT8 x INT8 -> INT32 ---------------------------- */
+
+/* (alpha*sum + beta*c) evaluated in int64, then reduced mod 2^32 to int32
+ * two's complement.  Unsigned arithmetic keeps the wrap well defined. */
+static int32_t i8_element(int layout_b, int64_t K, int32_t alpha,
+                          const int8_t* A, int64_t lda, const int8_t* B,
+                          int64_t ldb, int32_t beta, const int32_t* C,
+                          int64_t ldc, int64_t i, int64_t j) {
+    int64_t sum = 0;
+    if (alpha != 0) {
+        for (int64_t k = 0; k < K; ++k) {
+            sum += (int64_t)A[i * lda + k] * (int64_t)B[b_index(layout_b, k, j, ldb)];
+            COUNT_MAC();
+        }
+    }
+    uint64_t r = (uint64_t)((int64_t)alpha) * (uint64_t)sum;
+    if (beta != 0) r += (uint64_t)((int64_t)beta) * (uint64_t)((int64_t)C[i * ldc + j]);
+    uint32_t low = (uint32_t)r;
+    int32_t out;
+    memcpy(&out, &low, sizeof out);
+    return out;
+}
+
+/* ---- public entry points ------------------------------------------------- */
+
+/* Full matrix, floating-point inputs.  ref and bound are M x N row-major fp64
+ * arrays with leading dimension N.  Returns 0, or -1 on an unsupported dtype. */
+int oracle_gemm_fp(int in_dtype, int out_dtype, int layout_b, int64_t M,
+                   int64_t N, int64_t K, double alpha, const void* A,
+                   int64_t lda, const void* B, int64_t ldb, double beta,
+                   const void* C, int64_t ldc, double* ref, double* bound) {
+    if (in_dtype != OR_F32 && in_dtype != OR_BF16 && in_dtype != OR_F16) return -1;
+    if (out_dtype != OR_F32 && out_dtype != OR_BF16 && out_dtype != OR_F16) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j)
+            fp_element(in_dtype, out_dtype, layout_b, K, alpha, A, lda, B, ldb,
+                       beta, C, ldc, i, j, &ref[i * N + j], &bound[i * N + j]);
+    return 0;
+}
+
+/* Selected elements only: for s < n_samples, element (rows[s], cols[s]). */
+int oracle_gemm_fp_sampled(int in_dtype, int out_dtype, int layout_b, int64_t K,
+                           double alpha, const void* A, int64_t lda,
+                           const void* B, int64_t ldb, double beta,
+                           const void* C, int64_t ldc, int64_t n_samples,
+                           const int64_t* rows, const int64_t* cols,
+                           double* ref, double* bound) {
+    if (in_dtype != OR_F32 && in_dtype != OR_BF16 && in_dtype != OR_F16) return -1;
+    if (out_dtype != OR_F32 && out_dtype != OR_BF16 && out_dtype != OR_F16) return -1;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t s = 0; s < n_samples; ++s)
+        fp_element(in_dtype, out_dtype, layout_b, K, alpha, A, lda, B, ldb,
+                   beta, C, ldc, rows[s], cols[s], &ref[s], &bound[s]);
+    return 0;
+}
+
+/* Full matrix, INT8 inputs, INT32 output (M x N, leading dimension N). */
+int oracle_gemm_i8(int layout_b, int64_t M, int64_t N, int64_t K, int32_t alpha,
+                   const int8_t* A, int64_t lda, const int8_t* B, int64_t ldb,
+                   int32_t beta, const int32_t* C, int64_t ldc, int32_t* out) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j)
+            out[i * N + j] = i8_element(layout_b, K, alpha, A, lda, B, ldb, beta,
+                                        C, ldc, i, j);
+    return 0;
+}
+
+int oracle_gemm_i8_sampled(int layout_b, int64_t K, int32_t alpha,
+                           const int8_t* A, int64_t lda, const int8_t* B,
+                           int64_t ldb, int32_t beta, const int32_t* C,
+                           int64_t ldc, int64_t n_samples, const int64_t* rows,
+                           const int64_t* cols, int32_t* out) {
+#pragma omp parallel for schedule(dynamic, 64)
+    for (int64_t s = 0; s < n_samples; ++s)
+        out[s] = i8_element(layout_b, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                            rows[s], cols[s]);
+    return 0;
+}
+
+/* ---- output rounding ----------------------------------------------------- */
+
+/* Nearest bfloat16 to x, ties to even, per IEEE 754 round-to-nearest-even
+ * applied to a format with 8 significant bits, exponent range [-126, 127]
+ * and subnormal quantum 2^-133.  Returns the 16-bit encoding. */
+uint16_t oracle_round_bf16(double x) {
+    float f;
+    uint32_t u;
+    if (isnan(x)) return 0x7fc0;
+    if (x == 0.0 || isinf(x)) {
+        f = (float)x;                         /* exact: +-0 and +-inf */
+    } else {
+        int e;
+        frexp(fabs(x), &e);                   /* |x| in [2^(e-1), 2^e) */
+        int exp2 = e - 1;                     /* floor(log2|x|) */
+        int q = exp2 < -126 ? -133 : exp2 - 7; /* quantum: 2^(exp - 7) */
+        double scaled = ldexp(x, -q);         /* exact: power-of-two scaling */
+        double n = nearbyint(scaled);         /* ties-to-even (default mode) */
+        double r = ldexp(n, q);
+        const double max_bf16 = ldexp(255.0, 120);   /* (2 - 2^-7) * 2^127 */
+        if (fabs(r) > max_bf16) r = copysign(INFINITY, x);
+        f = (float)r;                         /* exact: r has <= 8 bits */
+    }
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/* One unit in the last place of the bfloat16 value nearest x:
+ * 2^(floor(log2|x|) - 7) in the normal range, 2^-133 below it. */
+double oracle_ulp_bf16(double x) {
+    if (x == 0.0 || !isfinite(x)) return ldexp(1.0, -133);
+    int e;
+    frexp(fabs(x), &e);
+    int exp2 = e - 1;
+    return exp2 < -126 ? ldexp(1.0, -133) : ldexp(1.0, exp2 - 7);
+}
+
+/* Exact decode, exposed so the tests can pin it. */
+double oracle_decode_bf16(uint16_t h) { return decode_bf16(h); }
+double oracle_decode_f16(uint16_t h) { return decode_f16(h); }
+
+/* MAC counter of the instrumented build (-DORACLE_COUNT_MACS); -1 otherwise. */
+int64_t oracle_mac_count(void) {
+#ifdef ORACLE_COUNT_MACS
+    return __atomic_load_n(&g_mac_count, __ATOMIC_RELAXED);
+#else
+    return -1;
+#endif
+}
+
+void oracle_reset_mac_count(void) {
+#ifdef ORACLE_COUNT_MACS
+    __atomic_store_n(&g_mac_count, 0, __ATOMIC_RELAXED);
+#endif
+}
+
+/* Array forms of the rounding helpers (element-wise, same definitions). */
+void oracle_round_bf16_array(const double* x, uint16_t* out, int64_t n) {
+#pragma omp parallel for schedule(static)
+    for (int64_t s = 0; s < n; ++s) out[s] = oracle_round_bf16(x[s]);
+}
+
+void oracle_ulp_bf16_array(const double* x, double* out, int64_t n) {
+#pragma omp parallel for schedule(static)
+    for (int64_t s = 0; s < n; ++s) out[s] = oracle_ulp_bf16(x[s]);
+}

@@ -1,0 +1,339 @@
+"""Pins that tie the CPU oracle to facts outside itself.
+
+Each pin takes an ``oracle.Oracle`` (the real build, or a deliberately broken
+copy in the mutation test) and raises AssertionError when the oracle
+disagrees with what the mathematics or the pages fix:
+
+* identity and permutation matrices (exact results, transposition detected);
+* BLAS alpha/beta semantics (beta == 0 never reads C, alpha == 0 never reads
+  A and B), linearity in alpha;
+* integer-valued inputs against Python integers (exact);
+* tiny random shapes against exact rational arithmetic, within the fp64
+  summation error bound, and the error-bound formula itself;
+* INT8 against Python integers, including wrap-around mod 2**32;
+* the MAC count M*N*K (2MNK FLOPs) of the instrumented build;
+* bf16 decoding and IEEE round-to-nearest-even encoding.
+
+The GEMM definition pinned here is BLAS's C <- alpha*A*B + beta*C, "AI
+Programming: Matrix Product" (elainafan.one), section "Dense matrix
+multiplication"; row-major offsets row*ld + col from its section "Row-major
+order".
+"""
+from __future__ import annotations
+
+import random
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+F32, BF16, F16, I8, I32 = 0, 1, 2, 3, 4
+ROW, COL = 0, 1
+
+
+def _rng(seed):
+    g = torch.Generator().manual_seed(seed)
+    return g
+
+
+def _f32(shape, g):
+    return (torch.rand(shape, generator=g) * 2 - 1).numpy().astype(np.float32)
+
+
+def _bf16_bits(t):
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------- identity --
+
+def pin_identity(o):
+    g = _rng(1)
+    M = K = 23
+    N = 17
+    eye = np.eye(M, dtype=np.float32)
+    B = _f32((K, N), g)
+    C = _f32((M, N), g)
+    alpha, beta = 1.5, -0.5
+    ref, _ = o.gemm_fp(F32, F32, ROW, M, N, K, alpha, eye, K, B, N, beta, C, N)
+    want = alpha * B.astype(np.float64) + beta * C.astype(np.float64)
+    assert np.array_equal(ref, want), "I*B"
+    # B = I: result is alpha*A + beta*C
+    A = _f32((M, K), g)
+    C2 = _f32((M, K), g)
+    ref, _ = o.gemm_fp(F32, F32, ROW, M, K, K, alpha, A, K, np.eye(K, dtype=np.float32), K,
+                       beta, C2, K)
+    want = alpha * A.astype(np.float64) + beta * C2.astype(np.float64)
+    assert np.array_equal(ref, want), "A*I"
+    # bf16 storage: identity picks out the decoded B exactly
+    Bt = torch.randn((K, N), generator=g)
+    eyeb = _bf16_bits(torch.eye(M))
+    ref, _ = o.gemm_fp(BF16, F32, ROW, M, N, K, 1.0, eyeb, K, _bf16_bits(Bt), N, 0.0)
+    assert np.array_equal(ref, Bt.to(torch.bfloat16).double().numpy()), "bf16 I*B"
+
+
+# ------------------------------------------------------------- permutation --
+
+def pin_permutation(o):
+    g = _rng(2)
+    M, K, N = 9, 13, 11
+    perm_rows = torch.randperm(K, generator=g).numpy()
+    P = np.zeros((M, K), np.float32)
+    rows_used = perm_rows[:M]
+    P[np.arange(M), rows_used] = 1.0          # P @ B = B[rows_used]
+    B = _f32((K, N), g)
+    ref, _ = o.gemm_fp(F32, F32, ROW, M, N, K, 1.0, P, K, B, N, 0.0)
+    assert np.array_equal(ref, B[rows_used].astype(np.float64)), "P*B row-major"
+    # same B stored column-major (N x K): must give the same answer
+    Bt = np.ascontiguousarray(B.T)
+    ref_c, _ = o.gemm_fp(F32, F32, COL, M, N, K, 1.0, P, K, Bt, K, 0.0)
+    assert np.array_equal(ref_c, B[rows_used].astype(np.float64)), "P*B column-major"
+    # A @ Q permutes columns: column j of the result is column cols[j] of A
+    cols = torch.randperm(K, generator=g).numpy()[:N]
+    Q = np.zeros((K, N), np.float32)
+    Q[cols, np.arange(N)] = 1.0
+    A = _f32((M, K), g)
+    ref, _ = o.gemm_fp(F32, F32, ROW, M, N, K, 1.0, A, K, Q, N, 0.0)
+    assert np.array_equal(ref, A[:, cols].astype(np.float64)), "A*Q"
+    # leading dimensions larger than the row length
+    lda, ldb = K + 5, N + 3
+    Apad = np.full((M, lda), np.nan, np.float32)
+    Apad[:, :K] = A
+    Qpad = np.full((K, ldb), np.nan, np.float32)
+    Qpad[:, :N] = Q
+    ref, _ = o.gemm_fp(F32, F32, ROW, M, N, K, 1.0, Apad, lda, Qpad, ldb, 0.0)
+    assert np.array_equal(ref, A[:, cols].astype(np.float64)), "padded lda/ldb"
+
+
+# -------------------------------------------------------------- alpha/beta --
+
+def pin_alpha_beta(o):
+    g = _rng(3)
+    M, N, K = 7, 6, 5
+    A = _f32((M, K), g)
+    B = _f32((K, N), g)
+    Cnan = np.full((M, N), np.nan, np.float32)
+    ref, bound = o.gemm_fp(F32, F32, ROW, M, N, K, 1.0, A, K, B, N, 0.0, Cnan, N)
+    assert np.isfinite(ref).all() and np.isfinite(bound).all(), "beta=0 read C"
+    Anan = np.full((M, K), np.nan, np.float32)
+    C = _f32((M, N), g)
+    Bnan = np.full((K, N), np.nan, np.float32)
+    ref, _ = o.gemm_fp(F32, F32, ROW, M, N, K, 0.0, Anan, K, Bnan, N, 2.0, C, N)
+    assert np.array_equal(ref, 2.0 * C.astype(np.float64)), "alpha=0 read A/B"
+    # beta*C with alpha=1, beta=1 on integer data is the exact sum
+    Ai = torch.randint(-4, 5, (M, K), generator=g).numpy().astype(np.float32)
+    Bi = torch.randint(-4, 5, (K, N), generator=g).numpy().astype(np.float32)
+    Ci = torch.randint(-9, 10, (M, N), generator=g).numpy().astype(np.float32)
+    r1, _ = o.gemm_fp(F32, F32, ROW, M, N, K, 1.0, Ai, K, Bi, N, 1.0, Ci, N)
+    r0, _ = o.gemm_fp(F32, F32, ROW, M, N, K, 1.0, Ai, K, Bi, N, 0.0, Ci, N)
+    assert np.array_equal(r1, r0 + Ci), "beta=1 adds C"
+    # linearity in alpha
+    ra, _ = o.gemm_fp(F32, F32, ROW, M, N, K, 3.0, Ai, K, Bi, N, 0.0)
+    rb, _ = o.gemm_fp(F32, F32, ROW, M, N, K, -5.0, Ai, K, Bi, N, 0.0)
+    rab, _ = o.gemm_fp(F32, F32, ROW, M, N, K, -2.0, Ai, K, Bi, N, 0.0)
+    assert np.array_equal(ra + rb, rab), "linearity in alpha"
+
+
+# ------------------------------------------------------- exact small ints --
+
+def _py_gemm(A, B, C, alpha, beta, layout_b):
+    M, K = len(A), len(A[0])
+    N = len(B) if layout_b == COL else len(B[0])
+    out = []
+    for i in range(M):
+        row = []
+        for j in range(N):
+            s = 0
+            for k in range(K):
+                b = B[j][k] if layout_b == COL else B[k][j]
+                s += A[i][k] * b
+            row.append(alpha * s + (beta * C[i][j] if beta else 0))
+        out.append(row)
+    return out
+
+
+def pin_small_integers(o):
+    g = _rng(4)
+    M, N, K = 13, 11, 17
+    for in_dtype in (F32, BF16):
+        for layout in (ROW, COL):
+            A = torch.randint(-4, 5, (M, K), generator=g)
+            Bshape = (N, K) if layout == COL else (K, N)
+            B = torch.randint(-4, 5, Bshape, generator=g)
+            C = torch.randint(-8, 9, (M, N), generator=g)
+            want = _py_gemm(A.tolist(), B.tolist(), C.tolist(), 3, -2, layout)
+            if in_dtype == F32:
+                a, b = A.float().numpy(), B.float().numpy()
+            else:
+                a, b = _bf16_bits(A.float()), _bf16_bits(B.float())
+            ldb = K if layout == COL else N
+            ref, _ = o.gemm_fp(in_dtype, F32, layout, M, N, K, 3.0, a, K, b, ldb, -2.0,
+                               C.float().numpy(), N)
+            assert np.array_equal(ref, np.array(want, np.float64)), (in_dtype, layout)
+
+
+def pin_int8(o):
+    g = _rng(5)
+    M, N, K = 9, 10, 37
+    for layout in (ROW, COL):
+        A = torch.randint(-128, 128, (M, K), generator=g, dtype=torch.int8)
+        Bshape = (N, K) if layout == COL else (K, N)
+        B = torch.randint(-128, 128, Bshape, generator=g, dtype=torch.int8)
+        C = torch.randint(-2**31, 2**31, (M, N), generator=g, dtype=torch.int64).to(torch.int32)
+        ldb = K if layout == COL else N
+        for alpha, beta in ((1, 0), (-3, 7), (1 << 20, 1 << 30), (0, -1)):
+            got = o.gemm_i8(layout, M, N, K, alpha, A.numpy(), K, B.numpy(), ldb, beta,
+                            C.numpy(), N)
+            want = _py_gemm(A.tolist(), B.tolist(), C.tolist(), alpha, beta, layout)
+            wrapped = [[((v + 2**31) % 2**32) - 2**31 for v in row] for row in want]
+            assert np.array_equal(got, np.array(wrapped, np.int64)), (layout, alpha, beta)
+        # leading dimensions larger than the row length, padding full of junk
+        lda, ldb_p = K + 3, ldb + 5
+        Ap = torch.randint(-128, 128, (M, lda), generator=g, dtype=torch.int8)
+        Ap[:, :K] = A
+        Bp = torch.randint(-128, 128, (Bshape[0], ldb_p), generator=g, dtype=torch.int8)
+        Bp[:, :Bshape[1]] = B
+        got = o.gemm_i8(layout, M, N, K, 1, Ap.numpy(), lda, Bp.numpy(), ldb_p)
+        want = _py_gemm(A.tolist(), B.tolist(), C.tolist(), 1, 0, layout)
+        assert np.array_equal(got, np.array(want, np.int64)), ("padded", layout)
+        # all -128: the largest magnitude products
+        Am = torch.full((2, 64), -128, dtype=torch.int8)
+        Bm = torch.full((64, 3) if layout == ROW else (3, 64), -128, dtype=torch.int8)
+        got = o.gemm_i8(layout, 2, 3, 64, 1, Am.numpy(), 64, Bm.numpy(),
+                        3 if layout == ROW else 64)
+        assert (got == 64 * 16384).all()
+
+
+# ------------------------------------------------- rationals on tiny shapes --
+
+def pin_tiny_rational(o):
+    rnd = random.Random(6)
+    u = Fraction(1, 2**53)
+    for trial in range(60):
+        M, N, K = rnd.randint(1, 8), rnd.randint(1, 8), rnd.randint(1, 8)
+        layout = rnd.choice((ROW, COL))
+        # float32 values with spread exponents, so roundings really happen
+        def val():
+            return np.float32(rnd.uniform(-1, 1) * 2.0 ** rnd.randint(-20, 20))
+        A = np.array([[val() for _ in range(K)] for _ in range(M)], np.float32)
+        Bshape = (N, K) if layout == COL else (K, N)
+        B = np.array([[val() for _ in range(Bshape[1])] for _ in range(Bshape[0])], np.float32)
+        C = np.array([[val() for _ in range(N)] for _ in range(M)], np.float32)
+        alpha = float(np.float32(rnd.uniform(-2, 2)))
+        beta = rnd.choice((0.0, float(np.float32(rnd.uniform(-2, 2)))))
+        ldb = K if layout == COL else N
+        ref, bound = o.gemm_fp(F32, F32, layout, M, N, K, alpha, A, K, B, ldb, beta, C, N)
+        for i in range(M):
+            for j in range(N):
+                terms = []
+                for k in range(K):
+                    b = B[j, k] if layout == COL else B[k, j]
+                    terms.append(Fraction(float(A[i, k])) * Fraction(float(b)))
+                s = sum(terms, Fraction(0))
+                fa, fb = Fraction(alpha), Fraction(beta)
+                cterm = fb * Fraction(float(C[i, j])) if beta != 0 else Fraction(0)
+                exact = fa * s + cterm
+                abs_terms = sum((abs(t) for t in terms), Fraction(0))
+                mag = abs(fa) * abs_terms + abs(cterm)
+                n = K + 2
+                gamma = n * u / (1 - n * u)
+                err = abs(Fraction(float(ref[i, j])) - exact)
+                assert err <= gamma * mag + Fraction(2) ** -1074, (trial, i, j)
+                want_bound = Fraction(1, 10**4) * abs(fa) * abs_terms + abs(cterm) * Fraction(1, 2**22)
+                assert abs(Fraction(float(bound[i, j])) - want_bound) <= 8 * u * want_bound + \
+                    Fraction(2) ** -1074, ("bound", trial, i, j)
+
+
+# --------------------------------------------------------------- MAC count --
+
+def pin_mac_count(o_counting):
+    g = _rng(7)
+    for (M, N, K) in ((3, 5, 7), (16, 1, 33), (1, 9, 1)):
+        A = _f32((M, K), g)
+        B = _f32((K, N), g)
+        o_counting.reset_mac_count()
+        o_counting.gemm_fp(F32, F32, ROW, M, N, K, 1.0, A, K, B, N, 0.0)
+        assert o_counting.mac_count() == M * N * K, (M, N, K)
+        Ai = np.zeros((M, K), np.int8)
+        Bi = np.zeros((K, N), np.int8)
+        o_counting.reset_mac_count()
+        o_counting.gemm_i8(ROW, M, N, K, 1, Ai, K, Bi, N)
+        assert o_counting.mac_count() == M * N * K
+    o_counting.reset_mac_count()
+    o_counting.gemm_fp(F32, F32, ROW, 4, 4, 4, 0.0, np.zeros((4, 4), np.float32), 4,
+                       np.zeros((4, 4), np.float32), 4, 0.0)
+    assert o_counting.mac_count() == 0, "alpha=0 must not multiply"
+
+
+# ------------------------------------------------------------------- bf16 --
+
+def _bf16_value(bits):
+    """Value of a bf16 encoding from the IEEE definition (sign, 8-bit
+    exponent with bias 127, 7 fraction bits), as an exact Fraction."""
+    s = -1 if bits >> 15 else 1
+    e = (bits >> 7) & 0xFF
+    m = bits & 0x7F
+    if e == 0:
+        return s * Fraction(m, 2**7) * Fraction(2) ** -126
+    return s * (1 + Fraction(m, 2**7)) * Fraction(2) ** (e - 127)
+
+
+def pin_bf16_decode(o):
+    bits = np.arange(0, 1 << 16, 97, dtype=np.uint16)
+    got = o.decode_bf16(bits)
+    for b, v in zip(bits.tolist(), got.tolist()):
+        e = (b >> 7) & 0xFF
+        if e == 0xFF:
+            if b & 0x7F:
+                assert v != v
+            else:
+                assert v == (float("-inf") if b >> 15 else float("inf"))
+        else:
+            assert Fraction(v) == _bf16_value(b), hex(b)
+
+
+def pin_f16_decode(o):
+    bits = np.arange(0, 1 << 16, 61, dtype=np.uint16)
+    got = o.decode_f16(bits)
+    want = torch.from_numpy(bits.view(np.int16)).view(torch.float16).double().numpy()
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    assert same.all()
+
+
+def pin_bf16_round(o):
+    # hand cases from round-to-nearest-even on 8 significant bits
+    cases = [
+        (1.0, 0x3F80),
+        (1.0 + 2.0**-8, 0x3F80),            # tie -> even mantissa (0)
+        (1.0 + 3 * 2.0**-8, 0x3F82),        # tie -> even mantissa (2)
+        (1.0 + 2.0**-8 + 2.0**-30, 0x3F81),  # just above the tie
+        (-1.5, 0xBFC0),
+        (2.0**-133, 0x0001),                # smallest subnormal
+        (2.0**-134, 0x0000),                # tie between 0 and 2^-133 -> 0
+        (3 * 2.0**-134, 0x0002),            # tie between 1 and 2 quanta -> 2
+        ((2 - 2.0**-7) * 2.0**127, 0x7F7F),  # largest finite
+        ((2 - 2.0**-8) * 2.0**127, 0x7F80),  # tie with 2^128 -> overflow to inf
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+    ]
+    got = o.round_bf16(np.array([x for x, _ in cases], np.float64))
+    for (x, want), g in zip(cases, got.tolist()):
+        assert g == want, (x, hex(g), hex(want))
+    # agreement with torch's float32 -> bf16 round-to-nearest-even on many values
+    g = _rng(8)
+    x = torch.randn(20000, generator=g) * torch.exp2(torch.randint(-140, 128, (20000,),
+                                                                  generator=g).float())
+    x = x[torch.isfinite(x)]
+    want = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = o.round_bf16(x.double().numpy())
+    assert np.array_equal(got, want)
+
+
+def pin_ulp_bf16(o):
+    cases = {1.0: 2.0**-7, 1.5: 2.0**-7, -3.0: 2.0**-6, 2.0**-126: 2.0**-133,
+             3 * 2.0**-130: 2.0**-133, 2.0**127: 2.0**120, 0.0: 2.0**-133}
+    got = o.ulp_bf16(np.array(list(cases.keys())))
+    assert np.array_equal(got, np.array(list(cases.values())))
+
+
+ALL_PINS = [pin_identity, pin_permutation, pin_alpha_beta, pin_small_integers, pin_int8,
+            pin_tiny_rational, pin_bf16_decode, pin_f16_decode, pin_bf16_round, pin_ulp_bf16]

@@ -1,0 +1,84 @@
+"""Each plausible mistake planted in a copy of the oracle fails some pin.
+
+The mistakes are planted on the CPU, in a temporary copy of the oracle's C
+source; the real oracle is untouched.  A mutant that every pin accepted would
+mean the pins cannot see that class of bug.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+from tests import oracle_pins
+
+# (name, text in gemm_oracle.c, replacement, occurrence index)
+MUTANTS = [
+    ("b_layout_swapped", "j * ldb + k : k * ldb + j", "k * ldb + j : j * ldb + k", 0),
+    ("beta_term_dropped", "cterm = beta * load_fp(out_dtype, C, i * ldc + j);", "cterm = 0.0 * beta;", 0),
+    ("alpha_scales_c", "*ref = alpha * sum + cterm;", "*ref = alpha * (sum + cterm);", 0),
+    ("k_loop_short_fp", "for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 0; k + 1 < K; ++k) {", 0),
+    ("k_loop_short_i8", "for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 0; k + 1 < K; ++k) {", 1),
+    ("product_sign", "sum += a * b;", "sum -= a * b;", 0),
+    ("bf16_decode_shift", "((uint32_t)h) << 16", "((uint32_t)h) << 15", 0),
+    ("round_ties_away", "nearbyint(scaled)", "round(scaled)", 0),
+    ("i8_beta_dropped", "if (beta != 0) r +=", "if (0) r +=", 0),
+    ("bound_without_alpha", "1e-4 * fabs(alpha) * abs_sum", "1e-4 * abs_sum", 0),
+    ("ulp_one_bit_off", "ldexp(1.0, exp2 - 7)", "ldexp(1.0, exp2 - 8)", 0),
+    ("f16_bias", "e - 25);", "e - 24);", 0),
+    ("beta_zero_reads_c", "if (beta != 0.0) cterm", "if (1) cterm", 0),
+    ("alpha_zero_reads_ab", "if (alpha != 0.0) {", "if (1) {", 0),
+    ("lda_ignored", "load_fp(in_dtype, A, i * lda + k)", "load_fp(in_dtype, A, i * K + k)", 0),
+    ("i8_lda_ignored", "A[i * lda + k]", "A[i * K + k]", 0),
+]
+
+
+def _replace_nth(text, old, new, n):
+    idx = -1
+    for _ in range(n + 1):
+        idx = text.index(old, idx + 1)
+    return text[:idx] + new + text[idx + len(old):]
+
+
+_RUNNER = """
+import sys
+sys.path.insert(0, {root!r})
+import oracle
+from tests import oracle_pins
+plain = oracle.Oracle({plain!r})
+counting = oracle.Oracle({counting!r})
+failures = []
+for pin in oracle_pins.ALL_PINS:
+    try:
+        pin(plain)
+    except Exception:
+        failures.append(pin.__name__)
+try:
+    oracle_pins.pin_mac_count(counting)
+except Exception:
+    failures.append("pin_mac_count")
+print("FAILED_PINS", failures)
+sys.exit(1 if failures else 0)
+"""
+
+
+@pytest.mark.parametrize("name,old,new,nth", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, nth, tmp_path):
+    src = open(oracle.SOURCE).read()
+    mutated = _replace_nth(src, old, new, nth)
+    assert mutated != src
+    path = tmp_path / f"{name}.c"
+    path.write_text(mutated)
+    plain = str(tmp_path / f"lib{name}.so")
+    counting = str(tmp_path / f"lib{name}_count.so")
+    oracle.build_variant(str(path), plain)
+    oracle.build_variant(str(path), counting, ("ORACLE_COUNT_MACS",))
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    # a child process, so that a mutant that crashes (e.g. reads C through a
+    # null pointer when beta == 0) also counts as caught
+    proc = subprocess.run([sys.executable, "-c", _RUNNER.format(root=root, plain=plain,
+                                                                counting=counting)],
+                          capture_output=True, text=True, timeout=600,
+                          env={**os.environ, "OMP_NUM_THREADS": "2"})
+    assert proc.returncode != 0, f"mutant {name} passed every pin"
