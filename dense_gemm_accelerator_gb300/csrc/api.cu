@@ -1,0 +1,290 @@
+// api.cu -- the C ABI of include/dga.h: argument checks, path selection, and
+// the launch of the chosen kernel family on the caller's stream.
+//
+// The operation is BLAS GEMM, C <- alpha*A*B + beta*C ("AI Programming:
+// Matrix Product", section "Dense matrix multiplication"), with row-major
+// offsets row*ld + col (section "Row-major order").  BLAS conventions decide
+// what the pages leave open: M == 0 or N == 0 is a no-op, K == 0 or
+// alpha == 0 reads neither A nor B, beta == 0 never reads C, and invalid
+// arguments are reported as -(their 1-based position).
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "dga_internal.h"
+
+namespace dga {
+namespace {
+
+thread_local int t_last_path = DGA_PATH_AUTO;
+thread_local int t_last_launches = 0;
+thread_local int t_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::once_flag g_dev_once[kMaxDevices];
+cudaError_t g_dev_err[kMaxDevices];
+
+bool pair_supported(int in, int out) {
+    return (in == DGA_F32 && out == DGA_F32) || (in == DGA_BF16 && (out == DGA_F32 || out == DGA_BF16)) ||
+           (in == DGA_F16 && (out == DGA_F32 || out == DGA_F16)) || (in == DGA_I8 && out == DGA_I32);
+}
+
+size_t elem_size(int dt) {
+    switch (dt) {
+    case DGA_F32: case DGA_I32: return 4;
+    case DGA_BF16: case DGA_F16: return 2;
+    case DGA_I8: return 1;
+    default: return 0;
+    }
+}
+
+// Byte range [lo, hi) that a rows x cols matrix with row stride ld occupies.
+void span(const void* p, int64_t rows, int64_t cols, int64_t ld, size_t es, uintptr_t* lo,
+          uintptr_t* hi) {
+    *lo = reinterpret_cast<uintptr_t>(p);
+    *hi = *lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * static_cast<int64_t>(es));
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+// Validates everything but the pointers' alignment; fills *g.  Without
+// `with_pointers` (size queries), matrix pointers are neither required nor
+// checked for overlap.
+int check_args(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M, int64_t N,
+               int64_t K, const void* alpha, const void* A, int64_t lda, const void* B,
+               int64_t ldb, const void* beta, void* C, int64_t ldc, void* ws, size_t ws_bytes,
+               GemmArgs* g, bool with_pointers = true) {
+    if (in_dtype < DGA_F32 || in_dtype > DGA_I32 || out_dtype < DGA_F32 || out_dtype > DGA_I32)
+        return DGA_ERR_UNSUPPORTED;
+    if (layout_b != DGA_ROW_MAJOR && layout_b != DGA_COL_MAJOR) return DGA_ERR_UNSUPPORTED;
+    if (!pair_supported(in_dtype, out_dtype)) return DGA_ERR_UNSUPPORTED;
+    if (M < 0) return -4;
+    if (N < 0) return -5;
+    if (K < 0) return -6;
+    if (!alpha) return -7;
+    if (!beta) return -12;
+    g->in_dtype = in_dtype;
+    g->out_dtype = out_dtype;
+    g->layout_b = layout_b;
+    g->M = M;
+    g->N = N;
+    g->K = K;
+    if (in_dtype == DGA_I8) {
+        std::memcpy(&g->alpha_i, alpha, sizeof(int32_t));
+        std::memcpy(&g->beta_i, beta, sizeof(int32_t));
+        g->alpha_f = static_cast<float>(g->alpha_i);
+        g->beta_f = static_cast<float>(g->beta_i);
+    } else {
+        std::memcpy(&g->alpha_f, alpha, sizeof(float));
+        std::memcpy(&g->beta_f, beta, sizeof(float));
+        g->alpha_i = 0;
+        g->beta_i = 0;
+    }
+    const bool reads_ab = with_pointers && M > 0 && N > 0 && K > 0 && !alpha_is_zero(*g);
+    if (reads_ab && !A) return -8;
+    if (lda < (K > 1 ? K : 1)) return -9;
+    if (reads_ab && !B) return -10;
+    const int64_t min_ldb = layout_b == DGA_ROW_MAJOR ? (N > 1 ? N : 1) : (K > 1 ? K : 1);
+    if (ldb < min_ldb) return -11;
+    if (with_pointers && M > 0 && N > 0 && !C) return -13;
+    if (ldc < (N > 1 ? N : 1)) return -14;
+    if (ws_bytes > 0 && !ws) return -15;
+    g->A = A;
+    g->lda = lda;
+    g->B = B;
+    g->ldb = ldb;
+    g->C = C;
+    g->ldc = ldc;
+    g->ws = ws;
+    g->ws_bytes = ws_bytes;
+    if (with_pointers && M > 0 && N > 0) {
+        uintptr_t c0, c1;
+        span(C, M, N, ldc, elem_size(out_dtype), &c0, &c1);
+        if (reads_ab) {
+            uintptr_t a0, a1, b0, b1;
+            span(A, M, K, lda, elem_size(in_dtype), &a0, &a1);
+            if (layout_b == DGA_ROW_MAJOR) span(B, K, N, ldb, elem_size(in_dtype), &b0, &b1);
+            else span(B, N, K, ldb, elem_size(in_dtype), &b0, &b1);
+            if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return DGA_ERR_OVERLAP;
+        }
+    }
+    return DGA_OK;
+}
+
+// AUTO: the fastest family that accepts the arguments.
+int choose_path(const GemmArgs& g) {
+    if (g.K == 0 || alpha_is_zero(g)) return DGA_PATH_GENERIC;  // C <- beta*C only
+    if (g.in_dtype == DGA_F32) return simt_supports(g) ? DGA_PATH_SIMT : DGA_PATH_GENERIC;
+    if (g.in_dtype == DGA_BF16 || g.in_dtype == DGA_F16) {
+        if (skinny_supports(g)) return DGA_PATH_SKINNY;
+        if (tc_supports(g)) return DGA_PATH_TCGEN05;
+        return DGA_PATH_GENERIC;
+    }
+    if (g.in_dtype == DGA_I8) return tc_supports(g) ? DGA_PATH_TCGEN05 : DGA_PATH_GENERIC;
+    return DGA_PATH_GENERIC;
+}
+
+bool path_accepts(int path, const GemmArgs& g) {
+    const bool no_product = g.K == 0 || alpha_is_zero(g);
+    switch (path) {
+    case DGA_PATH_GENERIC: return generic_supports(g);
+    case DGA_PATH_SIMT: return !no_product && simt_supports(g);
+    case DGA_PATH_TCGEN05: return !no_product && tc_supports(g);
+    case DGA_PATH_SKINNY: return !no_product && skinny_supports(g);
+    default: return false;
+    }
+}
+
+size_t workspace_for(int path, const GemmArgs& g) {
+    return path == DGA_PATH_TCGEN05 ? tc_workspace_size(g) : 0;
+}
+
+int fail_cuda(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return DGA_ERR_CUDA;
+}
+
+}  // namespace
+
+cudaError_t current_device_info(DeviceInfo* out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::call_once(g_dev_once[dev], [dev] {
+        DeviceInfo d{};
+        d.ordinal = dev;
+        cudaError_t err = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (err == cudaSuccess) err = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (err == cudaSuccess) err = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (err == cudaSuccess)
+            err = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        g_dev[dev] = d;
+        g_dev_err[dev] = err;
+    });
+    *out = g_dev[dev];
+    return g_dev_err[dev];
+}
+
+}  // namespace dga
+
+using namespace dga;
+
+extern "C" {
+
+int dga_gemm_ex(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M, int64_t N,
+                int64_t K, const void* alpha, const void* A, int64_t lda, const void* B,
+                int64_t ldb, const void* beta, void* C, int64_t ldc, void* workspace,
+                size_t workspace_bytes, dga_path path, dga_stream_t stream) {
+    if (path < DGA_PATH_AUTO || path > DGA_PATH_SKINNY) return -17;
+    GemmArgs g{};
+    int st = check_args(in_dtype, out_dtype, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                        ldc, workspace, workspace_bytes, &g);
+    if (st != DGA_OK) return st;
+    g.stream = reinterpret_cast<cudaStream_t>(stream);
+    t_last_path = DGA_PATH_AUTO;
+    t_last_launches = 0;
+    if (M == 0 || N == 0) return DGA_OK;
+
+    DeviceInfo dev;
+    cudaError_t e = current_device_info(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev.major != 10 || dev.minor != 3) return DGA_ERR_DEVICE;
+
+    const int chosen = path == DGA_PATH_AUTO ? choose_path(g) : static_cast<int>(path);
+    if (!path_accepts(chosen, g)) return DGA_ERR_PATH;
+    if (workspace_bytes < workspace_for(chosen, g)) return DGA_ERR_WORKSPACE;
+
+    int launches = 0;
+    switch (chosen) {
+    case DGA_PATH_GENERIC: e = generic_launch(g, &launches); break;
+    case DGA_PATH_SIMT: e = simt_launch(g, &launches); break;
+    case DGA_PATH_SKINNY: e = skinny_launch(g, &launches); break;
+    case DGA_PATH_TCGEN05: e = tc_launch(g, dev, &launches); break;
+    default: return DGA_ERR_PATH;
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_path = chosen;
+    t_last_launches = launches;
+    return DGA_OK;
+}
+
+int dga_gemm(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M, int64_t N,
+             int64_t K, const void* alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
+             const void* beta, void* C, int64_t ldc, void* workspace, size_t workspace_bytes,
+             dga_stream_t stream) {
+    return dga_gemm_ex(in_dtype, out_dtype, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                       workspace, workspace_bytes, DGA_PATH_AUTO, stream);
+}
+
+size_t dga_gemm_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
+                               int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                               int64_t ldc, dga_path path) {
+    GemmArgs g{};
+    const float one = 1.0f;
+    const int32_t one_i = 1;
+    const void* alpha = in_dtype == DGA_I8 ? static_cast<const void*>(&one_i) : &one;
+    if (check_args(in_dtype, out_dtype, layout_b, M, N, K, alpha, nullptr, lda, nullptr, ldb,
+                   alpha, nullptr, ldc, nullptr, 0, &g, /*with_pointers=*/false) != DGA_OK)
+        return 0;
+    if (M == 0 || N == 0 || K == 0) return 0;
+    // Pointer-free query: operands are assumed 16-byte aligned.
+    static const char aligned16[16] __attribute__((aligned(16))) = {};
+    int chosen = static_cast<int>(path);
+    if (path == DGA_PATH_AUTO) {
+        GemmArgs probe = g;
+        probe.A = aligned16;
+        probe.B = aligned16;
+        chosen = choose_path(probe);
+    }
+    return workspace_for(chosen, g);
+}
+
+int dga_select_path(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M,
+                    int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
+                    const void* C, int64_t ldc) {
+    GemmArgs g{};
+    const float one = 1.0f;
+    const int32_t one_i = 1;
+    const void* alpha = in_dtype == DGA_I8 ? static_cast<const void*>(&one_i) : &one;
+    int st = check_args(in_dtype, out_dtype, layout_b, M, N, K, alpha, A, lda, B, ldb, alpha,
+                        const_cast<void*>(C), ldc, nullptr, 0, &g);
+    if (st != DGA_OK) return st < 0 ? st : -st;
+    return choose_path(g);
+}
+
+int dga_last_path(void) { return t_last_path; }
+
+int dga_last_launch_count(void) { return t_last_launches; }
+
+int dga_sync_status(dga_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e);
+    int st = 0;
+    e = tc_status_take(&st);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return st != 0 ? DGA_ERR_DEVICE_TIMEOUT : DGA_OK;
+}
+
+int dga_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char* dga_status_string(int status) {
+    if (status < 0) return "invalid argument (the negated value is its 1-based position)";
+    switch (status) {
+    case DGA_OK: return "ok";
+    case DGA_ERR_UNSUPPORTED: return "unsupported dtype pair or layout";
+    case DGA_ERR_CUDA: return "a CUDA call failed";
+    case DGA_ERR_DEVICE_TIMEOUT: return "a kernel's bounded wait expired";
+    case DGA_ERR_PATH: return "the forced kernel family cannot run these arguments";
+    case DGA_ERR_WORKSPACE: return "workspace smaller than dga_gemm_workspace_size()";
+    case DGA_ERR_OVERLAP: return "C overlaps A or B";
+    case DGA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    default: return "unknown status";
+    }
+}
+
+int dga_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,68 @@
+// dga_internal.h -- host-side declarations shared by the library's
+// translation units (one per kernel family) and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "dga.h"
+
+namespace dga {
+
+// One validated GEMM call.  alpha/beta are kept both as float (floating-point
+// inputs) and as int32 (INT8 inputs); only the one matching in_dtype is used.
+struct GemmArgs {
+    int in_dtype, out_dtype, layout_b;
+    int64_t M, N, K;
+    float alpha_f, beta_f;
+    int32_t alpha_i, beta_i;
+    const void* A;
+    int64_t lda;
+    const void* B;
+    int64_t ldb;
+    void* C;
+    int64_t ldc;
+    void* ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+struct DeviceInfo {
+    int ordinal;
+    int sm_count;
+    int major, minor;
+    int max_smem_optin;  // bytes of dynamic shared memory one block may opt into
+};
+
+// Properties of the current device (queried once per device).
+cudaError_t current_device_info(DeviceInfo* out);
+
+inline bool aligned(const void* p, size_t bytes) {
+    return (reinterpret_cast<uintptr_t>(p) % bytes) == 0;
+}
+
+inline bool alpha_is_zero(const GemmArgs& a) {
+    return a.in_dtype == DGA_I8 ? a.alpha_i == 0 : a.alpha_f == 0.0f;
+}
+
+// ---- kernel families: supports() says whether the family can run the
+// arguments; launch() enqueues its kernels and adds their count to *launches.
+
+bool generic_supports(const GemmArgs& a);
+cudaError_t generic_launch(const GemmArgs& a, int* launches);
+
+bool simt_supports(const GemmArgs& a);
+cudaError_t simt_launch(const GemmArgs& a, int* launches);
+
+bool skinny_supports(const GemmArgs& a);
+cudaError_t skinny_launch(const GemmArgs& a, int* launches);
+
+bool tc_supports(const GemmArgs& a);
+size_t tc_workspace_size(const GemmArgs& a);
+cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);
+// Reads and clears this device's tcgen05 status word (non-zero: a wait expired).
+cudaError_t tc_status_take(int* status);
+
+}  // namespace dga

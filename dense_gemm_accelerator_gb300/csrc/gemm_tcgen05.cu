@@ -1,0 +1,639 @@
+// gemm_tcgen05.cu -- GEMM on the 5th-generation tensor cores of sm_103a.
+//
+// What it computes: C <- alpha * A * B + beta * C with bf16 or fp16 inputs,
+// fp32 accumulation and fp32 / bf16 / fp16 output -- the Tensor Core
+// precision rows (BF16 / FP16 inputs, FP32 accumulate) of "Matrix
+// multiplication: arithmetic intensity, tiling and Tensor Core", section
+// 5.5.  The pages' own tensor-core kernels are WMMA 16x16x16 warp tiles on
+// A100/H100; this one is built for Blackwell instead:
+//
+//   * One persistent CTA per SM walks output tiles of 128 x 256 in a grouped
+//     order (16 tile-rows at a time) so that concurrently running tiles share
+//     A and B panels in L2.
+//   * Warp 0 (one lane) is the TMA producer: 2-D tensor-map loads of a
+//     128 x 64 A box and a 256 x 64 B box (64 bf16 = one 128-byte swizzle
+//     row) into a 4-stage shared-memory ring, each stage guarded by a
+//     "full" and an "empty" mbarrier.  Out-of-range rows and the K tail are
+//     filled with zeros by the TMA unit, which is the zero-fill edge rule of
+//     "AI Programming: Matrix Product", section "Shared Memory Tiling".
+//   * Warp 1 (one lane) issues tcgen05.mma (M = 128, N = 256, K = 16; four per
+//     stage) into an fp32 accumulator in tensor memory, and tcgen05.commit to
+//     release each stage and, after the last K block, the accumulator.
+//   * Warps 2-5 are the epilogue: tcgen05.ld moves the accumulator to
+//     registers, 32 columns at a time, for the fused alpha/beta update and the
+//     masked store.  TMEM holds two accumulators (2 x 256 of its 512
+//     columns), so the epilogue of tile i overlaps the main loop of tile i+1.
+//   * Every wait is bounded in time; a wait that expires records a code in a
+//     per-device status word, tells the other roles to stop, and the CTA
+//     drains its outstanding copies and MMAs and frees its TMEM before
+//     returning (read with dga_sync_status()).
+//
+// Operands reach the kernel K-major (A row-major, B column-major).  Other
+// layouts -- row-major B, a leading dimension TMA cannot express, or INT8
+// inputs (encoded exactly as bf16, see below) -- are first repacked into the
+// caller's workspace by pack_kmajor_kernel.
+//
+// INT8 x INT8 -> INT32 (tcgen05 has no integer MMA on sm_103a: ptxas rejects
+// kind::i8 for this target).  Every int8 value is an exact bf16, every
+// product of two is an integer of magnitude <= 2^14, and the tensor core
+// accumulates in fp32.  The K loop is cut into chunks of 512: within a chunk
+// every partial sum is an integer of magnitude <= 512 * 2^14 = 2^23, which
+// fp32 represents exactly, so each chunk's fp32 accumulator is the exact
+// integer chunk sum.  The epilogue converts each chunk result to int32 and
+// adds it into int32 registers (two's-complement wrap), so the final sum is
+// exact for any K.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "dga_internal.h"
+#include "epilogue.cuh"
+#include "ptx.cuh"
+
+namespace dga {
+
+__device__ int g_tc_status;  // non-zero: a bounded wait expired (role code)
+
+namespace {
+
+constexpr int BM = 128;  // tile rows (UMMA M)
+constexpr int BK = 64;   // K per stage: 64 x 2 bytes = one 128-byte swizzle row
+constexpr int UK = 16;   // K per tcgen05.mma (kind::f16)
+constexpr int kStages = 4;
+constexpr int kGroupM = 16;  // tile-rows per raster group
+constexpr int kI8ChunkBlocks = 8;  // INT8: K blocks per exact fp32 chunk (8 x 64 = 512)
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
+
+enum : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
+
+struct TcParams {
+    int64_t M, N, K;
+    void* C;
+    int64_t ldc;
+    float alpha, beta;
+    int32_t alpha_i, beta_i;
+    int vec_c;  // C 16-byte aligned and ldc a multiple of 16 bytes
+    uint32_t tiles_m, tiles_n, num_tiles, num_kb;
+};
+
+// Shared-memory plan (dynamic, 1024-byte aligned): the stage ring, then the
+// barriers.  BN is 256 for floating point, 256 for INT8 too (the epilogue
+// then uses 8 warps, each owning half of the columns).
+template <int BN>
+struct Smem {
+    static constexpr uint32_t kABytes = BM * BK * 2;
+    static constexpr uint32_t kBBytes = BN * BK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kRing = kStages * kStageBytes;
+    static constexpr uint32_t kBarOffset = kRing;
+    // full[S], empty[S], acc_full[2], acc_empty[2], drain, then tmem slot + abort flag
+    static constexpr uint32_t kTotal = kRing + (2 * kStages + 5) * 8 + 16;
+    static constexpr uint32_t kLaunchBytes = kTotal + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ void tile_coords(uint32_t t, const TcParams& p, uint32_t& tm,
+                                            uint32_t& tn) {
+    const uint32_t group_size = kGroupM * p.tiles_n;
+    const uint32_t group = t / group_size;
+    const uint32_t first_m = group * kGroupM;
+    const uint32_t gm = min(p.tiles_m - first_m, static_cast<uint32_t>(kGroupM));
+    const uint32_t r = t % group_size;
+    tm = first_m + r % gm;
+    tn = r / gm;
+}
+
+__device__ __forceinline__ void record_failure(int role, volatile int* abort_flag) {
+    atomicCAS(&g_tc_status, 0, role);
+    *abort_flag = 1;
+}
+
+// ---- epilogue stores ---------------------------------------------------------
+
+template <typename TOut>
+__device__ __forceinline__ void store_row_chunk(const TcParams& p, int64_t row, int64_t col,
+                                                const float (&v)[32]) {
+    TOut* crow = static_cast<TOut*>(p.C) + row * p.ldc;
+    if (p.vec_c && col + 31 < p.N) {
+        if constexpr (sizeof(TOut) == 4) {
+            float4* dst = reinterpret_cast<float4*>(crow + col);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.beta != 0.0f) o = dst[q];
+                o.x = axpby(p.alpha, v[4 * q + 0], p.beta, o.x);
+                o.y = axpby(p.alpha, v[4 * q + 1], p.beta, o.y);
+                o.z = axpby(p.alpha, v[4 * q + 2], p.beta, o.z);
+                o.w = axpby(p.alpha, v[4 * q + 3], p.beta, o.w);
+                dst[q] = o;
+            }
+        } else {
+            // 16-bit outputs: 8 elements per 16-byte store
+            uint4* dst = reinterpret_cast<uint4*>(crow + col);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 raw = make_uint4(0, 0, 0, 0);
+                if (p.beta != 0.0f) raw = dst[q];
+                TOut* tmp = reinterpret_cast<TOut*>(&raw);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    float old = p.beta != 0.0f ? OutT<TOut>::load(&tmp[j]) : 0.0f;
+                    OutT<TOut>::store(&tmp[j], axpby(p.alpha, v[8 * q + j], p.beta, old));
+                }
+                dst[q] = raw;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (col + j < p.N) {
+                float old = p.beta != 0.0f ? OutT<TOut>::load(crow + col + j) : 0.0f;
+                OutT<TOut>::store(crow + col + j, axpby(p.alpha, v[j], p.beta, old));
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void store_row_chunk_i32(const TcParams& p, int64_t row, int64_t col,
+                                                    const int32_t (&v)[32]) {
+    int32_t* crow = static_cast<int32_t*>(p.C) + row * p.ldc;
+    if (p.vec_c && col + 31 < p.N) {
+        int4* dst = reinterpret_cast<int4*>(crow + col);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            int4 o = make_int4(0, 0, 0, 0);
+            if (p.beta_i != 0) o = dst[q];
+            o.x = axpby_i32(p.alpha_i, v[4 * q + 0], p.beta_i, o.x);
+            o.y = axpby_i32(p.alpha_i, v[4 * q + 1], p.beta_i, o.y);
+            o.z = axpby_i32(p.alpha_i, v[4 * q + 2], p.beta_i, o.z);
+            o.w = axpby_i32(p.alpha_i, v[4 * q + 3], p.beta_i, o.w);
+            dst[q] = o;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (col + j < p.N) {
+                int32_t old = p.beta_i != 0 ? crow[col + j] : 0;
+                crow[col + j] = axpby_i32(p.alpha_i, v[j], p.beta_i, old);
+            }
+        }
+    }
+}
+
+// ---- the kernel ----------------------------------------------------------------
+//
+// kI8: INT8 mode (bf16-encoded operands, chunked exact accumulation, int32 out).
+// BN: tile columns.  Epilogue warps: 4 (float) or 8 (INT8: two column halves).
+
+template <bool kBf16, bool kI8, int BN, typename TOut>
+__global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   TcParams p) {
+    using S = Smem<BN>;
+    constexpr int kEpiWarps = kI8 ? 8 : 4;
+    constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
+    constexpr uint32_t kIdesc = idesc_f16(kBf16, BM, BN);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOffset);
+    uint64_t* empty = full + kStages;
+    uint64_t* acc_full = empty + kStages;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], kEpiWarps * 32);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued_phase[kStages];
+            bool issued[kStages];
+            for (int s = 0; s < kStages; ++s) issued[s] = false;
+            bool ok = true;
+            for (uint32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                uint32_t tm, tn;
+                tile_coords(t, p, tm, tn);
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag, kWaitLimitNs)) {
+                        record_failure(kRoleProducer, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* a_dst = smem + stage * S::kStageBytes;
+                    uint8_t* b_dst = a_dst + S::kABytes;
+                    mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+                    tma_load_2d(a_dst, &tmA, &full[stage], static_cast<int32_t>(kb * BK),
+                                static_cast<int32_t>(tm * BM));
+                    tma_load_2d(b_dst, &tmB, &full[stage], static_cast<int32_t>(kb * BK),
+                                static_cast<int32_t>(tn * BN));
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == kStages) { stage = 0; phase ^= 1; }
+                }
+            }
+            // Copies still in flight must land before shared memory goes away.
+            for (int s = 0; s < kStages; ++s)
+                if (issued[s]) {
+                    volatile int never = 0;
+                    mbar_wait_bounded(&full[s], issued_phase[s], &never, kWaitLimitNs);
+                }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (uint32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+                const uint32_t n_chunks = kI8 ? (p.num_kb + kI8ChunkBlocks - 1) / kI8ChunkBlocks : 1;
+                for (uint32_t ch = 0; ok && ch < n_chunks; ++ch) {
+                    if (!mbar_wait_bounded(&acc_empty[acc], acc_phase ^ 1, abort_flag, kWaitLimitNs)) {
+                        record_failure(kRoleMma, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + acc * BN;
+                    const uint32_t kb_begin = kI8 ? ch * kI8ChunkBlocks : 0;
+                    const uint32_t kb_end = kI8 ? min(p.num_kb, kb_begin + kI8ChunkBlocks) : p.num_kb;
+                    for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
+                        if (!mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                            record_failure(kRoleMma, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(smem + stage * S::kStageBytes);
+                        const uint64_t a_desc = smem_desc_kmajor_sw128(a_addr);
+                        const uint64_t b_desc = smem_desc_kmajor_sw128(a_addr + S::kABytes);
+#pragma unroll
+                        for (int k = 0; k < BK / UK; ++k) {
+                            // +32 bytes along K inside the 128-byte swizzle row
+                            tc_mma_f16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc,
+                                       (kb > kb_begin || k > 0) ? 1u : 0u);
+                        }
+                        tc_commit(&empty[stage]);
+                        if (++stage == kStages) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    tc_commit(&acc_full[acc]);
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                }
+            }
+            // Every MMA issued so far must finish before TMEM is freed.
+            tc_commit(drain);
+            volatile int never = 0;
+            mbar_wait_bounded(drain, 0, &never, kWaitLimitNs);
+        }
+    } else {
+        // ------------------------------------------------ epilogue warps
+        const int ew = warp - 2;              // 0 .. kEpiWarps-1
+        const int quarter = warp & 3;         // TMEM lanes this warp may access
+        const int col_half = kI8 ? (ew >> 2) : 0;  // INT8: which half of the columns
+        constexpr int kColsPerWarp = kI8 ? BN / 2 : BN;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t acc = 0, acc_phase = 0;
+        bool ok = true;
+        for (uint32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            uint32_t tm, tn;
+            tile_coords(t, p, tm, tn);
+            const int64_t row = static_cast<int64_t>(tm) * BM + quarter * 32 + lane;
+            const int64_t col0 = static_cast<int64_t>(tn) * BN + col_half * kColsPerWarp;
+            if constexpr (!kI8) {
+                if (!mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
+                    record_failure(kRoleEpilogue, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < kColsPerWarp / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem_base + lane_base + acc * BN + c * 32, r);
+                    tmem_ld_wait();
+                    float v[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                    if (row < p.M) store_row_chunk<TOut>(p, row, col0 + c * 32, v);
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[acc]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            } else {
+                int32_t sum[kColsPerWarp];
+#pragma unroll
+                for (int j = 0; j < kColsPerWarp; ++j) sum[j] = 0;
+                const uint32_t n_chunks = (p.num_kb + kI8ChunkBlocks - 1) / kI8ChunkBlocks;
+                for (uint32_t ch = 0; ch < n_chunks; ++ch) {
+                    if (!mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
+                        record_failure(kRoleEpilogue, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < kColsPerWarp / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(
+                            tmem_base + lane_base + acc * BN + col_half * kColsPerWarp + c * 32, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            // exact integer in fp32 -> int32, wrapping add
+                            const int32_t chunk = __float2int_rn(__uint_as_float(r[j]));
+                            sum[c * 32 + j] = static_cast<int32_t>(
+                                static_cast<uint32_t>(sum[c * 32 + j]) + static_cast<uint32_t>(chunk));
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&acc_empty[acc]);
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                }
+                if (!ok) break;
+                if (row < p.M) {
+#pragma unroll
+                    for (int c = 0; c < kColsPerWarp / 32; ++c) {
+                        int32_t v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = sum[c * 32 + j];
+                        store_row_chunk_i32(p, row, col0 + c * 32, v);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---- operand repacking into the workspace ------------------------------------
+//
+// dst[r][k] = src(r, k) converted to bf16/fp16 storage, for r < rows, k < K;
+// zero for K <= k < ld_dst.  src(r, k) = src[r*ld_src + k] (k-contiguous) or
+// src[k*ld_src + r] (transposed).  A 32 x 32 tile goes through shared memory
+// so that both the read and the write are coalesced.
+
+template <typename TSrc, typename TDst>
+__device__ __forceinline__ TDst convert_elem(TSrc v);
+template <> __device__ __forceinline__ __nv_bfloat16 convert_elem(__nv_bfloat16 v) { return v; }
+template <> __device__ __forceinline__ __half convert_elem(__half v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 convert_elem(int8_t v) {
+    return __float2bfloat16_rn(static_cast<float>(v));  // exact: |v| <= 128
+}
+
+template <typename TSrc, typename TDst, bool kTransposed>
+__global__ void __launch_bounds__(256) pack_kmajor_kernel(const TSrc* __restrict__ src,
+                                                          int64_t ld_src, int64_t rows,
+                                                          int64_t K, TDst* __restrict__ dst,
+                                                          int64_t ld_dst) {
+    __shared__ TSrc tile[32][33];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
+    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    for (int i = ty; i < 32; i += 8) {
+        if constexpr (kTransposed) {
+            // read along r (contiguous in memory): tile[k][r]
+            const int64_t k = k0 + i, r = r0 + tx;
+            tile[i][tx] = (k < K && r < rows) ? src[k * ld_src + r] : TSrc(0);
+        } else {
+            const int64_t r = r0 + i, k = k0 + tx;
+            tile[i][tx] = (r < rows && k < K) ? src[r * ld_src + k] : TSrc(0);
+        }
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int64_t r = r0 + i, k = k0 + tx;
+        if (r < rows && k < ld_dst) {
+            TSrc v = kTransposed ? tile[tx][i] : tile[i][tx];
+            dst[r * ld_dst + k] = (k < K) ? convert_elem<TSrc, TDst>(v) : convert_elem<TSrc, TDst>(TSrc(0));
+        }
+    }
+}
+
+// ---- host side -------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// K-major operand: rows x K elements of 2 bytes, row stride ld elements.
+cudaError_t make_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                            int64_t ld, uint32_t box_rows, bool bf16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+constexpr int kBnFloat = 256;
+constexpr int kBnI8 = 256;
+constexpr size_t kWsAlign = 256;
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+// Which operands need repacking into the workspace.
+struct PackPlan {
+    bool pack_a, pack_b;
+    int64_t kp;  // padded K of packed operands (multiple of 8 elements = 16 bytes)
+    size_t a_bytes, b_bytes;
+};
+
+PackPlan plan_for(const GemmArgs& a) {
+    PackPlan pl{};
+    pl.kp = round_up(a.K, 8);
+    const bool i8 = a.in_dtype == DGA_I8;
+    pl.pack_a = i8 || a.lda % 8 != 0 || !aligned(a.A, 16);
+    pl.pack_b = i8 || a.layout_b != DGA_COL_MAJOR || a.ldb % 8 != 0 || !aligned(a.B, 16);
+    pl.a_bytes = pl.pack_a ? round_up(a.M * pl.kp * 2, kWsAlign) : 0;
+    pl.b_bytes = pl.pack_b ? round_up(a.N * pl.kp * 2, kWsAlign) : 0;
+    return pl;
+}
+
+// Workspace size when pointers are not known: assume aligned pointers.
+PackPlan plan_for_sizes(const GemmArgs& a) {
+    GemmArgs b = a;
+    static const char aligned_probe[16] __attribute__((aligned(16))) = {};
+    b.A = aligned_probe;
+    b.B = aligned_probe;
+    return plan_for(b);
+}
+
+template <bool kBf16, bool kI8, int BN, typename TOut>
+cudaError_t launch_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
+                          const DeviceInfo& dev, cudaStream_t s) {
+    auto kern = tc_gemm_kernel<kBf16, kI8, BN, TOut>;
+    const int smem = static_cast<int>(Smem<BN>::kLaunchBytes);
+    if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(std::min<uint32_t>(p.num_tiles, dev.sm_count));
+    kern<<<grid, kI8 ? 320 : 192, smem, s>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+template <typename TSrc, typename TDst>
+cudaError_t launch_pack(const void* src, int64_t ld_src, bool transposed, int64_t rows,
+                        int64_t K, void* dst, int64_t ld_dst, cudaStream_t s) {
+    dim3 grid(static_cast<unsigned>((ld_dst + 31) / 32), static_cast<unsigned>((rows + 31) / 32));
+    if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+    if (transposed)
+        pack_kmajor_kernel<TSrc, TDst, true><<<grid, 256, 0, s>>>(
+            static_cast<const TSrc*>(src), ld_src, rows, K, static_cast<TDst*>(dst), ld_dst);
+    else
+        pack_kmajor_kernel<TSrc, TDst, false><<<grid, 256, 0, s>>>(
+            static_cast<const TSrc*>(src), ld_src, rows, K, static_cast<TDst*>(dst), ld_dst);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tc_supports(const GemmArgs& a) {
+    const bool fp = (a.in_dtype == DGA_BF16 && (a.out_dtype == DGA_F32 || a.out_dtype == DGA_BF16)) ||
+                    (a.in_dtype == DGA_F16 && (a.out_dtype == DGA_F32 || a.out_dtype == DGA_F16));
+    const bool i8 = a.in_dtype == DGA_I8 && a.out_dtype == DGA_I32;
+    if (!fp && !i8) return false;
+    if (a.K < 1 || a.M < 1 || a.N < 1) return false;
+    // tensor-map extents are 32-bit; tile counts fit comfortably in 32 bits
+    if (a.M >= (int64_t(1) << 31) || a.N >= (int64_t(1) << 31) || a.K >= (int64_t(1) << 31)) return false;
+    return encode_fn() != nullptr;
+}
+
+size_t tc_workspace_size(const GemmArgs& a) {
+    PackPlan pl = (a.A && a.B) ? plan_for(a) : plan_for_sizes(a);
+    return pl.a_bytes + pl.b_bytes;
+}
+
+cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
+    const bool i8 = a.in_dtype == DGA_I8;
+    const bool bf16 = i8 || a.in_dtype == DGA_BF16;
+    PackPlan pl = plan_for(a);
+    if (a.ws_bytes < pl.a_bytes + pl.b_bytes) return cudaErrorInvalidValue;
+    const void* A = a.A;
+    int64_t lda = a.lda;
+    const void* B = a.B;
+    int64_t ldb = a.ldb;
+    cudaError_t e;
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    if (pl.pack_a) {
+        void* dst = ws;
+        if (i8) e = launch_pack<int8_t, __nv_bfloat16>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, a.stream);
+        else if (bf16) e = launch_pack<__nv_bfloat16, __nv_bfloat16>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, a.stream);
+        else e = launch_pack<__half, __half>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, a.stream);
+        if (e != cudaSuccess) return e;
+        ++*launches;
+        A = dst;
+        lda = pl.kp;
+    }
+    if (pl.pack_b) {
+        void* dst = ws + pl.a_bytes;
+        const bool tr = a.layout_b == DGA_ROW_MAJOR;  // B(k, j) = B[k*ldb + j]: transpose to N x K
+        if (i8) e = launch_pack<int8_t, __nv_bfloat16>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, a.stream);
+        else if (bf16) e = launch_pack<__nv_bfloat16, __nv_bfloat16>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, a.stream);
+        else e = launch_pack<__half, __half>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, a.stream);
+        if (e != cudaSuccess) return e;
+        ++*launches;
+        B = dst;
+        ldb = pl.kp;
+    }
+    const int BN = i8 ? kBnI8 : kBnFloat;
+    CUtensorMap ma, mb;
+    e = make_kmajor_map(&ma, A, a.M, a.K, lda, BM, bf16);
+    if (e != cudaSuccess) return e;
+    e = make_kmajor_map(&mb, B, a.N, a.K, ldb, BN, bf16);
+    if (e != cudaSuccess) return e;
+
+    TcParams p{};
+    p.M = a.M;
+    p.N = a.N;
+    p.K = a.K;
+    p.C = a.C;
+    p.ldc = a.ldc;
+    p.alpha = a.alpha_f;
+    p.beta = a.beta_f;
+    p.alpha_i = a.alpha_i;
+    p.beta_i = a.beta_i;
+    const int out_size = (a.out_dtype == DGA_F32 || a.out_dtype == DGA_I32) ? 4 : 2;
+    p.vec_c = ((a.ldc * out_size) % 16 == 0 && aligned(a.C, 16)) ? 1 : 0;
+    p.tiles_m = static_cast<uint32_t>((a.M + BM - 1) / BM);
+    p.tiles_n = static_cast<uint32_t>((a.N + BN - 1) / BN);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.num_kb = static_cast<uint32_t>((a.K + BK - 1) / BK);
+
+    if (i8) e = launch_kernel<true, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream);
+    else if (bf16 && a.out_dtype == DGA_F32) e = launch_kernel<true, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
+    else if (bf16) e = launch_kernel<true, false, kBnFloat, __nv_bfloat16>(ma, mb, p, dev, a.stream);
+    else if (a.out_dtype == DGA_F32) e = launch_kernel<false, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
+    else e = launch_kernel<false, false, kBnFloat, __half>(ma, mb, p, dev, a.stream);
+    if (e == cudaSuccess) ++*launches;
+    return e;
+}
+
+cudaError_t tc_status_take(int* status) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_tc_status, sizeof v);
+    if (e != cudaSuccess) return e;
+    if (v != 0) {
+        int zero = 0;
+        e = cudaMemcpyToSymbol(g_tc_status, &zero, sizeof zero);
+    }
+    *status = v;
+    return e;
+}
+
+}  // namespace dga

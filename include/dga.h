@@ -1,0 +1,165 @@
+/*
+ * dga.h -- dense GEMM on one GB300 (sm_103a): the C ABI.
+ *
+ * The one operation is the BLAS GEMM update
+ *
+ *     C <- alpha * A * B + beta * C,   A: M x K,  B: K x N,  C: M x N,
+ *
+ * as defined in "AI Programming: Matrix Product" (elainafan.one), section
+ * "Dense matrix multiplication": alpha and beta let one call both scale the
+ * product and accumulate into C.  Matrices are row-major, element (r, c) at
+ * offset r*ld + c (same page, section "Row-major order"); B may instead be
+ * column-major, which is how a Linear layer stores its weight (same page,
+ * section "Fully-connected layer": Y = X * W^T with W of shape
+ * [out_features, in_features]).
+ *
+ * Every call runs on the GPU, in kernels of this library; nothing falls back
+ * to the CPU or to another library.  All calls are asynchronous on `stream`
+ * and never synchronise, except dga_sync_status().
+ *
+ * Ownership: A, B, C and the workspace are caller-owned device memory (any
+ * allocator, e.g. a PyTorch caching allocator).  The library allocates no
+ * device memory and keeps no per-call state on the device beyond one status
+ * word per kernel family.  C must not overlap A or B (detected, rejected).
+ *
+ * Thread safety: calls from several host threads are safe; dga_last_path()
+ * and dga_last_cuda_error() are per host thread.
+ */
+#ifndef DGA_H_
+#define DGA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* dga_stream_t;
+
+/* Element types.  Supported (in, out) pairs:
+ *   (DGA_F32, DGA_F32)    exact FP32 FFMA arithmetic, never TF32
+ *   (DGA_BF16, DGA_F32)   bf16 inputs, fp32 accumulate, fp32 output
+ *   (DGA_BF16, DGA_BF16)  bf16 inputs, fp32 accumulate, bf16 output (nearest-even)
+ *   (DGA_F16, DGA_F32)    fp16 inputs, fp32 accumulate, fp32 output
+ *   (DGA_F16, DGA_F16)    fp16 inputs, fp32 accumulate, fp16 output (nearest-even)
+ *   (DGA_I8, DGA_I32)     int8 inputs, exact integer products and sums, int32
+ *                         output; alpha*sum + beta*c is reduced mod 2^32.      */
+typedef enum { DGA_F32 = 0, DGA_BF16 = 1, DGA_F16 = 2, DGA_I8 = 3, DGA_I32 = 4 } dga_dtype;
+
+/* Layout of B only; A and C are always row-major.
+ *   DGA_ROW_MAJOR: B(k, j) = B[k*ldb + j], ldb >= max(1, N)
+ *   DGA_COL_MAJOR: B(k, j) = B[j*ldb + k], ldb >= max(1, K)  (B stored N x K) */
+typedef enum { DGA_ROW_MAJOR = 0, DGA_COL_MAJOR = 1 } dga_layout;
+
+/* Kernel family.  DGA_PATH_AUTO picks the fastest one that accepts the
+ * arguments; the others force one family (for tests and measurement) and make
+ * the call fail with DGA_ERR_PATH when that family cannot run the arguments.
+ *   GENERIC  any dtype pair, any layout, alignment or leading dimension
+ *   SIMT     FP32 register-tiled FFMA kernel (F32 -> F32)
+ *   TCGEN05  5th-generation tensor cores, TMA + mbarrier pipeline, TMEM
+ *            accumulators (BF16/F16 inputs; INT8 through exact bf16 encoding)
+ *   SKINNY   bandwidth-bound kernel for M <= 16 with column-major B
+ *            (decode-shaped X * W^T; BF16/F16 inputs)                          */
+typedef enum {
+    DGA_PATH_AUTO = 0,
+    DGA_PATH_GENERIC = 1,
+    DGA_PATH_SIMT = 2,
+    DGA_PATH_TCGEN05 = 3,
+    DGA_PATH_SKINNY = 4
+} dga_path;
+
+/* Status codes.  0 is success.  A negative value -p names the p-th argument
+ * of dga_gemm_ex (1-based) as invalid, in the manner of BLAS's xerbla:
+ *   -4 M < 0, -5 N < 0, -6 K < 0, -7 alpha NULL, -8 A NULL, -9 lda too small,
+ *   -10 B NULL, -11 ldb too small, -12 beta NULL, -13 C NULL,
+ *   -14 ldc too small, -15 workspace NULL while workspace_bytes > 0,
+ *   -17 path not a dga_path value.                                          */
+#define DGA_OK 0
+#define DGA_ERR_UNSUPPORTED 1     /* (in, out) dtype pair or layout value not supported */
+#define DGA_ERR_CUDA 2            /* a CUDA call failed; see dga_last_cuda_error()      */
+#define DGA_ERR_DEVICE_TIMEOUT 3  /* a kernel gave up waiting (dga_sync_status only)    */
+#define DGA_ERR_PATH 4            /* the forced path cannot run these arguments         */
+#define DGA_ERR_WORKSPACE 5       /* workspace_bytes < dga_gemm_workspace_size(...)     */
+#define DGA_ERR_OVERLAP 6         /* C overlaps A or B                                  */
+#define DGA_ERR_DEVICE 7          /* current device is not sm_103 (GB300)               */
+
+/*
+ * dga_gemm -- C <- alpha*A*B + beta*C on `stream`, path chosen automatically.
+ *
+ *   in_dtype, out_dtype  one of the supported pairs above
+ *   layout_b             DGA_ROW_MAJOR or DGA_COL_MAJOR (B only)
+ *   M, N, K              sizes, >= 0
+ *   alpha, beta          HOST pointers to the scalars: float for floating
+ *                        point inputs, int32_t for DGA_I8 inputs.  beta == 0:
+ *                        C is not read (NaN or Inf there does not propagate).
+ *                        alpha == 0 or K == 0: A and B are not read.
+ *   A, lda               device pointer, A(i, k) = A[i*lda + k], lda >= max(1, K)
+ *   B, ldb               device pointer, see dga_layout
+ *   C, ldc               device pointer, C(i, j) = C[i*ldc + j], ldc >= max(1, N)
+ *   workspace            device scratch of at least workspace_bytes, or NULL
+ *   workspace_bytes      must be >= dga_gemm_workspace_size() for these args
+ *                        (0 for every path but INT8 on the tensor cores)
+ *   stream               CUDA stream the kernels are enqueued on
+ *
+ * M == 0 or N == 0 returns DGA_OK and touches no memory.  Returns a status
+ * code; a kernel that timed out is reported later by dga_sync_status().
+ */
+int dga_gemm(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
+             int64_t M, int64_t N, int64_t K,
+             const void* alpha, const void* A, int64_t lda,
+             const void* B, int64_t ldb, const void* beta,
+             void* C, int64_t ldc,
+             void* workspace, size_t workspace_bytes, dga_stream_t stream);
+
+/* dga_gemm with the kernel family forced (argument 17).  Same semantics. */
+int dga_gemm_ex(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
+                int64_t M, int64_t N, int64_t K,
+                const void* alpha, const void* A, int64_t lda,
+                const void* B, int64_t ldb, const void* beta,
+                void* C, int64_t ldc,
+                void* workspace, size_t workspace_bytes, dga_path path,
+                dga_stream_t stream);
+
+/* Bytes of workspace dga_gemm_ex needs for these arguments on `path`
+ * (DGA_PATH_AUTO: the path dga_gemm would choose).  Pointers are not needed:
+ * the answer depends on dtypes, layout, sizes and leading dimensions only. */
+size_t dga_gemm_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
+                               int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldc, dga_path path);
+
+/* The path that dga_gemm_ex would run for these arguments (never AUTO), or a
+ * negative status when the arguments are invalid.  A and B pointer alignment
+ * matters: pass the real pointers. */
+int dga_select_path(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
+                    int64_t M, int64_t N, int64_t K,
+                    const void* A, int64_t lda, const void* B, int64_t ldb,
+                    const void* C, int64_t ldc);
+
+/* The dga_path of the last successful dga_gemm/dga_gemm_ex on this host thread
+ * (DGA_PATH_AUTO if none yet or if the call did no GEMM work). */
+int dga_last_path(void);
+
+/* Number of kernels the last successful call on this host thread launched. */
+int dga_last_launch_count(void);
+
+/* Synchronises `stream`, then reads and clears the device status words the
+ * kernels write when one of their bounded waits expires.  Returns DGA_OK,
+ * DGA_ERR_DEVICE_TIMEOUT, or DGA_ERR_CUDA when the synchronisation failed. */
+int dga_sync_status(dga_stream_t stream);
+
+/* The cudaError_t value behind the last DGA_ERR_CUDA on this host thread. */
+int dga_last_cuda_error(void);
+
+/* A static string naming a status code. */
+const char* dga_status_string(int status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int dga_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGA_H_ */

@@ -1,0 +1,109 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/dga.h declares, and rejects invalid arguments before touching the
+device (BLAS-style codes: -position of the bad argument)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import dense_gemm_accelerator_gb300 as dga
+from dense_gemm_accelerator_gb300 import build as dga_build
+from dense_gemm_accelerator_gb300 import inputs as gen
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dga_build.build()
+    return dga.lib()
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(dga_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared_symbols()
+    assert {"dga_gemm", "dga_gemm_ex", "dga_sync_status"} <= declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    assert declared <= set(dga.SIGNATURES), "binding lacks a declared entry point"
+
+
+def test_version_and_strings(lib):
+    assert dga.dga_version() >= 100
+    for st in (0, 1, 2, 3, 4, 5, 6, 7, -4):
+        assert dga.dga_status_string(st)
+
+
+def _call(**over):
+    one, zero = ctypes.c_float(1.0), ctypes.c_float(0.0)
+    args = dict(in_dtype=gen.F32, out_dtype=gen.F32, layout_b=gen.ROW_MAJOR, M=4, N=4, K=4,
+                alpha=ctypes.byref(one), A=0x1000, lda=4, B=0x2000, ldb=4, beta=ctypes.byref(zero),
+                C=0x3000, ldc=4, workspace=None, workspace_bytes=0, path=dga.PATH_AUTO, stream=None)
+    args.update(over)
+    return dga.dga_gemm_ex(*args.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(M=-1), -4), (dict(N=-1), -5), (dict(K=-1), -6), (dict(alpha=None), -7),
+    (dict(A=None), -8), (dict(lda=3), -9), (dict(B=None), -10), (dict(ldb=3), -11),
+    (dict(beta=None), -12), (dict(C=None), -13), (dict(ldc=3), -14),
+    (dict(workspace=None, workspace_bytes=16), -15), (dict(path=9), -17),
+    (dict(in_dtype=gen.F32, out_dtype=gen.BF16), dga.ERR_UNSUPPORTED),
+    (dict(in_dtype=gen.I8, out_dtype=gen.F32), dga.ERR_UNSUPPORTED),
+    (dict(layout_b=5), dga.ERR_UNSUPPORTED),
+    (dict(C=0x1004), dga.ERR_OVERLAP),
+])
+def test_argument_errors(lib, over, code):
+    assert _call(**over) == code
+
+
+def test_col_major_ldb_rule(lib):
+    # column-major B needs ldb >= K, not >= N
+    assert _call(layout_b=gen.COL_MAJOR, K=8, lda=8, ldb=4) == -11
+
+
+def test_m_zero_is_a_no_op_without_device(lib):
+    assert _call(M=0, A=None, C=None) == dga.OK
+    assert _call(N=0, B=None, C=None) == dga.OK
+
+
+def test_workspace_size_query(lib):
+    W = gen.WORKLOADS
+    # INT8 on the tensor cores packs A and B as bf16: 2 bytes x (M + N) x K8
+    w = W["int8_ragged"]
+    ws = dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
+                                     w.N, w.N, dga.PATH_TCGEN05)
+    assert ws >= 2 * (w.M + w.N) * w.K
+    # column-major bf16 with aligned leading dimensions needs nothing
+    w = W["bf16_8192"]
+    assert dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
+                                       w.K, w.N, dga.PATH_TCGEN05) == 0
+    # row-major B is transposed into the workspace
+    assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.ROW_MAJOR, 256, 512, 100, 104,
+                                       512, 512, dga.PATH_TCGEN05) >= 512 * 104 * 2
+    assert dga.dga_gemm_workspace_size(gen.F32, gen.F32, gen.ROW_MAJOR, 64, 64, 64, 64, 64, 64,
+                                       dga.PATH_SIMT) == 0
+
+
+def test_binding_layout_from_strides():
+    A = torch.empty(6, 5)
+    C = torch.empty(6, 7)
+    lda, layout, ldb, ldc = dga.operand_layout(A, torch.empty(5, 7), C)
+    assert (lda, layout, ldb, ldc) == (5, gen.ROW_MAJOR, 7, 7)
+    lda, layout, ldb, ldc = dga.operand_layout(A, torch.empty(7, 5).t(), C)
+    assert (layout, ldb) == (gen.COL_MAJOR, 5)
+    with pytest.raises(ValueError):
+        dga.operand_layout(A.t(), torch.empty(5, 7), torch.empty(5, 7))
+    with pytest.raises(ValueError):
+        dga.operand_layout(A, torch.empty(10, 14)[::2, ::2], C)
