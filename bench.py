@@ -1,0 +1,562 @@
+"""Benchmark: dense GEMM throughput on GB300 against its roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one GEMM of the named workload (default fp32_4096: FP32 SGEMM
+M=N=K=4096, alpha=1.5, beta=0.5, the SIMT path) through the library's C ABI,
+with every input resident in HBM.  Input sets are rotated so that the bytes a
+step touches are never in L2 from the step before (the rotation spans more
+than 2x the 129 MB L2).  Rank 0 prints ONE JSON line.
+
+Extra keys beside the contract's: `per_dtype` (the other hot-path workloads
+-- BF16 8192^3 on tcgen05, skinny M in {1, 8, 16}, INT8 4093x4099x4096 --
+each timed the same way, with its roofline fraction) and `peaks` (where every
+denominator came from).
+
+`--impl reference` times the CPU oracle (plain fp64 triple loop, as it
+stands) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS/TOPS and % of GB300 roofline per dtype; skinny-M HBM GB/s"
+L2_BYTES = 129 * 1024 * 1024
+
+# ------------------------------------------------------------ accounting --
+#
+# FLOPs and algorithmic bytes.  A GEMM does K multiplies and K adds per
+# output: 2*M*N*K FLOPs ("GEMM optimisation, part 0" (chongfengling.github.io),
+# section "Measurement"; "Matrix multiplication: arithmetic intensity, tiling
+# and Tensor Core", section 5.2).  Algorithmic bytes count each operand once:
+# A and B read, C written, and C read as well when beta != 0 (section 5.1's
+# "minimum bytes" column).  Intensity I = FLOPs / bytes (section 5.1).
+
+DTYPE_BYTES = {0: 4, 1: 2, 2: 2, 3: 1, 4: 4}
+
+
+def gemm_flops(M, N, K):
+    return 2 * M * N * K
+
+
+def gemm_bytes(M, N, K, in_bytes, out_bytes, reads_c):
+    return in_bytes * (M * K + K * N) + out_bytes * M * N * (2 if reads_c else 1)
+
+
+def intensity(flops, nbytes):
+    return flops / nbytes
+
+
+def tile_intensity(T, elem_bytes=4):
+    """Per K-step of a T x T block tile: 2*T^3 FLOPs over 2*T^2 elements."""
+    return (2 * T ** 3) / (elem_bytes * 2 * T ** 2)
+
+
+def workload_accounting(w):
+    fl = gemm_flops(w.M, w.N, w.K)
+    by = gemm_bytes(w.M, w.N, w.K, DTYPE_BYTES[w.in_dtype], DTYPE_BYTES[w.out_dtype], w.beta != 0)
+    return fl, by
+
+
+# ------------------------------------------------------------------ peaks --
+
+def load_peaks(sm_count):
+    """Roofline denominators: the measured copy bandwidth and bf16 GEMM
+    throughput of the GB300s (MEASURED_PEAKS.json), else the stated
+    fallback; the FP32 FFMA peak from unit counts and the maximum SM clock."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    src = "measured"
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        hbm = float(pk["hbm_gbs"])
+        bf16 = float(pk["bf16_tflops"])
+        bf16_sus = float(pk.get("bf16_tflops_sustained", bf16))
+        sm_max = float(pk.get("sm_max_mhz", 2070.0))
+    except (OSError, KeyError, ValueError):
+        src = "fallback"
+        hbm, bf16, bf16_sus, sm_max = 6800.0, 1900.0, 1700.0, 2070.0
+    # 128 FP32 lanes per SM, one FFMA (2 FLOP) per lane per clock
+    fp32 = sm_count * 128 * 2 * sm_max * 1e6 / 1e12
+    return {"source": src, "hbm_gbs": hbm, "bf16_tflops": bf16,
+            "bf16_tflops_sustained": bf16_sus, "fp32_ffma_tflops": fp32,
+            "fp32_ffma_basis": f"{sm_count} SMs x 128 lanes x 2 FLOP x {sm_max:.0f} MHz",
+            "sm_max_mhz": sm_max}
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for t, line in self.lines:
+            if not (t0 <= t <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------- GPU workloads --
+
+class Runner:
+    """Device-resident input sets for one workload and the dga call on them."""
+
+    def __init__(self, w, device, sets, seed=0):
+        import torch
+
+        import dense_gemm_accelerator_gb300 as dga
+        from dense_gemm_accelerator_gb300 import inputs as gen
+        self.w, self.dga, self.gen = w, dga, gen
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.sets = []
+        tdt = gen.TORCH_DTYPE
+        for _ in range(sets):
+            A = self._draw((w.M, w.K), w.dist_a, w.in_dtype, g, device)
+            Bs = (w.N, w.K) if w.layout_b == gen.COL_MAJOR else (w.K, w.N)
+            B = self._draw(Bs, w.dist_b, w.in_dtype, g, device)
+            C = self._draw((w.M, w.N), w.dist_c if w.beta != 0 else ("uniform",), w.out_dtype, g,
+                           device) if w.beta != 0 else torch.empty((w.M, w.N), dtype=tdt[w.out_dtype],
+                                                                   device=device)
+            self.sets.append((A, B, C))
+        A, B, C = self.sets[0]
+        lda, layout, ldb, ldc = dga.operand_layout(A, self._bview(B), C)
+        self.lda, self.ldb, self.ldc = lda, ldb, ldc
+        self.ws_bytes = dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N,
+                                                    w.K, lda, ldb, ldc, dga.PATH_AUTO)
+        self.ws = torch.empty(max(self.ws_bytes, 1), dtype=torch.uint8, device=device)
+        self.alpha = dga.scalar(w.alpha, w.in_dtype)
+        self.beta = dga.scalar(w.beta, w.in_dtype)
+
+    def _bview(self, B):
+        return B.t() if self.w.layout_b == self.gen.COL_MAJOR else B
+
+    @staticmethod
+    def _draw(shape, dist, code, g, device):
+        import torch
+
+        from dense_gemm_accelerator_gb300 import inputs as gen
+        if dist[0] == "uniform":
+            return (torch.rand(shape, generator=g, device=device) * 2 - 1).to(gen.TORCH_DTYPE[code])
+        if dist[0] == "normal":
+            return (torch.randn(shape, generator=g, device=device) * dist[1]).to(gen.TORCH_DTYPE[code])
+        return torch.randint(-128, 128, shape, generator=g, device=device,
+                             dtype=torch.int8 if code == gen.I8 else torch.int32)
+
+    def call(self, i, stream):
+        import ctypes
+        A, B, C = self.sets[i % len(self.sets)]
+        w, dga = self.w, self.dga
+        st = dga.dga_gemm(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K,
+                          ctypes.byref(self.alpha), A.data_ptr(), self.lda, B.data_ptr(), self.ldb,
+                          ctypes.byref(self.beta), C.data_ptr(), self.ldc, self.ws.data_ptr(),
+                          self.ws_bytes, stream)
+        if st != dga.OK:
+            raise dga.DgaError(st, f"dga_gemm ({w.name})")
+        return dga.dga_last_launch_count()
+
+
+def sets_for(w, min_sets=2):
+    """Enough input sets that one rotation spans > 2x L2."""
+    from dense_gemm_accelerator_gb300 import inputs as gen
+    per = DTYPE_BYTES[w.in_dtype] * (w.M * w.K + w.K * w.N) + DTYPE_BYTES[w.out_dtype] * w.M * w.N
+    n = max(min_sets, -(-2 * L2_BYTES // per) + 1)
+    del gen
+    return int(n)
+
+
+def time_kernel(runner, steps, warmup):
+    """Back-to-back launches on one stream, CUDA events around each call."""
+    import torch
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    for i in range(warmup):
+        runner.call(i, s)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    launches = 0
+    for i in range(steps):
+        ev[i][0].record(stream)
+        launches += runner.call(warmup + i, s)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    return ms, launches
+
+
+def roofline_for(w, ms_mean, peaks, sustained=False):
+    fl, by = workload_accounting(w)
+    from dense_gemm_accelerator_gb300 import inputs as gen
+    if w.name.startswith("skinny"):
+        ach = by / (ms_mean * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": by}
+    ach = fl / (ms_mean * 1e-3) / 1e12
+    if w.in_dtype == gen.F32:
+        return {"bound": "alu", "achieved": ach, "peak": peaks["fp32_ffma_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["fp32_ffma_tflops"],
+                "algorithmic_flops": fl}
+    pk = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    return {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s" if w.in_dtype != gen.I8 else "TOP/s",
+            "frac": ach / pk, "algorithmic_flops": fl,
+            "peak_kind": "bf16 tensor (INT8 runs as exact bf16 products)" if w.in_dtype == gen.I8 else "bf16 tensor"}
+
+
+def traffic_record(kernel_src, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(workload)
+    if not entry:
+        return None
+    src = os.path.join(ROOT, "dense_gemm_accelerator_gb300", "csrc", kernel_src)
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if entry.get("source_sha256_16") != digest:
+        return None
+    return entry.get("bytes_per_launch")
+
+
+KERNEL_SOURCE = {"fp32": "sgemm_simt.cu", "bf16": "gemm_tcgen05.cu", "skinny": "gemv_skinny.cu",
+                 "int8": "gemm_tcgen05.cu"}
+
+
+def source_of(w):
+    if w.name.startswith("skinny"):
+        return KERNEL_SOURCE["skinny"]
+    if w.name.startswith("fp32"):
+        return KERNEL_SOURCE["fp32"]
+    return KERNEL_SOURCE["int8" if w.name.startswith("int8") else "bf16"]
+
+
+# ----------------------------------------------------------------- e2e leg --
+
+def e2e_leg(w, steps, warmup, device):
+    """Same metric through the public API with host buffers: every step copies
+    the inputs from pinned host memory, runs the GEMM and reads C back."""
+    import torch
+
+    import dense_gemm_accelerator_gb300 as dga
+    from dense_gemm_accelerator_gb300 import inputs as gen
+    A, B, C = gen.make_inputs(w, with_c=w.beta != 0)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hC = C.pin_memory() if C is not None else None
+    out = torch.empty((w.M, w.N), dtype=gen.TORCH_DTYPE[w.out_dtype]).pin_memory()
+    dA = torch.empty_like(hA, device=device)
+    dB = torch.empty_like(hB, device=device)
+    dC = torch.empty((w.M, w.N), dtype=gen.TORCH_DTYPE[w.out_dtype], device=device)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        if hC is not None:
+            dC.copy_(hC, non_blocking=True)
+        dga.gemm(dA, dB.t() if w.layout_b == gen.COL_MAJOR else dB, dC, w.alpha, w.beta)
+        out.copy_(dC, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    fl, by = workload_accounting(w)
+    h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size() + \
+        (hC.numel() * hC.element_size() if hC is not None else 0)
+    d2h = out.numel() * out.element_size()
+    if w.name.startswith("skinny"):
+        val, unit = by / (ms * 1e-3) / 1e9, "GB/s"
+    else:
+        val, unit = fl / (ms * 1e-3) / 1e12, "TFLOPS"
+    return {"value": val, "unit": unit, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------- CPU oracle timing --
+
+class OracleSample:
+    """Times the CPU oracle, as it stands, on the first `rows` output rows of
+    the workload (all N columns, full K), on this host's cores."""
+
+    def __init__(self, w):
+        self.threads = len(os.sched_getaffinity(0))
+        os.environ.setdefault("OMP_NUM_THREADS", str(self.threads))
+        self.threads = int(os.environ["OMP_NUM_THREADS"])
+        from dense_gemm_accelerator_gb300 import inputs as gen
+        self.w, self.gen = w, gen
+        self.A, self.B, self.C = gen.make_inputs(w, with_c=w.beta != 0)
+        self.ldb = w.K if w.layout_b == gen.COL_MAJOR else w.N
+
+    def run(self, rows):
+        import oracle
+        w, gen = self.w, self.gen
+        a = self.A[:rows].contiguous()
+        c = self.C[:rows].contiguous() if self.C is not None else None
+        t = time.perf_counter()
+        if w.in_dtype == gen.I8:
+            oracle.gemm_i8(w.layout_b, rows, w.N, w.K, w.alpha, a, w.K, self.B, self.ldb, w.beta,
+                           c, w.N)
+        else:
+            oracle.gemm_fp(w.in_dtype, w.out_dtype, w.layout_b, rows, w.N, w.K, w.alpha, a, w.K,
+                           self.B, self.ldb, w.beta, c, w.N)
+        return time.perf_counter() - t
+
+    def rows_for(self, target_s):
+        probe = max(1, min(self.w.M, self.threads))
+        dt = self.run(probe)
+        return int(min(self.w.M, max(probe, probe * target_s / max(dt, 1e-6))))
+
+
+# ------------------------------------------------------------------- main --
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def reference_arm(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    # each step is a bounded sample, sized so the whole run stays within minutes
+    per_step_s = max(0.5, min(4.0, 150.0 / (args.steps + args.warmup)))
+    sampler = OracleSample(w)
+    rows = sampler.rows_for(per_step_s)
+    fl_total, dt_total = 0.0, 0.0
+    for i in range(args.warmup + args.steps):
+        dt = sampler.run(rows)
+        if i >= args.warmup:
+            fl_total += gemm_flops(rows, w.N, w.K)
+            dt_total += dt
+    val = fl_total / dt_total / 1e12
+    unit = "TFLOPS"
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt_total / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                       "beta": w.beta},
+            "cpu_baseline": {"value": val, "unit": unit, "cores": sampler.threads, "kind": "oracle",
+                             "sample": f"first {rows} of {w.M} output rows, all {w.N} columns, "
+                                       f"full K={w.K}, per step"},
+            "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="fp32_4096")
+    ap.add_argument("--impl", default="dga", choices=["dga", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip per_dtype, e2e and cpu legs")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target length of the oracle's CPU-baseline sample")
+    args = ap.parse_args()
+
+    from dense_gemm_accelerator_gb300 import inputs as gen
+    w = gen.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    rank, world, local = dist_env()
+    if world == 1:
+        __graft_entry__.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+        if rank == 0:
+            __graft_entry__.build()
+        dist.barrier()
+    import dense_gemm_accelerator_gb300 as dga
+    dga.lib()
+
+    props = torch.cuda.get_device_properties(device)
+    peaks = load_peaks(props.multi_processor_count)
+
+    runner = Runner(w, device, sets_for(w), seed=rank)
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    for i in range(args.warmup):
+        runner.call(i, s)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_begin = time.time()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    launches = 0
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        launches += runner.call(args.warmup + i, s)
+        ev[i][1].record(stream)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_end = time.time()
+    time.sleep(0.2)
+    clocks.stop()
+    total_ms = g0.elapsed_time(g1)
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    kern_ms = [a.elapsed_time(b) for a, b in ev]
+    kmean = statistics.mean(kern_ms)
+    ms_per_step = total_ms / args.steps
+    fl, by = workload_accounting(w)
+    if w.name.startswith("skinny"):
+        value, unit = world * by / (ms_per_step * 1e-3) / 1e9, "GB/s"
+    else:
+        value, unit = world * fl / (ms_per_step * 1e-3) / 1e12, "TFLOPS"
+    roof = roofline_for(w, kmean, peaks)
+    roof["traffic"] = traffic_record(source_of(w), w.name)
+    roof["kernel_ms_mean"] = kmean
+    roof["kernel_ms_median"] = statistics.median(kern_ms)
+
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": {gen.F32: "f32", gen.BF16: "bf16", gen.F16: "f16", gen.I8: "int8"}[w.in_dtype],
+            "data": "synthetic",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
+                       "beta": w.beta, "layout_b": "col" if w.layout_b else "row",
+                       "path": dga.PATH_NAMES[dga.dga_last_path()],
+                       "l2": f"inputs rotated over {len(runner.sets)} resident sets (> 2x L2 per rotation)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": roof, "gpu_launches": launches,
+            "clocks": clocks.summary(t_begin, t_end), "peaks": peaks}
+    del runner
+    torch.cuda.empty_cache()
+
+    if rank == 0 and world == 1 and not args.no_extras:
+        line["e2e"] = e2e_leg(w, max(3, args.steps // 3), 2, device)
+        per = {}
+        for name in ("bf16_8192", "skinny_m1", "skinny_m8", "skinny_m16", "int8_ragged"):
+            if name == w.name:
+                continue
+            ow = gen.WORKLOADS[name]
+            r = Runner(ow, device, sets_for(ow, 3 if name.startswith("skinny") else 2))
+            ms, nl = time_kernel(r, 20, 5)
+            rf = roofline_for(ow, statistics.mean(ms), peaks)
+            rf["traffic"] = traffic_record(source_of(ow), name)
+            rf["ms_mean"] = statistics.mean(ms)
+            rf["ms_median"] = statistics.median(ms)
+            rf["launches_per_call"] = nl / 20
+            rf["path"] = dga.PATH_NAMES[dga.dga_last_path()]
+            if rf["bound"] == "tensor":
+                rf["frac_of_sustained"] = rf["achieved"] / peaks["bf16_tflops_sustained"]
+            per[name] = rf
+            del r
+            torch.cuda.empty_cache()
+        line["per_dtype"] = per
+        sampler = OracleSample(w)
+        rows = sampler.rows_for(args.cpu_seconds)
+        dt = sampler.run(rows)
+        rate = gemm_flops(rows, w.N, w.K) / dt
+        line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOPS", "cores": sampler.threads,
+                                "kind": "oracle",
+                                "sample": f"first {rows} of {w.M} output rows (all {w.N} columns, "
+                                          f"K={w.K}) in {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

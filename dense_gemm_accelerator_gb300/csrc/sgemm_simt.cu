@@ -42,11 +42,13 @@ struct Params {
     int64_t ldc;
     float alpha, beta;
     int vec_c;  // C is 16-byte aligned and ldc % 4 == 0: float4 epilogue
+    int vec_a;  // A 16-byte aligned and lda % 4 == 0: float4 loads of A
+    int vec_b;  // the same for B
 };
 
 __device__ __forceinline__ float4 ld_f4_masked(const float* row, int64_t col, int64_t ncols,
-                                               bool row_ok) {
-    if (row_ok && col + 3 < ncols) return __ldg(reinterpret_cast<const float4*>(row + col));
+                                               bool row_ok, bool vec) {
+    if (vec && row_ok && col + 3 < ncols) return __ldg(reinterpret_cast<const float4*>(row + col));
     float v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = (row_ok && col + i < ncols) ? __ldg(row + col + i) : 0.0f;
@@ -73,12 +75,13 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_128x128_kernel(Params p) {
     const float* a_src = p.A + (a_row_ok ? a_grow : 0) * p.lda;
     const int64_t b_gcol = col0 + b_c;
 
-    auto load_a = [&](int64_t k0) { return ld_f4_masked(a_src, k0 + a_k, p.K, a_row_ok); };
+    const bool vec_a = p.vec_a != 0, vec_b = p.vec_b != 0;
+    auto load_a = [&](int64_t k0) { return ld_f4_masked(a_src, k0 + a_k, p.K, a_row_ok, vec_a); };
     auto load_b = [&](int64_t k0) {
         int64_t gk = k0 + b_k;
         bool ok = gk < p.K;
         const float* row = p.B + (ok ? gk : 0) * p.ldb;
-        return ld_f4_masked(row, b_gcol, p.N, ok);
+        return ld_f4_masked(row, b_gcol, p.N, ok, vec_b);
     };
     auto stash = [&](int buf, float4 a, float4 b) {
         As[buf][a_k + 0][a_r] = a.x;
@@ -169,14 +172,14 @@ __global__ void __launch_bounds__(kThreads, 2) sgemm_128x128_kernel(Params p) {
 
 bool simt_supports(const GemmArgs& a) {
     return a.in_dtype == DGA_F32 && a.out_dtype == DGA_F32 && a.layout_b == DGA_ROW_MAJOR &&
-           a.lda % 4 == 0 && a.ldb % 4 == 0 && aligned(a.A, 16) && aligned(a.B, 16) &&
            (a.M + BM - 1) / BM <= 65535;
 }
 
 cudaError_t simt_launch(const GemmArgs& a, int* launches) {
     Params p{a.M, a.N, a.K, static_cast<const float*>(a.A), a.lda,
              static_cast<const float*>(a.B), a.ldb, static_cast<float*>(a.C), a.ldc,
-             a.alpha_f, a.beta_f, (a.ldc % 4 == 0 && aligned(a.C, 16)) ? 1 : 0};
+             a.alpha_f, a.beta_f, (a.ldc % 4 == 0 && aligned(a.C, 16)) ? 1 : 0,
+             (a.lda % 4 == 0 && aligned(a.A, 16)) ? 1 : 0, (a.ldb % 4 == 0 && aligned(a.B, 16)) ? 1 : 0};
     dim3 grid(static_cast<unsigned>((a.N + BN - 1) / BN), static_cast<unsigned>((a.M + BM - 1) / BM));
     sgemm_128x128_kernel<<<grid, kThreads, 0, a.stream>>>(p);
     cudaError_t e = cudaGetLastError();
