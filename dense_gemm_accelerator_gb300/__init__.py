@@ -43,6 +43,8 @@ SIGNATURES = {
     "dga_last_cuda_error": (_CI, []),
     "dga_status_string": (ctypes.c_char_p, [_CI]),
     "dga_version": (_CI, []),
+    "dga_gemm_i8_noalloc": (_CI, [_CI, _I64, _I64, _I64, _VP, _VP, _I64, _VP, _I64, _VP, _VP,
+                                  _I64, _VP]),
 }
 
 _lock = threading.Lock()
@@ -121,6 +123,14 @@ def dga_status_string(status):
 
 def dga_version():
     return lib().dga_version()
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def dga_gemm_i8_noalloc(layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream):
+    return lib().dga_gemm_i8_noalloc(layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                                     stream)
 
 
 # ---- tensor convenience layer ----------------------------------------------

@@ -148,6 +148,8 @@ int fail_cuda(cudaError_t e) {
 
 }  // namespace
 
+int note_cuda_error(cudaError_t e) { return fail_cuda(e); }
+
 cudaError_t current_device_info(DeviceInfo* out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -36,6 +36,9 @@ struct DeviceInfo {
     int max_smem_optin;  // bytes of dynamic shared memory one block may opt into
 };
 
+// Records `e` as this host thread's last CUDA error; returns DGA_ERR_CUDA.
+int note_cuda_error(cudaError_t e);
+
 // Properties of the current device (queried once per device).
 cudaError_t current_device_info(DeviceInfo* out);
 

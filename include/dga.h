@@ -155,6 +155,39 @@ int dga_last_cuda_error(void);
 /* A static string naming a status code. */
 const char* dga_status_string(int status);
 
+/*
+ * dga_gemm_i8_noalloc -- INT8 x INT8 -> INT32 GEMM that allocates nothing and
+ * takes no workspace.  The pages have no counterpart: this entry point exists
+ * for callers that cannot allocate device memory at all -- a plugin handed
+ * only its input and output buffers, an engine that reserves all device
+ * memory at start-up and forbids allocations afterwards, or a
+ * latency-critical loop that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation.
+ *
+ * Same computation and argument meanings as dga_gemm with in_dtype = DGA_I8,
+ * out_dtype = DGA_I32 (alpha, beta: host pointers to int32_t; A, B, C device
+ * pointers; result alpha*A*B + beta*C reduced mod 2^32), run on the tensor
+ * cores.  Instead of a caller workspace it uses one scratch area of
+ * DGA_NOALLOC_SCRATCH_BYTES compiled into the library:
+ *   - every GPU on which it is called holds that area until the process exits;
+ *   - the call is refused with DGA_ERR_WORKSPACE, before anything is
+ *     enqueued, when (M + N) * round_up(K, 8) * 2 bytes (the operands
+ *     re-encoded as bf16) exceed it, e.g. M + N = 8192 at K = 4096 fits;
+ *   - all calls share the area and it keeps the last call's contents
+ *     (nothing in it needs to start at zero: each call rewrites all it reads);
+ *     calls that overlap on the GPU -- other streams, other host threads --
+ *     race on it, so serialise them;
+ *   - the first call on a device looks up the area's device address with that
+ *     device current; make that first call before any stream capture.
+ * Argument errors are -(position in this function's argument list); other
+ * codes as for dga_gemm_ex.
+ */
+#define DGA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+int dga_gemm_i8_noalloc(dga_layout layout_b, int64_t M, int64_t N, int64_t K,
+                        const int32_t* alpha, const int8_t* A, int64_t lda,
+                        const int8_t* B, int64_t ldb, const int32_t* beta,
+                        int32_t* C, int64_t ldc, dga_stream_t stream);
+
 /* Library version: major*10000 + minor*100 + patch. */
 int dga_version(void);
 
