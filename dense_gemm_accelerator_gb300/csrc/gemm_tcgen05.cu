@@ -78,10 +78,12 @@ struct TcParams {
     uint32_t tiles_m, tiles_n, num_tiles, num_kb;
 };
 
-// Shared-memory plan (dynamic, 1024-byte aligned): the stage ring, then the
-// barriers.  BN is 256 for floating point, 256 for INT8 too (the epilogue
-// then uses 8 warps, each owning half of the columns).
-template <int BN>
+// Shared-memory plan (dynamic, 1024-byte aligned): the stage ring, the
+// barriers, then one 32 x 33 staging square per epilogue warp (the padding
+// column keeps both the row-wise writes and the column-wise reads free of
+// bank conflicts).  BN is the tile width; kEpiWarps is 4 for floating point,
+// 8 for INT8 (two warps per TMEM lane quarter, each owning half the columns).
+template <int BN, int kEpiWarps>
 struct Smem {
     static constexpr uint32_t kABytes = BM * BK * 2;
     static constexpr uint32_t kBBytes = BN * BK * 2;
@@ -89,7 +91,10 @@ struct Smem {
     static constexpr uint32_t kRing = kStages * kStageBytes;
     static constexpr uint32_t kBarOffset = kRing;
     // full[S], empty[S], acc_full[2], acc_empty[2], drain, then tmem slot + abort flag
-    static constexpr uint32_t kTotal = kRing + (2 * kStages + 5) * 8 + 16;
+    static constexpr uint32_t kBarBytes = (2 * kStages + 5) * 8 + 16;
+    static constexpr uint32_t kEpiOffset = (kBarOffset + kBarBytes + 127) / 128 * 128;
+    static constexpr uint32_t kEpiWarpBytes = 32 * 33 * 4;
+    static constexpr uint32_t kTotal = kEpiOffset + kEpiWarps * kEpiWarpBytes;
     static constexpr uint32_t kLaunchBytes = kTotal + 1024;  // + alignment slack
 };
 
@@ -110,75 +115,53 @@ __device__ __forceinline__ void record_failure(int role, volatile int* abort_fla
 }
 
 // ---- epilogue stores ---------------------------------------------------------
+//
+// A warp holds a 32 x 32 block of the tile: lane l has row (row_base + l),
+// columns col_base + j in v[j].  Storing that directly would make every store
+// instruction touch 32 different rows.  The block is therefore transposed
+// through shared memory, so that each store instruction writes 32
+// consecutive elements of one row (whole 32-byte sectors), whatever the
+// alignment of C or ldc.
 
 template <typename TOut>
-__device__ __forceinline__ void store_row_chunk(const TcParams& p, int64_t row, int64_t col,
-                                                const float (&v)[32]) {
-    TOut* crow = static_cast<TOut*>(p.C) + row * p.ldc;
-    if (p.vec_c && col + 31 < p.N) {
-        if constexpr (sizeof(TOut) == 4) {
-            float4* dst = reinterpret_cast<float4*>(crow + col);
+__device__ __forceinline__ void store_block_staged(const TcParams& p, uint32_t* stage, int lane,
+                                                   int64_t row_base, int64_t col_base,
+                                                   const uint32_t (&v)[32]) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.beta != 0.0f) o = dst[q];
-                o.x = axpby(p.alpha, v[4 * q + 0], p.beta, o.x);
-                o.y = axpby(p.alpha, v[4 * q + 1], p.beta, o.y);
-                o.z = axpby(p.alpha, v[4 * q + 2], p.beta, o.z);
-                o.w = axpby(p.alpha, v[4 * q + 3], p.beta, o.w);
-                dst[q] = o;
-            }
-        } else {
-            // 16-bit outputs: 8 elements per 16-byte store
-            uint4* dst = reinterpret_cast<uint4*>(crow + col);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 raw = make_uint4(0, 0, 0, 0);
-                if (p.beta != 0.0f) raw = dst[q];
-                TOut* tmp = reinterpret_cast<TOut*>(&raw);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    float old = p.beta != 0.0f ? OutT<TOut>::load(&tmp[j]) : 0.0f;
-                    OutT<TOut>::store(&tmp[j], axpby(p.alpha, v[8 * q + j], p.beta, old));
-                }
-                dst[q] = raw;
-            }
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (col + j < p.N) {
-                float old = p.beta != 0.0f ? OutT<TOut>::load(crow + col + j) : 0.0f;
-                OutT<TOut>::store(crow + col + j, axpby(p.alpha, v[j], p.beta, old));
-            }
+    for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = v[j];
+    __syncwarp();
+    const int64_t col = col_base + lane;
+    const bool col_ok = col < p.N;
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+        const int64_t row = row_base + i;
+        if (col_ok && row < p.M) {
+            TOut* dst = static_cast<TOut*>(p.C) + row * p.ldc + col;
+            const float old = p.beta != 0.0f ? OutT<TOut>::load(dst) : 0.0f;
+            OutT<TOut>::store(dst, axpby(p.alpha, __uint_as_float(stage[i * 33 + lane]), p.beta, old));
         }
     }
+    __syncwarp();  // the next block reuses the square
 }
 
-__device__ __forceinline__ void store_row_chunk_i32(const TcParams& p, int64_t row, int64_t col,
-                                                    const int32_t (&v)[32]) {
-    int32_t* crow = static_cast<int32_t*>(p.C) + row * p.ldc;
-    if (p.vec_c && col + 31 < p.N) {
-        int4* dst = reinterpret_cast<int4*>(crow + col);
+__device__ __forceinline__ void store_block_staged_i32(const TcParams& p, uint32_t* stage,
+                                                       int lane, int64_t row_base,
+                                                       int64_t col_base, const int32_t* v) {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            int4 o = make_int4(0, 0, 0, 0);
-            if (p.beta_i != 0) o = dst[q];
-            o.x = axpby_i32(p.alpha_i, v[4 * q + 0], p.beta_i, o.x);
-            o.y = axpby_i32(p.alpha_i, v[4 * q + 1], p.beta_i, o.y);
-            o.z = axpby_i32(p.alpha_i, v[4 * q + 2], p.beta_i, o.z);
-            o.w = axpby_i32(p.alpha_i, v[4 * q + 3], p.beta_i, o.w);
-            dst[q] = o;
-        }
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (col + j < p.N) {
-                int32_t old = p.beta_i != 0 ? crow[col + j] : 0;
-                crow[col + j] = axpby_i32(p.alpha_i, v[j], p.beta_i, old);
-            }
+    for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = static_cast<uint32_t>(v[j]);
+    __syncwarp();
+    const int64_t col = col_base + lane;
+    const bool col_ok = col < p.N;
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i) {
+        const int64_t row = row_base + i;
+        if (col_ok && row < p.M) {
+            int32_t* dst = static_cast<int32_t*>(p.C) + row * p.ldc + col;
+            const int32_t old = p.beta_i != 0 ? *dst : 0;
+            *dst = axpby_i32(p.alpha_i, static_cast<int32_t>(stage[i * 33 + lane]), p.beta_i, old);
         }
     }
+    __syncwarp();
 }
 
 // ---- the kernel ----------------------------------------------------------------
@@ -190,8 +173,8 @@ template <bool kBf16, bool kI8, int BN, typename TOut>
 __global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    TcParams p) {
-    using S = Smem<BN>;
     constexpr int kEpiWarps = kI8 ? 8 : 4;
+    using S = Smem<BN, kEpiWarps>;
     constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
     constexpr uint32_t kIdesc = idesc_f16(kBf16, BM, BN);
 
@@ -321,12 +304,13 @@ __global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
         const int col_half = kI8 ? (ew >> 2) : 0;  // INT8: which half of the columns
         constexpr int kColsPerWarp = kI8 ? BN / 2 : BN;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t* stage = reinterpret_cast<uint32_t*>(smem + S::kEpiOffset + ew * S::kEpiWarpBytes);
         uint32_t acc = 0, acc_phase = 0;
         bool ok = true;
         for (uint32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
             uint32_t tm, tn;
             tile_coords(t, p, tm, tn);
-            const int64_t row = static_cast<int64_t>(tm) * BM + quarter * 32 + lane;
+            const int64_t row_base = static_cast<int64_t>(tm) * BM + quarter * 32;
             const int64_t col0 = static_cast<int64_t>(tn) * BN + col_half * kColsPerWarp;
             if constexpr (!kI8) {
                 if (!mbar_wait_bounded(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
@@ -339,10 +323,7 @@ __global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tmem_base + lane_base + acc * BN + c * 32, r);
                     tmem_ld_wait();
-                    float v[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-                    if (row < p.M) store_row_chunk<TOut>(p, row, col0 + c * 32, v);
+                    store_block_staged<TOut>(p, stage, lane, row_base, col0 + c * 32, r);
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty[acc]);
@@ -378,15 +359,9 @@ __global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
                     if (++acc == 2) { acc = 0; acc_phase ^= 1; }
                 }
                 if (!ok) break;
-                if (row < p.M) {
 #pragma unroll
-                    for (int c = 0; c < kColsPerWarp / 32; ++c) {
-                        int32_t v[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = sum[c * 32 + j];
-                        store_row_chunk_i32(p, row, col0 + c * 32, v);
-                    }
-                }
+                for (int c = 0; c < kColsPerWarp / 32; ++c)
+                    store_block_staged_i32(p, stage, lane, row_base, col0 + c * 32, &sum[c * 32]);
             }
         }
     }
@@ -518,7 +493,7 @@ template <bool kBf16, bool kI8, int BN, typename TOut>
 cudaError_t launch_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
                           const DeviceInfo& dev, cudaStream_t s) {
     auto kern = tc_gemm_kernel<kBf16, kI8, BN, TOut>;
-    const int smem = static_cast<int>(Smem<BN>::kLaunchBytes);
+    const int smem = static_cast<int>(Smem<BN, kI8 ? 8 : 4>::kLaunchBytes);
     if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

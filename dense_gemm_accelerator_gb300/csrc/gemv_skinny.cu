@@ -13,7 +13,12 @@
 // arithmetic off the critical path.
 //
 //  * Each weight element is loaded once, 16 bytes per lane, with
-//    ld.global.nc.L1::no_allocate (streamed, never re-read).
+//    ld.global.nc.L1::no_allocate (streamed, never re-read) and an L2
+//    prefetch size of 256 bytes, so DRAM sees whole 256-byte requests for
+//    rows that a warp walks 64 bytes at a time.
+//  * The loads of several K steps are kept in flight per warp (a software
+//    pipeline over a register ring), since the whole kernel is a single
+//    pass over the weight.
 //  * The M <= 16 activation rows are the "B" operand of an mma.sync
 //    m16n8k16 (fp32 accumulate) and the weight rows its "A" operand, so a
 //    warp computes 16 weight rows x 8 activation rows per instruction; the
@@ -35,9 +40,6 @@
 namespace dga {
 namespace {
 
-constexpr int kWarps = 8;
-constexpr int kRT = 2;  // 16-row weight tiles per CTA
-
 struct Params {
     int64_t M, N, K;
     const void* X;
@@ -51,17 +53,17 @@ struct Params {
 
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
     return v;
 }
 
 __device__ __forceinline__ uint4 ld_cached(const void* p) {
     uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
+    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
     return v;
 }
 
@@ -83,30 +85,40 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
     }
 }
 
-// MT = number of 8-row activation tiles (1 for M <= 8, 2 for M <= 16).
-template <bool kBf16, int MT, typename TOut>
-__global__ void __launch_bounds__(kWarps * 32) skinny_kernel(Params p) {
-    __shared__ float red[kWarps][kRT * 16][MT * 8 + 1];
+// One 32-element K step of a warp: RT weight tiles (two 16-byte loads per
+// lane each: rows g and g+8) and MT activation tiles (one load per lane).
+template <int RT, int MT>
+struct Step {
+    uint4 w[RT][2];
+    uint4 x[MT];
+};
+
+// MT = number of 8-row activation tiles (1 for M <= 8, 2 for M <= 16);
+// RT = 16-row weight tiles per CTA; WARPS split K; PF = K steps of loads
+// kept in flight per warp (software pipeline depth).
+template <bool kBf16, int MT, typename TOut, int RT, int WARPS, int PF>
+__global__ void __launch_bounds__(WARPS * 32) skinny_kernel(Params p) {
+    __shared__ float red[WARPS][RT * 16][MT * 8 + 1];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * (kRT * 16);
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * (RT * 16);
 
     // This warp's K range, in whole 32-element steps.
     const int64_t steps = (p.K + 31) / 32;
-    const int64_t per_warp = (steps + kWarps - 1) / kWarps;
+    const int64_t per_warp = (steps + WARPS - 1) / WARPS;
     const int64_t s_begin = warp * per_warp;
     const int64_t s_end = min(steps, s_begin + per_warp);
 
     const char* W = static_cast<const char*>(p.W);
     const char* X = static_cast<const char*>(p.X);
-    // Row pointers (clamped when the row does not exist; masked below).
-    const char* wrow[kRT][2];
-    bool wok[kRT][2];
+    // Row pointers (clamped when the row does not exist; such loads are skipped).
+    const char* wrow[RT][2];
+    bool wok[RT][2];
 #pragma unroll
-    for (int r = 0; r < kRT; ++r)
+    for (int r = 0; r < RT; ++r)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            int64_t n = n0 + r * 16 + g + h * 8;
+            const int64_t n = n0 + r * 16 + g + h * 8;
             wok[r][h] = n < p.N;
             wrow[r][h] = W + (wok[r][h] ? n : 0) * p.ldw * 2;
         }
@@ -114,48 +126,63 @@ __global__ void __launch_bounds__(kWarps * 32) skinny_kernel(Params p) {
     bool xok[MT];
 #pragma unroll
     for (int m = 0; m < MT; ++m) {
-        int64_t row = m * 8 + g;
+        const int64_t row = m * 8 + g;
         xok[m] = row < p.M;
         xrow[m] = X + (xok[m] ? row : 0) * p.ldx * 2;
     }
 
-    float acc[kRT][MT][4];
+    float acc[RT][MT][4];
 #pragma unroll
-    for (int r = 0; r < kRT; ++r)
+    for (int r = 0; r < RT; ++r)
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[r][m][i] = 0.0f;
 
     const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll 4
-    for (int64_t s = s_begin; s < s_end; ++s) {
+    auto load = [&](Step<RT, MT>& st, int64_t s) {
         const int64_t k = s * 32 + t * 8;  // this lane's 8 consecutive k (K % 8 == 0)
-        const bool kok = k < p.K;
-        uint4 w[kRT][2], x[MT];
+        const bool kok = s < s_end && k < p.K;
 #pragma unroll
-        for (int r = 0; r < kRT; ++r)
+        for (int r = 0; r < RT; ++r)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-                w[r][h] = (kok && wok[r][h]) ? ld_stream(wrow[r][h] + k * 2) : zero;
+                st.w[r][h] = (kok && wok[r][h]) ? ld_stream(wrow[r][h] + k * 2) : zero;
 #pragma unroll
-        for (int m = 0; m < MT; ++m) x[m] = (kok && xok[m]) ? ld_cached(xrow[m] + k * 2) : zero;
+        for (int m = 0; m < MT; ++m) st.x[m] = (kok && xok[m]) ? ld_cached(xrow[m] + k * 2) : zero;
+    };
+    auto compute = [&](const Step<RT, MT>& st) {
 #pragma unroll
-        for (int r = 0; r < kRT; ++r)
+        for (int r = 0; r < RT; ++r)
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 // k-slots {2t,2t+1 | 2t+8,2t+9} <- this lane's k {0,1 | 2,3}, then {4,5 | 6,7}
-                mma16816<kBf16>(acc[r][m], w[r][0].x, w[r][1].x, w[r][0].y, w[r][1].y, x[m].x,
-                                x[m].y);
-                mma16816<kBf16>(acc[r][m], w[r][0].z, w[r][1].z, w[r][0].w, w[r][1].w, x[m].z,
-                                x[m].w);
+                mma16816<kBf16>(acc[r][m], st.w[r][0].x, st.w[r][1].x, st.w[r][0].y,
+                                st.w[r][1].y, st.x[m].x, st.x[m].y);
+                mma16816<kBf16>(acc[r][m], st.w[r][0].z, st.w[r][1].z, st.w[r][0].w,
+                                st.w[r][1].w, st.x[m].z, st.x[m].w);
             }
+    };
+
+    // Software pipeline: PF steps of loads in flight; ring slots are indexed
+    // by compile-time constants so they stay in registers.
+    Step<RT, MT> ring[PF];
+#pragma unroll
+    for (int u = 0; u < PF; ++u) load(ring[u], s_begin + u);
+    for (int64_t s0 = s_begin; s0 < s_end; s0 += PF) {
+#pragma unroll
+        for (int u = 0; u < PF; ++u) {
+            if (s0 + u < s_end) {
+                compute(ring[u]);
+                load(ring[u], s0 + u + PF);
+            }
+        }
     }
 
     // D fragment: (row g, cols 2t, 2t+1) and (row g+8, same cols); rows are
     // weight rows (output columns n), columns are activation rows (m).
 #pragma unroll
-    for (int r = 0; r < kRT; ++r)
+    for (int r = 0; r < RT; ++r)
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             red[warp][r * 16 + g][m * 8 + 2 * t] = acc[r][m][0];
@@ -166,24 +193,29 @@ __global__ void __launch_bounds__(kWarps * 32) skinny_kernel(Params p) {
     __syncthreads();
 
     TOut* Y = static_cast<TOut*>(p.Y);
-    for (int e = threadIdx.x; e < kRT * 16 * MT * 8; e += kWarps * 32) {
-        const int nl = e % (kRT * 16), m = e / (kRT * 16);  // consecutive threads: consecutive n
+    for (int e = threadIdx.x; e < RT * 16 * MT * 8; e += WARPS * 32) {
+        const int nl = e % (RT * 16), m = e / (RT * 16);  // consecutive threads: consecutive n
         const int64_t n = n0 + nl;
         if (m >= p.M || n >= p.N) continue;
         float sum = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) sum += red[w][nl][m];
+        for (int w = 0; w < WARPS; ++w) sum += red[w][nl][m];
         TOut* dst = Y + m * p.ldy + n;
-        float old = p.beta != 0.0f ? OutT<TOut>::load(dst) : 0.0f;
+        const float old = p.beta != 0.0f ? OutT<TOut>::load(dst) : 0.0f;
         OutT<TOut>::store(dst, axpby(p.alpha, sum, p.beta, old));
     }
 }
 
+// Chosen shape (measured on GB300 at N = K = 8192): 32 weight rows per CTA,
+// 8 warps splitting K, 4 K-steps of loads in flight for M <= 8 and 3 for
+// M <= 16 (where a deeper pipeline no longer fits the register budget).
+constexpr int kRT = 2, kWarps = 8, kPF1 = 4, kPF2 = 3;
+
 template <bool kBf16, typename TOut>
 cudaError_t launch_typed(const Params& p, cudaStream_t s) {
     dim3 grid(static_cast<unsigned>((p.N + kRT * 16 - 1) / (kRT * 16)));
-    if (p.M <= 8) skinny_kernel<kBf16, 1, TOut><<<grid, kWarps * 32, 0, s>>>(p);
-    else skinny_kernel<kBf16, 2, TOut><<<grid, kWarps * 32, 0, s>>>(p);
+    if (p.M <= 8) skinny_kernel<kBf16, 1, TOut, kRT, kWarps, kPF1><<<grid, kWarps * 32, 0, s>>>(p);
+    else skinny_kernel<kBf16, 2, TOut, kRT, kWarps, kPF2><<<grid, kWarps * 32, 0, s>>>(p);
     return cudaGetLastError();
 }
 
