@@ -344,7 +344,7 @@ def e2e_leg(w, steps, warmup, device):
     if w.name.startswith("skinny"):
         val, unit = by / (ms * 1e-3) / 1e9, "GB/s"
     else:
-        val, unit = fl / (ms * 1e-3) / 1e12, "TFLOPS"
+        val, unit = fl / (ms * 1e-3) / 1e12, ("TOPS" if w.in_dtype == gen.I8 else "TFLOPS")
     return {"value": val, "unit": unit, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h}
 
@@ -491,17 +491,20 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    # one kernel launch per step on this path: its mean duration is the
-    # timed region over the launches in it
-    kmean = g0.elapsed_time(g1) / max(1, launches)
+    # the dominant kernel's time per launch: the whole call's time per step
+    # (the paths measured here launch one kernel per call; when a call
+    # launches more, their sum is attributed to the call)
+    kmean = g0.elapsed_time(g1) / args.steps
     fl, by = workload_accounting(w)
     if w.name.startswith("skinny"):
         value, unit = world * by / (ms_per_step * 1e-3) / 1e9, "GB/s"
     else:
-        value, unit = world * fl / (ms_per_step * 1e-3) / 1e12, "TFLOPS"
+        value = world * fl / (ms_per_step * 1e-3) / 1e12
+        unit = "TOPS" if w.in_dtype == gen.I8 else "TFLOPS"
     roof = roofline_for(w, kmean, peaks)
     roof["traffic"] = traffic_record(source_of(w), w.name)
     roof["kernel_ms_mean"] = kmean
+    roof["launches_per_step"] = launches / args.steps
 
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

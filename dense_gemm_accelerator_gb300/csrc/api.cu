@@ -137,8 +137,27 @@ bool path_accepts(int path, const GemmArgs& g) {
     }
 }
 
-size_t workspace_for(int path, const GemmArgs& g) {
+// Workspace the call cannot run without.
+size_t workspace_required(int path, const GemmArgs& g) {
     return path == DGA_PATH_TCGEN05 ? tc_workspace_size(g) : 0;
+}
+
+// SM count of the current device for size queries made without a GPU: the
+// real count when the device can be queried, else 152 (GB300).
+int sm_count_or_default() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+        return n;
+    cudaGetLastError();  // clear the failed query
+    return 152;
+}
+
+// Workspace the call would use if given: required bytes, or for the SIMT
+// path the optional bytes of its split last wave.
+size_t workspace_wanted(int path, const GemmArgs& g) {
+    if (path == DGA_PATH_SIMT) return simt_workspace_size(g, sm_count_or_default());
+    return workspace_required(path, g);
 }
 
 int fail_cuda(cudaError_t e) {
@@ -197,12 +216,12 @@ int dga_gemm_ex(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, in
 
     const int chosen = path == DGA_PATH_AUTO ? choose_path(g) : static_cast<int>(path);
     if (!path_accepts(chosen, g)) return DGA_ERR_PATH;
-    if (workspace_bytes < workspace_for(chosen, g)) return DGA_ERR_WORKSPACE;
+    if (workspace_bytes < workspace_required(chosen, g)) return DGA_ERR_WORKSPACE;
 
     int launches = 0;
     switch (chosen) {
     case DGA_PATH_GENERIC: e = generic_launch(g, &launches); break;
-    case DGA_PATH_SIMT: e = simt_launch(g, &launches); break;
+    case DGA_PATH_SIMT: e = simt_launch(g, dev, &launches); break;
     case DGA_PATH_SKINNY: e = skinny_launch(g, &launches); break;
     case DGA_PATH_TCGEN05: e = tc_launch(g, dev, &launches); break;
     default: return DGA_ERR_PATH;
@@ -241,7 +260,7 @@ size_t dga_gemm_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype, dga_layo
         probe.B = aligned16;
         chosen = choose_path(probe);
     }
-    return workspace_for(chosen, g);
+    return workspace_wanted(chosen, g);
 }
 
 int dga_select_path(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M,

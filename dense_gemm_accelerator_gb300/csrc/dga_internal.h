@@ -57,7 +57,9 @@ bool generic_supports(const GemmArgs& a);
 cudaError_t generic_launch(const GemmArgs& a, int* launches);
 
 bool simt_supports(const GemmArgs& a);
-cudaError_t simt_launch(const GemmArgs& a, int* launches);
+// Optional workspace: with this many bytes the last wave is split along K.
+size_t simt_workspace_size(const GemmArgs& a, int sm_count);
+cudaError_t simt_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);
 
 bool skinny_supports(const GemmArgs& a);
 cudaError_t skinny_launch(const GemmArgs& a, int* launches);

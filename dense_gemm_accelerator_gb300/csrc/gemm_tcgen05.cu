@@ -19,7 +19,7 @@
 //   * Warp 1 (one lane) issues tcgen05.mma (M = 128, N = 256, K = 16; four per
 //     stage) into an fp32 accumulator in tensor memory, and tcgen05.commit to
 //     release each stage and, after the last K block, the accumulator.
-//   * Warps 2-5 are the epilogue: tcgen05.ld moves the accumulator to
+//   * Warps 2-5 are the epilogue (INT8: warps 2-17, see below): tcgen05.ld moves the accumulator to
 //     registers, 32 columns at a time, for the fused alpha/beta update and the
 //     masked store.  TMEM holds two accumulators (2 x 256 of its 512
 //     columns), so the epilogue of tile i overlaps the main loop of tile i+1.
@@ -31,21 +31,27 @@
 // Operands reach the kernel K-major (A row-major, B column-major).  Other
 // layouts -- row-major B, a leading dimension TMA cannot express, or INT8
 // inputs (encoded exactly as bf16, see below) -- are first repacked into the
-// caller's workspace by pack_kmajor_kernel.
+// caller's workspace by pack_rows_kernel / pack_transposed_kernel.
 //
 // INT8 x INT8 -> INT32 (tcgen05 has no integer MMA on sm_103a: ptxas rejects
 // kind::i8 for this target).  Every int8 value is an exact bf16, every
 // product of two is an integer of magnitude <= 2^14, and the tensor core
-// accumulates in fp32.  The K loop is cut into chunks of 512: within a chunk
-// every partial sum is an integer of magnitude <= 512 * 2^14 = 2^23, which
+// accumulates in fp32.  The K loop is cut into chunks of 256: within a chunk
+// every partial sum is an integer of magnitude <= 256 * 2^14 = 2^22, which
 // fp32 represents exactly, so each chunk's fp32 accumulator is the exact
-// integer chunk sum.  The epilogue converts each chunk result to int32 and
-// adds it into int32 registers (two's-complement wrap), so the final sum is
-// exact for any K.
+// integer chunk sum.  The epilogue turns each chunk result x into an integer
+// with one fp32 add: x + 1.5 * 2^23 lies in [2^23, 2^24], where fp32 spacing
+// is 1 (2^24 itself is exact), so the sum is exact and its bit pattern is
+// 0x4B400000 + x.  Those bit patterns are added in int32 registers
+// (two's-complement wrap) and n_chunks * 0x4B400000 is subtracted at the
+// end, so the final sum is exact for any K.  Sixteen epilogue warps (64
+// columns each) keep each chunk's TMEM reads short, because the MMA of chunk
+// c+2 must wait until the epilogue has drained chunk c from the same buffer.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "dga_internal.h"
@@ -63,7 +69,9 @@ constexpr int BK = 64;   // K per stage: 64 x 2 bytes = one 128-byte swizzle row
 constexpr int UK = 16;   // K per tcgen05.mma (kind::f16)
 constexpr int kStages = 4;
 constexpr int kGroupM = 16;  // tile-rows per raster group
-constexpr int kI8ChunkBlocks = 8;  // INT8: K blocks per exact fp32 chunk (8 x 64 = 512)
+constexpr int kI8ChunkBlocks = 4;  // INT8: K blocks per exact fp32 chunk (4 x 64 = 256)
+constexpr float kI8Magic = 12582912.0f;      // 1.5 * 2^23
+constexpr uint32_t kI8MagicBits = 0x4B400000u;  // its bit pattern
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
 enum : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
@@ -81,9 +89,10 @@ struct TcParams {
 // Shared-memory plan (dynamic, 1024-byte aligned): the stage ring, the
 // barriers, then one 32 x 33 staging square per epilogue warp (the padding
 // column keeps both the row-wise writes and the column-wise reads free of
-// bank conflicts).  BN is the tile width; kEpiWarps is 4 for floating point,
-// 8 for INT8 (two warps per TMEM lane quarter, each owning half the columns).
-template <int BN, int kEpiWarps>
+// bank conflicts).  BN is the tile width; kSquares is 4 for floating point
+// (one per epilogue warp) and 8 for INT8, whose 16 epilogue warps share them
+// in two rounds.
+template <int BN, int kSquares>
 struct Smem {
     static constexpr uint32_t kABytes = BM * BK * 2;
     static constexpr uint32_t kBBytes = BN * BK * 2;
@@ -94,7 +103,7 @@ struct Smem {
     static constexpr uint32_t kBarBytes = (2 * kStages + 5) * 8 + 16;
     static constexpr uint32_t kEpiOffset = (kBarOffset + kBarBytes + 127) / 128 * 128;
     static constexpr uint32_t kEpiWarpBytes = 32 * 33 * 4;
-    static constexpr uint32_t kTotal = kEpiOffset + kEpiWarps * kEpiWarpBytes;
+    static constexpr uint32_t kTotal = kEpiOffset + kSquares * kEpiWarpBytes;
     static constexpr uint32_t kLaunchBytes = kTotal + 1024;  // + alignment slack
 };
 
@@ -170,11 +179,11 @@ __device__ __forceinline__ void store_block_staged_i32(const TcParams& p, uint32
 // BN: tile columns.  Epilogue warps: 4 (float) or 8 (INT8: two column halves).
 
 template <bool kBf16, bool kI8, int BN, typename TOut>
-__global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
+__global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    TcParams p) {
-    constexpr int kEpiWarps = kI8 ? 8 : 4;
-    using S = Smem<BN, kEpiWarps>;
+    constexpr int kEpiWarps = kI8 ? 16 : 4;
+    using S = Smem<BN, kI8 ? 8 : 4>;
     constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
     constexpr uint32_t kIdesc = idesc_f16(kBf16, BM, BN);
 
@@ -301,10 +310,12 @@ __global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
         // ------------------------------------------------ epilogue warps
         const int ew = warp - 2;              // 0 .. kEpiWarps-1
         const int quarter = warp & 3;         // TMEM lanes this warp may access
-        const int col_half = kI8 ? (ew >> 2) : 0;  // INT8: which half of the columns
-        constexpr int kColsPerWarp = kI8 ? BN / 2 : BN;
+        // INT8: four warps per lane quarter, each owning a quarter of the columns
+        const int col_half = kI8 ? (ew >> 2) : 0;
+        constexpr int kColsPerWarp = kI8 ? BN / 4 : BN;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        uint32_t* stage = reinterpret_cast<uint32_t*>(smem + S::kEpiOffset + ew * S::kEpiWarpBytes);
+        uint32_t* stage =
+            reinterpret_cast<uint32_t*>(smem + S::kEpiOffset + (ew & 7) * S::kEpiWarpBytes);
         uint32_t acc = 0, acc_phase = 0;
         bool ok = true;
         for (uint32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
@@ -348,10 +359,10 @@ __global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
                         tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            // exact integer in fp32 -> int32, wrapping add
-                            const int32_t chunk = __float2int_rn(__uint_as_float(r[j]));
+                            // exact integer x in fp32 -> bits of x + 1.5*2^23 = 0x4B400000 + x
+                            const float shifted = __fadd_rn(__uint_as_float(r[j]), kI8Magic);
                             sum[c * 32 + j] = static_cast<int32_t>(
-                                static_cast<uint32_t>(sum[c * 32 + j]) + static_cast<uint32_t>(chunk));
+                                static_cast<uint32_t>(sum[c * 32 + j]) + __float_as_uint(shifted));
                         }
                     }
                     tc_fence_before();
@@ -359,9 +370,21 @@ __global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
                     if (++acc == 2) { acc = 0; acc_phase ^= 1; }
                 }
                 if (!ok) break;
+                const uint32_t bias = n_chunks * kI8MagicBits;  // wraps mod 2^32, as the sums do
 #pragma unroll
-                for (int c = 0; c < kColsPerWarp / 32; ++c)
-                    store_block_staged_i32(p, stage, lane, row_base, col0 + c * 32, &sum[c * 32]);
+                for (int j = 0; j < kColsPerWarp; ++j)
+                    sum[j] = static_cast<int32_t>(static_cast<uint32_t>(sum[j]) - bias);
+                // 16 warps, 8 staging squares: warps 0-7 store first, then 8-15
+                // (named barrier 1 over the 512 epilogue threads).
+                for (int round = 0; round < 2; ++round) {
+                    if ((ew >> 3) == round) {
+#pragma unroll
+                        for (int c = 0; c < kColsPerWarp / 32; ++c)
+                            store_block_staged_i32(p, stage, lane, row_base, col0 + c * 32,
+                                                   &sum[c * 32]);
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+                }
             }
         }
     }
@@ -377,44 +400,85 @@ __global__ void __launch_bounds__(kI8 ? 320 : 192, 1)
 
 // ---- operand repacking into the workspace ------------------------------------
 //
-// dst[r][k] = src(r, k) converted to bf16/fp16 storage, for r < rows, k < K;
-// zero for K <= k < ld_dst.  src(r, k) = src[r*ld_src + k] (k-contiguous) or
-// src[k*ld_src + r] (transposed).  A 32 x 32 tile goes through shared memory
-// so that both the read and the write are coalesced.
+// dst[r][k] = src(r, k) converted to 16-bit storage (bf16/fp16; int8 values
+// become exact bf16), for r < rows, k < K, and zero for K <= k < ld_dst.
+// ld_dst is a multiple of 8, so every thread writes whole 16-byte vectors.
+// src(r, k) = src[r*ld_src + k] (k-contiguous) or src[k*ld_src + r]
+// (transposed, e.g. a row-major B that the tensor cores need K-major).
 
-template <typename TSrc, typename TDst>
-__device__ __forceinline__ TDst convert_elem(TSrc v);
-template <> __device__ __forceinline__ __nv_bfloat16 convert_elem(__nv_bfloat16 v) { return v; }
-template <> __device__ __forceinline__ __half convert_elem(__half v) { return v; }
-template <> __device__ __forceinline__ __nv_bfloat16 convert_elem(int8_t v) {
-    return __float2bfloat16_rn(static_cast<float>(v));  // exact: |v| <= 128
+template <typename TSrc> struct PackIn;
+template <> struct PackIn<int8_t> {
+    __device__ __forceinline__ static uint16_t bits(int8_t v) {  // exact: |v| <= 128
+        return __bfloat16_as_ushort(__float2bfloat16_rn(static_cast<float>(v)));
+    }
+};
+template <> struct PackIn<__nv_bfloat16> {
+    __device__ __forceinline__ static uint16_t bits(__nv_bfloat16 v) { return __bfloat16_as_ushort(v); }
+};
+template <> struct PackIn<__half> {
+    __device__ __forceinline__ static uint16_t bits(__half v) { return __half_as_ushort(v); }
+};
+
+__device__ __forceinline__ uint4 pack8(const uint16_t (&h)[8]) {
+    return make_uint4(h[0] | (uint32_t(h[1]) << 16), h[2] | (uint32_t(h[3]) << 16),
+                      h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
 }
 
-template <typename TSrc, typename TDst, bool kTransposed>
-__global__ void __launch_bounds__(256) pack_kmajor_kernel(const TSrc* __restrict__ src,
-                                                          int64_t ld_src, int64_t rows,
-                                                          int64_t K, TDst* __restrict__ dst,
-                                                          int64_t ld_dst) {
-    __shared__ TSrc tile[32][33];
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32;
-    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
-    for (int i = ty; i < 32; i += 8) {
-        if constexpr (kTransposed) {
-            // read along r (contiguous in memory): tile[k][r]
-            const int64_t k = k0 + i, r = r0 + tx;
-            tile[i][tx] = (k < K && r < rows) ? src[k * ld_src + r] : TSrc(0);
+// k-contiguous source: one thread per 8 consecutive k of a row (grid-stride).
+template <typename TSrc>
+__global__ void __launch_bounds__(256) pack_rows_kernel(const TSrc* __restrict__ src, int64_t ld_src,
+                                                        int64_t rows, int64_t K,
+                                                        uint16_t* __restrict__ dst, int64_t ld_dst,
+                                                        int vec_src) {
+    const int64_t groups = ld_dst / 8;
+    const int64_t total = rows * groups;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / groups, k = (i % groups) * 8;
+        const TSrc* s = src + r * ld_src + k;
+        uint16_t h[8];
+        if (vec_src && k + 8 <= K) {
+            // 8 elements in one load: 8 bytes of int8 or 16 bytes of 16-bit data
+            TSrc v[8];
+            if constexpr (sizeof(TSrc) == 1) *reinterpret_cast<uint2*>(v) = __ldg(reinterpret_cast<const uint2*>(s));
+            else *reinterpret_cast<uint4*>(v) = __ldg(reinterpret_cast<const uint4*>(s));
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[j] = PackIn<TSrc>::bits(v[j]);
         } else {
-            const int64_t r = r0 + i, k = k0 + tx;
-            tile[i][tx] = (r < rows && k < K) ? src[r * ld_src + k] : TSrc(0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[j] = k + j < K ? PackIn<TSrc>::bits(s[j]) : uint16_t(0);
         }
+        *reinterpret_cast<uint4*>(dst + r * ld_dst + k) = pack8(h);
+    }
+}
+
+// Transposed source: a 64 (k) x 64 (r) tile per block through shared memory;
+// reads walk r (contiguous in the source), writes walk k (16-byte vectors).
+template <typename TSrc>
+__global__ void __launch_bounds__(256) pack_transposed_kernel(const TSrc* __restrict__ src,
+                                                              int64_t ld_src, int64_t rows,
+                                                              int64_t K, uint16_t* __restrict__ dst,
+                                                              int64_t ld_dst) {
+    __shared__ uint16_t tile[64][64 + 2];  // tile[k][r], already converted
+    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 64;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;
+    const int t = threadIdx.x;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+        const int idx = i * 256 + t, kk = idx >> 6, rr = idx & 63;
+        const int64_t k = k0 + kk, r = r0 + rr;
+        tile[kk][rr] = (k < K && r < rows) ? PackIn<TSrc>::bits(src[k * ld_src + r]) : uint16_t(0);
     }
     __syncthreads();
-    for (int i = ty; i < 32; i += 8) {
-        const int64_t r = r0 + i, k = k0 + tx;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int idx = i * 256 + t, rr = idx >> 3, kq = (idx & 7) * 8;
+        const int64_t r = r0 + rr, k = k0 + kq;
         if (r < rows && k < ld_dst) {
-            TSrc v = kTransposed ? tile[tx][i] : tile[i][tx];
-            dst[r * ld_dst + k] = (k < K) ? convert_elem<TSrc, TDst>(v) : convert_elem<TSrc, TDst>(TSrc(0));
+            uint16_t h[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) h[j] = tile[kq + j][rr];
+            *reinterpret_cast<uint4*>(dst + r * ld_dst + k) = pack8(h);
         }
     }
 }
@@ -498,21 +562,26 @@ cudaError_t launch_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const Tc
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(std::min<uint32_t>(p.num_tiles, dev.sm_count));
-    kern<<<grid, kI8 ? 320 : 192, smem, s>>>(ma, mb, p);
+    kern<<<grid, kI8 ? 576 : 192, smem, s>>>(ma, mb, p);
     return cudaGetLastError();
 }
 
-template <typename TSrc, typename TDst>
+template <typename TSrc>
 cudaError_t launch_pack(const void* src, int64_t ld_src, bool transposed, int64_t rows,
-                        int64_t K, void* dst, int64_t ld_dst, cudaStream_t s) {
-    dim3 grid(static_cast<unsigned>((ld_dst + 31) / 32), static_cast<unsigned>((rows + 31) / 32));
-    if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-    if (transposed)
-        pack_kmajor_kernel<TSrc, TDst, true><<<grid, 256, 0, s>>>(
-            static_cast<const TSrc*>(src), ld_src, rows, K, static_cast<TDst*>(dst), ld_dst);
-    else
-        pack_kmajor_kernel<TSrc, TDst, false><<<grid, 256, 0, s>>>(
-            static_cast<const TSrc*>(src), ld_src, rows, K, static_cast<TDst*>(dst), ld_dst);
+                        int64_t K, void* dst, int64_t ld_dst, int sm_count, cudaStream_t s) {
+    if (transposed) {
+        dim3 grid(static_cast<unsigned>((ld_dst + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+        if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+        pack_transposed_kernel<TSrc><<<grid, 256, 0, s>>>(static_cast<const TSrc*>(src), ld_src,
+                                                          rows, K, static_cast<uint16_t*>(dst), ld_dst);
+    } else {
+        const int vec = (ld_src * static_cast<int64_t>(sizeof(TSrc))) % (8 * sizeof(TSrc)) == 0 &&
+                        aligned(src, 8 * sizeof(TSrc));
+        const int64_t work = rows * (ld_dst / 8);
+        const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sm_count) * 16);
+        pack_rows_kernel<TSrc><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
+            static_cast<const TSrc*>(src), ld_src, rows, K, static_cast<uint16_t*>(dst), ld_dst, vec);
+    }
     return cudaGetLastError();
 }
 
@@ -547,9 +616,9 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     if (pl.pack_a) {
         void* dst = ws;
-        if (i8) e = launch_pack<int8_t, __nv_bfloat16>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, a.stream);
-        else if (bf16) e = launch_pack<__nv_bfloat16, __nv_bfloat16>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, a.stream);
-        else e = launch_pack<__half, __half>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, a.stream);
+        if (i8) e = launch_pack<int8_t>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        else if (bf16) e = launch_pack<__nv_bfloat16>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        else e = launch_pack<__half>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
         if (e != cudaSuccess) return e;
         ++*launches;
         A = dst;
@@ -558,9 +627,9 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     if (pl.pack_b) {
         void* dst = ws + pl.a_bytes;
         const bool tr = a.layout_b == DGA_ROW_MAJOR;  // B(k, j) = B[k*ldb + j]: transpose to N x K
-        if (i8) e = launch_pack<int8_t, __nv_bfloat16>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, a.stream);
-        else if (bf16) e = launch_pack<__nv_bfloat16, __nv_bfloat16>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, a.stream);
-        else e = launch_pack<__half, __half>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, a.stream);
+        if (i8) e = launch_pack<int8_t>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        else if (bf16) e = launch_pack<__nv_bfloat16>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        else e = launch_pack<__half>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
         if (e != cudaSuccess) return e;
         ++*launches;
         B = dst;

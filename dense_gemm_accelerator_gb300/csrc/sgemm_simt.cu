@@ -19,14 +19,20 @@
 //     warp stages 32 consecutive rows at one k, so the transposing stores hit
 //     32 consecutive words (no bank conflicts), and the 8 A values a thread
 //     needs per k are two 128-bit broadcast loads;
-//   * tiles that lie wholly inside the matrices (and K a multiple of 16) run
-//     a copy of the main loop without any bounds checks; edge tiles load
-//     zeros outside M, N and K and mask their stores.
+//   * tiles that lie wholly inside the matrices (and a K range that is a
+//     whole number of slices) run a copy of the main loop without any bounds
+//     checks; edge tiles load zeros outside M, N and K and mask their stores;
+//   * problems with fewer tiles than resident blocks cut every tile along K
+//     into 2-4 ranges whose partial sums go to the caller's workspace and are
+//     added in a fixed order by a second small kernel, so that most SMs are
+//     not left idle.
 //
 // Thread layout: 8 warps tile the block as 2 (M) x 4 (N) warp tiles of
 // 64 x 32; inside a warp, lane = lm * 4 + ln with lm in 0..7, ln in 0..3.  A
 // thread owns rows {wm*64 + lm*4 + i, wm*64 + 32 + lm*4 + i} and columns
 // {wn*32 + ln*4 + j, wn*32 + 16 + ln*4 + j}, i, j in 0..3.
+#include <algorithm>
+
 #include "dga_internal.h"
 #include "epilogue.cuh"
 
@@ -50,6 +56,13 @@ struct Params {
     int vec_c;  // C is 16-byte aligned and ldc % 4 == 0: float4 epilogue
     int vec_a;  // A 16-byte aligned and lda % 4 == 0: float4 loads of A
     int vec_b;  // the same for B
+    // Tile schedule: tile t covers rows (t / tiles_n)*BM, columns (t % tiles_n)*BN.
+    // Blocks below full_tiles own one tile each; each block above owns one of
+    // `parts` K-ranges (part_k deep) of a tail tile and writes its partial
+    // product to `partials` (BM x BN floats per block, row-major).
+    int64_t tiles_n, full_tiles, part_k;
+    int parts;
+    float* partials;
 };
 
 struct Smem {
@@ -71,10 +84,13 @@ __device__ __forceinline__ float4 ld_f4_checked(const float* row, int64_t col, i
     return make_float4(v[0], v[1], v[2], v[3]);
 }
 
-// One block tile; kChecked = false only for tiles wholly inside M, N with
-// K % BK == 0 and 16-byte-friendly A and B.
+// One block tile over K in [k_begin, k_end).  kChecked = false only for
+// tiles wholly inside M, N whose K range is a whole number of slices, with
+// 16-byte-friendly A and B.  `partial` non-null: write the raw accumulators
+// there (BM x BN, row-major) instead of the alpha/beta epilogue.
 template <bool kChecked>
-__device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t row0, int64_t col0) {
+__device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t row0, int64_t col0,
+                                           int64_t k_begin, int64_t k_end, float* partial) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 
@@ -96,8 +112,8 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
             ra = ld_f4(a_src + k0 + a_k);
             rb = ld_f4(b_src + (k0 + b_k) * p.ldb);
         } else {
-            ra = ld_f4_checked(a_src, k0 + a_k, p.K, a_ok, vec_a);
-            const bool kok = k0 + b_k < p.K;
+            ra = ld_f4_checked(a_src, k0 + a_k, k_end, a_ok, vec_a);
+            const bool kok = k0 + b_k < k_end;
             rb = ld_f4_checked(p.B + (kok ? k0 + b_k : 0) * p.ldb, col0 + b_c, p.N, kok, vec_b);
         }
     };
@@ -121,14 +137,14 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
 
-    const int64_t n_slices = (p.K + BK - 1) / BK;
-    fetch(0);
+    const int64_t n_slices = (k_end - k_begin + BK - 1) / BK;
+    fetch(k_begin);
     stash(0);
     __syncthreads();
     for (int64_t s = 0; s < n_slices; ++s) {
         const int buf = static_cast<int>(s & 1);
         const bool more = s + 1 < n_slices;
-        if (more) fetch((s + 1) * BK);
+        if (more) fetch(k_begin + (s + 1) * BK);
         // Fragments are double-buffered in registers: the shared-memory loads
         // for k+1 are issued before the 64 FFMAs of k.
         float a[2][8], b[2][8];
@@ -151,6 +167,17 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
         // that ended it, so it can be overwritten now.
         if (more) stash(buf ^ 1);
         __syncthreads();
+    }
+
+    if (partial != nullptr) {
+        // a K-range of a tail tile: raw partial sums, reduced by sgemm_tail_reduce
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float* prow = partial + (i < 4 ? am0 + i : am1 + (i - 4)) * BN;
+            *reinterpret_cast<float4*>(prow + bn0) = *reinterpret_cast<const float4*>(&acc[i][0]);
+            *reinterpret_cast<float4*>(prow + bn1) = *reinterpret_cast<const float4*>(&acc[i][4]);
+        }
+        return;
     }
 
     // Epilogue: out = alpha*acc + beta*C, float4 where aligned, masked at edges.
@@ -189,31 +216,130 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
 template <int kMinBlocks>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) sgemm_128x128_kernel(Params p) {
     __shared__ __align__(16) Smem sm;
-    const int64_t row0 = static_cast<int64_t>(blockIdx.y) * BM;
-    const int64_t col0 = static_cast<int64_t>(blockIdx.x) * BN;
-    const bool interior = row0 + BM <= p.M && col0 + BN <= p.N && p.K % BK == 0 &&
+    const int64_t b = blockIdx.x;
+    int64_t tile, k_begin = 0, k_end = p.K;
+    float* partial = nullptr;
+    if (b < p.full_tiles) {
+        tile = b;
+    } else {
+        const int64_t u = b - p.full_tiles;
+        tile = p.full_tiles + u / p.parts;
+        k_begin = (u % p.parts) * p.part_k;
+        k_end = min(p.K, k_begin + p.part_k);
+        partial = p.partials + u * (BM * BN);
+    }
+    const int64_t row0 = (tile / p.tiles_n) * BM;
+    const int64_t col0 = (tile % p.tiles_n) * BN;
+    const bool interior = row0 + BM <= p.M && col0 + BN <= p.N && (k_end - k_begin) % BK == 0 &&
                           p.vec_a && p.vec_b;
-    if (interior) block_tile<false>(p, sm, row0, col0);
-    else block_tile<true>(p, sm, row0, col0);
+    if (interior) block_tile<false>(p, sm, row0, col0, k_begin, k_end, partial);
+    else block_tile<true>(p, sm, row0, col0, k_begin, k_end, partial);
+}
+
+// Sums the K-range partials of each tail tile in part order (so the result
+// does not depend on which block finished first) and applies the epilogue.
+__global__ void __launch_bounds__(kThreads) sgemm_tail_reduce(Params p) {
+    const int64_t tile = p.full_tiles + blockIdx.x;
+    const int64_t row0 = (tile / p.tiles_n) * BM;
+    const int64_t col0 = (tile % p.tiles_n) * BN;
+    const float* base = p.partials + static_cast<int64_t>(blockIdx.x) * p.parts * (BM * BN);
+    for (int e = threadIdx.x; e < BM * BN / 4; e += kThreads) {
+        const int r = e / (BN / 4), c = (e % (BN / 4)) * 4;
+        float4 sum = *reinterpret_cast<const float4*>(base + r * BN + c);
+        for (int q = 1; q < p.parts; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(base + q * (BM * BN) + r * BN + c);
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+        }
+        const int64_t row = row0 + r, col = col0 + c;
+        if (row >= p.M) continue;
+        float* crow = p.C + row * p.ldc;
+        const float v[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (col + j < p.N) {
+                const float old = p.beta != 0.0f ? crow[col + j] : 0.0f;
+                crow[col + j] = axpby(p.alpha, v[j], p.beta, old);
+            }
+        }
+    }
+}
+
+// How the tiles are scheduled.  With at least one full wave of tiles, whole
+// tiles only: a block alone on its SM in the last, partial wave runs faster
+// than paired blocks do, and splitting that wave along K measured slower at
+// 4096^3 on GB300.  With fewer tiles than resident blocks, most SMs would
+// idle, so every tile is cut along K into `parts` ranges (2-4, each at least
+// 256 deep) whose partial sums are added afterwards.  parts == 1: no split.
+struct Schedule {
+    int64_t tiles, tiles_n, full_tiles, part_k;
+    int parts;
+    size_t partial_bytes;
+};
+
+Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int sm_count) {
+    Schedule sc{};
+    sc.tiles_n = (N + BN - 1) / BN;
+    sc.tiles = ((M + BM - 1) / BM) * sc.tiles_n;
+    sc.full_tiles = sc.tiles;
+    sc.parts = 1;
+    sc.part_k = K;
+    const int64_t slots = static_cast<int64_t>(kSimtBlocksPerSm) * sm_count;
+    if (slots <= 0 || sc.tiles >= slots) return sc;
+    const int64_t tail = sc.tiles;
+    int64_t parts = std::min<int64_t>(4, slots / tail);
+    parts = std::min<int64_t>(parts, K / 256);  // keep every part at least 256 deep
+    if (parts < 2) return sc;
+    const int64_t part_k = ((K + parts - 1) / parts + BK - 1) / BK * BK;
+    parts = (K + part_k - 1) / part_k;
+    if (parts < 2) return sc;
+    sc.full_tiles = sc.tiles - tail;
+    sc.parts = static_cast<int>(parts);
+    sc.part_k = part_k;
+    sc.partial_bytes = static_cast<size_t>(tail) * parts * BM * BN * sizeof(float);
+    return sc;
 }
 
 }  // namespace
 
 bool simt_supports(const GemmArgs& a) {
-    return a.in_dtype == DGA_F32 && a.out_dtype == DGA_F32 && a.layout_b == DGA_ROW_MAJOR &&
-           (a.M + BM - 1) / BM <= 65535;
+    return a.in_dtype == DGA_F32 && a.out_dtype == DGA_F32 && a.layout_b == DGA_ROW_MAJOR;
 }
 
-cudaError_t simt_launch(const GemmArgs& a, int* launches) {
+size_t simt_workspace_size(const GemmArgs& a, int sm_count) {
+    return plan_schedule(a.M, a.N, a.K, sm_count).partial_bytes;
+}
+
+cudaError_t simt_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
+    Schedule sc = plan_schedule(a.M, a.N, a.K, dev.sm_count);
+    if (sc.parts > 1 && (a.ws == nullptr || a.ws_bytes < sc.partial_bytes)) {
+        // not enough workspace for the split tail: whole tiles only
+        sc.full_tiles = sc.tiles;
+        sc.parts = 1;
+        sc.part_k = a.K;
+    }
     Params p{a.M, a.N, a.K, static_cast<const float*>(a.A), a.lda,
              static_cast<const float*>(a.B), a.ldb, static_cast<float*>(a.C), a.ldc,
              a.alpha_f, a.beta_f, (a.ldc % 4 == 0 && aligned(a.C, 16)) ? 1 : 0,
-             (a.lda % 4 == 0 && aligned(a.A, 16)) ? 1 : 0, (a.ldb % 4 == 0 && aligned(a.B, 16)) ? 1 : 0};
-    dim3 grid(static_cast<unsigned>((a.N + BN - 1) / BN), static_cast<unsigned>((a.M + BM - 1) / BM));
-    sgemm_128x128_kernel<kSimtBlocksPerSm><<<grid, kThreads, 0, a.stream>>>(p);
+             (a.lda % 4 == 0 && aligned(a.A, 16)) ? 1 : 0, (a.ldb % 4 == 0 && aligned(a.B, 16)) ? 1 : 0,
+             sc.tiles_n, sc.full_tiles, sc.part_k, sc.parts,
+             sc.parts > 1 ? static_cast<float*>(a.ws) : nullptr};
+    const int64_t tail = sc.tiles - sc.full_tiles;
+    const int64_t blocks = sc.full_tiles + tail * sc.parts;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    sgemm_128x128_kernel<kSimtBlocksPerSm><<<static_cast<unsigned>(blocks), kThreads, 0, a.stream>>>(p);
     cudaError_t e = cudaGetLastError();
-    if (e == cudaSuccess) ++*launches;
-    return e;
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    if (tail > 0 && sc.parts > 1) {
+        sgemm_tail_reduce<<<static_cast<unsigned>(tail), kThreads, 0, a.stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        ++*launches;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace dga

@@ -99,8 +99,15 @@ typedef enum {
  *   B, ldb               device pointer, see dga_layout
  *   C, ldc               device pointer, C(i, j) = C[i*ldc + j], ldc >= max(1, N)
  *   workspace            device scratch of at least workspace_bytes, or NULL
- *   workspace_bytes      must be >= dga_gemm_workspace_size() for these args
- *                        (0 for every path but INT8 on the tensor cores)
+ *   workspace_bytes      bytes at `workspace`.  The tensor-core path needs
+ *                        dga_gemm_workspace_size() bytes when it repacks
+ *                        operands (INT8 inputs, row-major B, leading
+ *                        dimensions TMA cannot express) and fails with
+ *                        DGA_ERR_WORKSPACE without them.  The FP32 SIMT path
+ *                        uses workspace only if given enough: then the tiles
+ *                        of its last, partial wave are split along K (faster
+ *                        for shapes whose tile count is not a multiple of the
+ *                        resident blocks); with less it runs whole tiles.
  *   stream               CUDA stream the kernels are enqueued on
  *
  * M == 0 or N == 0 returns DGA_OK and touches no memory.  Returns a status
@@ -122,9 +129,12 @@ int dga_gemm_ex(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
                 void* workspace, size_t workspace_bytes, dga_path path,
                 dga_stream_t stream);
 
-/* Bytes of workspace dga_gemm_ex needs for these arguments on `path`
- * (DGA_PATH_AUTO: the path dga_gemm would choose).  Pointers are not needed:
- * the answer depends on dtypes, layout, sizes and leading dimensions only. */
+/* Bytes of workspace dga_gemm_ex can use for these arguments on `path`
+ * (DGA_PATH_AUTO: the path dga_gemm would choose): required bytes for the
+ * tensor-core path, optional bytes for the SIMT path (see dga_gemm).
+ * Pointers are not needed: the answer depends on dtypes, layout, sizes,
+ * leading dimensions and the current device's SM count (152 is assumed when
+ * no device can be queried). */
 size_t dga_gemm_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
                                int64_t M, int64_t N, int64_t K,
                                int64_t lda, int64_t ldb, int64_t ldc, dga_path path);

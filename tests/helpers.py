@@ -21,7 +21,7 @@ TORCH = gen.TORCH_DTYPE
 
 
 def run_gpu(path, in_dtype, out_dtype, layout_b, A, B, C, alpha, beta, lda=None, ldb=None,
-            ldc=None, M=None, N=None, K=None, offsets=(0, 0, 0), expect=dga.OK):
+            ldc=None, M=None, N=None, K=None, offsets=(0, 0, 0), expect=dga.OK, workspace=True):
     """Copy host buffers to the GPU, call dga_gemm_ex through the C ABI and
     return C as a host tensor (same shape as the host C buffer).
 
@@ -53,13 +53,15 @@ def run_gpu(path, in_dtype, out_dtype, layout_b, A, B, C, alpha, beta, lda=None,
     # the size query assumes aligned pointers; packing never needs more than
     # one M x K and one N x K bf16 copy (plus alignment)
     ws_bytes = max(ws_bytes, 2 * (M + N) * ((K + 7) // 8 * 8) + 1024)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if not workspace:
+        ws_bytes = 0
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     al = dga.scalar(alpha, in_dtype)
     be = dga.scalar(beta, in_dtype)
     stream = torch.cuda.current_stream().cuda_stream
     st = dga.dga_gemm_ex(in_dtype, out_dtype, layout_b, M, N, K, ctypes.byref(al), a_ptr, lda,
-                         b_ptr, ldb, ctypes.byref(be), c_ptr, ldc, ws.data_ptr(), ws_bytes, path,
-                         stream)
+                         b_ptr, ldb, ctypes.byref(be), c_ptr, ldc,
+                         ws.data_ptr() if ws_bytes else None, ws_bytes, path, stream)
     assert st == expect, f"dga_gemm_ex returned {st} ({dga.dga_status_string(st)})"
     sync = dga.dga_sync_status(stream)
     assert sync == dga.OK, dga.dga_status_string(sync)

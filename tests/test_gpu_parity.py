@@ -75,6 +75,22 @@ def test_simt_config_256():
     assert_close(got, ref, bound, gen.F32, "fp32_256")
 
 
+@pytest.mark.parametrize("M,N,K", [(1152, 1152, 1024), (1000, 1100, 1500), (300, 300, 3000),
+                                   (1408, 1408, 2048)])
+def test_simt_split_tail(M, N, K):
+    # fewer tiles than resident blocks: every tile is split along K into
+    # workspace partials that a second kernel reduces
+    A, B, C = _mats(gen.F32, gen.F32, gen.ROW_MAJOR, M, N, K, 21)
+    got = run_gpu(S, gen.F32, gen.F32, gen.ROW_MAJOR, A, B, C, 1.5, 0.5)
+    assert dga.dga_last_launch_count() == 2, "expected the split tail"
+    ref, bound = oracle_ref(gen.F32, gen.F32, gen.ROW_MAJOR, A, B, C, 1.5, 0.5)
+    assert_close(got, ref, bound, gen.F32, f"split tail {M}x{N}x{K}")
+    # without workspace the same call runs whole tiles, one launch
+    got2 = run_gpu(S, gen.F32, gen.F32, gen.ROW_MAJOR, A, B, C, 1.5, 0.5, workspace=False)
+    assert dga.dga_last_launch_count() == 1
+    assert_close(got2, ref, bound, gen.F32, f"whole tiles {M}x{N}x{K}")
+
+
 def test_simt_padded_ld():
     check(S, gen.F32, gen.F32, gen.ROW_MAJOR, 130, 70, 50, 1.0, 1.0, lda=52, ldb=76, ldc=73)
 
