@@ -386,6 +386,26 @@ class OracleSample:
 
 # ------------------------------------------------------------------- main --
 
+def max_over_ranks(local_ms, world, device=None):
+    """The slowest rank's timed-region length (ms): the job finishes when the
+    last replica does.  Works with any process-group backend (NCCL on the
+    GPUs, gloo in the CPU tests)."""
+    if world <= 1:
+        return float(local_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_ms)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step_per_rank, world, steps, max_ms, scale):
+    """Whole-job throughput: the units every rank processed (weak scaling:
+    each replica runs the full workload) over the slowest rank's time."""
+    return world * units_per_step_per_rank * steps / (max_ms * 1e-3) / scale
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
@@ -485,11 +505,7 @@ def main():
     t_end = time.time()
     time.sleep(0.2)
     clocks.stop()
-    total_ms = g0.elapsed_time(g1)
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(g0.elapsed_time(g1), world, device)
     ms_per_step = total_ms / args.steps
     # the dominant kernel's time per launch: the whole call's time per step
     # (the paths measured here launch one kernel per call; when a call
@@ -497,9 +513,9 @@ def main():
     kmean = g0.elapsed_time(g1) / args.steps
     fl, by = workload_accounting(w)
     if w.name.startswith("skinny"):
-        value, unit = world * by / (ms_per_step * 1e-3) / 1e9, "GB/s"
+        value, unit = job_throughput(by, world, args.steps, total_ms, 1e9), "GB/s"
     else:
-        value = world * fl / (ms_per_step * 1e-3) / 1e12
+        value = job_throughput(fl, world, args.steps, total_ms, 1e12)
         unit = "TOPS" if w.in_dtype == gen.I8 else "TFLOPS"
     roof = roofline_for(w, kmean, peaks)
     roof["traffic"] = traffic_record(source_of(w), w.name)

@@ -43,6 +43,7 @@ SIGNATURES = {
     "dga_last_cuda_error": (_CI, []),
     "dga_status_string": (ctypes.c_char_p, [_CI]),
     "dga_version": (_CI, []),
+    "dga_selftest_bounded_wait": (_CI, [_I64, _VP]),
     "dga_gemm_i8_noalloc": (_CI, [_CI, _I64, _I64, _I64, _VP, _VP, _I64, _VP, _I64, _VP, _VP,
                                   _I64, _VP]),
 }
@@ -123,6 +124,10 @@ def dga_status_string(status):
 
 def dga_version():
     return lib().dga_version()
+
+
+def dga_selftest_bounded_wait(limit_ns, stream):
+    return lib().dga_selftest_bounded_wait(limit_ns, stream)
 
 
 NOALLOC_SCRATCH_BYTES = 64 << 20

@@ -291,6 +291,13 @@ int dga_sync_status(dga_stream_t stream) {
 
 int dga_last_cuda_error(void) { return t_last_cuda_error; }
 
+int dga_selftest_bounded_wait(int64_t limit_ns, dga_stream_t stream) {
+    if (limit_ns <= 0 || limit_ns > 2000000000) return -1;
+    cudaError_t e = tc_selftest_wait(static_cast<uint64_t>(limit_ns),
+                                     reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DGA_OK : fail_cuda(e);
+}
+
 const char* dga_status_string(int status) {
     if (status < 0) return "invalid argument (the negated value is its 1-based position)";
     switch (status) {

@@ -67,6 +67,8 @@ cudaError_t skinny_launch(const GemmArgs& a, int* launches);
 bool tc_supports(const GemmArgs& a);
 size_t tc_workspace_size(const GemmArgs& a);
 cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);
+// Launches a kernel whose bounded wait runs out after limit_ns (self-test).
+cudaError_t tc_selftest_wait(uint64_t limit_ns, cudaStream_t stream);
 // Reads and clears this device's tcgen05 status word (non-zero: a wait expired).
 cudaError_t tc_status_take(int* status);
 

@@ -8,8 +8,8 @@
 // A100/H100; this one is built for Blackwell instead:
 //
 //   * One persistent CTA per SM walks output tiles of 128 x 256 in a grouped
-//     order (16 tile-rows at a time) so that concurrently running tiles share
-//     A and B panels in L2.
+//     order (a group of tile rows sized so its A panels stay in L2) so that
+//     concurrently running tiles share A and B panels in L2.
 //   * Warp 0 (one lane) is the TMA producer: 2-D tensor-map loads of a
 //     128 x 64 A box and a 256 x 64 B box (64 bf16 = one 128-byte swizzle
 //     row) into a 4-stage shared-memory ring, each stage guarded by a
@@ -68,13 +68,12 @@ constexpr int BM = 128;  // tile rows (UMMA M)
 constexpr int BK = 64;   // K per stage: 64 x 2 bytes = one 128-byte swizzle row
 constexpr int UK = 16;   // K per tcgen05.mma (kind::f16)
 constexpr int kStages = 4;
-constexpr int kGroupM = 16;  // tile-rows per raster group
 constexpr int kI8ChunkBlocks = 4;  // INT8: K blocks per exact fp32 chunk (4 x 64 = 256)
 constexpr float kI8Magic = 12582912.0f;      // 1.5 * 2^23
 constexpr uint32_t kI8MagicBits = 0x4B400000u;  // its bit pattern
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
 
-enum : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
+enum : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleSelfTest = 4 };
 
 struct TcParams {
     int64_t M, N, K;
@@ -84,6 +83,7 @@ struct TcParams {
     int32_t alpha_i, beta_i;
     int vec_c;  // C 16-byte aligned and ldc a multiple of 16 bytes
     uint32_t tiles_m, tiles_n, num_tiles, num_kb;
+    uint32_t group_m;  // tile rows per raster group
 };
 
 // Shared-memory plan (dynamic, 1024-byte aligned): the stage ring, the
@@ -109,10 +109,10 @@ struct Smem {
 
 __device__ __forceinline__ void tile_coords(uint32_t t, const TcParams& p, uint32_t& tm,
                                             uint32_t& tn) {
-    const uint32_t group_size = kGroupM * p.tiles_n;
+    const uint32_t group_size = p.group_m * p.tiles_n;
     const uint32_t group = t / group_size;
-    const uint32_t first_m = group * kGroupM;
-    const uint32_t gm = min(p.tiles_m - first_m, static_cast<uint32_t>(kGroupM));
+    const uint32_t first_m = group * p.group_m;
+    const uint32_t gm = min(p.tiles_m - first_m, p.group_m);
     const uint32_t r = t % group_size;
     tm = first_m + r % gm;
     tn = r / gm;
@@ -398,6 +398,27 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
     }
 }
 
+// ---- self-test of the bounded wait ----------------------------------------------
+//
+// Waits on an mbarrier that nothing ever arrives at, with the same bounded
+// wait the GEMM roles use, so that the give-up path (status word, abort
+// flag, orderly return) can be exercised on a GPU without hanging it.
+
+__global__ void bounded_wait_probe_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        volatile int* flag = &abort_flag;
+        if (!mbar_wait_bounded(&bar, 0, flag, limit_ns)) record_failure(kRoleSelfTest, flag);
+    }
+}
+
 // ---- operand repacking into the workspace ------------------------------------
 //
 // dst[r][k] = src(r, k) converted to 16-bit storage (bf16/fp16; int8 values
@@ -553,6 +574,19 @@ PackPlan plan_for_sizes(const GemmArgs& a) {
     return plan_for(b);
 }
 
+// Tile rows per raster group.  The resident CTAs work on consecutive tiles,
+// i.e. on `group_m` tile rows at a time while B's column panels stream past;
+// the A panels of one group should stay in L2 (half of it, leaving room for
+// the streamed B panels and C), and the larger the group the fewer times B
+// is read from DRAM.
+uint32_t raster_group_rows(int64_t K, uint32_t tiles_m) {
+    const double a_panel = static_cast<double>(BM) * K * 2;  // bytes of one A tile row
+    const double budget = 32.0 * 1024 * 1024;  // measured best: 16 tile rows at K = 8192
+    uint32_t g = static_cast<uint32_t>(budget / a_panel);
+    g = std::max<uint32_t>(8, std::min<uint32_t>(g, 64));
+    return std::min(g, tiles_m);
+}
+
 template <bool kBf16, bool kI8, int BN, typename TOut>
 cudaError_t launch_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
                           const DeviceInfo& dev, cudaStream_t s) {
@@ -658,6 +692,7 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     p.tiles_n = static_cast<uint32_t>((a.N + BN - 1) / BN);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.num_kb = static_cast<uint32_t>((a.K + BK - 1) / BK);
+    p.group_m = raster_group_rows(a.K, p.tiles_m);
 
     if (i8) e = launch_kernel<true, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream);
     else if (bf16 && a.out_dtype == DGA_F32) e = launch_kernel<true, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
@@ -666,6 +701,11 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     else e = launch_kernel<false, false, kBnFloat, __half>(ma, mb, p, dev, a.stream);
     if (e == cudaSuccess) ++*launches;
     return e;
+}
+
+cudaError_t tc_selftest_wait(uint64_t limit_ns, cudaStream_t stream) {
+    bounded_wait_probe_kernel<<<1, 32, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t tc_status_take(int* status) {

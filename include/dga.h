@@ -159,6 +159,15 @@ int dga_last_launch_count(void);
  * DGA_ERR_DEVICE_TIMEOUT, or DGA_ERR_CUDA when the synchronisation failed. */
 int dga_sync_status(dga_stream_t stream);
 
+/* Failure-detection self-test.  Enqueues one small kernel that waits on an
+ * mbarrier nothing arrives at, using the same bounded wait as the GEMM
+ * kernels, and gives up after limit_ns nanoseconds (0 < limit_ns <= 2e9,
+ * else -1).  The next dga_sync_status(stream) must then report
+ * DGA_ERR_DEVICE_TIMEOUT, and the GPU context stays usable.  Lets a caller
+ * check the timeout path on its own GPU without faulting or hanging it.
+ * The pages have no counterpart (their kernels have no waits). */
+int dga_selftest_bounded_wait(int64_t limit_ns, dga_stream_t stream);
+
 /* The cudaError_t value behind the last DGA_ERR_CUDA on this host thread. */
 int dga_last_cuda_error(void);
 

@@ -73,6 +73,11 @@ def test_col_major_ldb_rule(lib):
     assert _call(layout_b=gen.COL_MAJOR, K=8, lda=8, ldb=4) == -11
 
 
+def test_selftest_limit_validated(lib):
+    assert dga.dga_selftest_bounded_wait(0, None) == -1
+    assert dga.dga_selftest_bounded_wait(3_000_000_000, None) == -1
+
+
 def test_m_zero_is_a_no_op_without_device(lib):
     assert _call(M=0, A=None, C=None) == dga.OK
     assert _call(N=0, B=None, C=None) == dga.OK

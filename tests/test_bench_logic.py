@@ -1,0 +1,102 @@
+"""bench.py's host logic without a GPU: FLOP/byte accounting against the
+figures the pages print, and the multi-rank path (max over ranks, whole-job
+throughput, rank-0-only reference arm) with world_size-2 gloo process groups.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def _page_figures():
+    with open(os.path.join(HERE, "golden", "page_figures.json")) as f:
+        return json.load(f)["figures"]
+
+
+def test_accounting_matches_page_figures():
+    fig = {f["id"]: f for f in _page_figures()}
+    # 2*N^3 FLOPs of a 2048^3 GEMM
+    assert bench.gemm_flops(2048, 2048, 2048) == pytest.approx(fig["naive_2048_flops"]["value"], rel=1e-3)
+    # GEMV (M x N fp32 matrix times vector): 2MN / 4MN = 0.5 FLOP/B
+    M = N = 8192
+    gemv = bench.intensity(bench.gemm_flops(M, 1, N), bench.gemm_bytes(M, 1, N, 4, 4, False))
+    assert gemv == pytest.approx(fig["gemv_intensity"]["value"], rel=1e-3)
+    # square N = 1024: 2N^3 / 12N^2 ~ 170 FLOP/B
+    sq = bench.intensity(bench.gemm_flops(1024, 1024, 1024), bench.gemm_bytes(1024, 1024, 1024, 4, 4, False))
+    assert sq == pytest.approx(fig["square_1024_intensity"]["value"], rel=0.01)
+    # block tile T: T/4 FLOP/B -> 8 at T=32, 32 at T=128
+    assert bench.tile_intensity(32) == fig["tile_32_intensity"]["value"]
+    assert bench.tile_intensity(128) == fig["tile_128_intensity"]["value"]
+    # naive kernel: one FMA per 8 bytes read -> 0.25 FLOP/B
+    assert bench.intensity(2 * 2048, 8 * 2048) == fig["naive_intensity"]["value"]
+    # 8x8 register tile: 64 FMA per 16 shared-memory reads
+    assert 64 / (8 + 8) == fig["register_tile_fma_per_read"]["value"]
+    # RTX 5080 machine balance
+    assert 56.28e12 / 960e9 == pytest.approx(fig["rtx5080_balance"]["value"])
+    # global load requests of the naive kernel at 2048^3 with 16x16 blocks:
+    # 2 loads per k per thread, one request per warp instruction
+    assert 2048 ** 3 * 2 // 32 == fig["naive_load_requests"]["value"]
+
+
+def test_peaks_from_measured_file(tmp_path, monkeypatch):
+    pk = bench.load_peaks(152)
+    assert pk["fp32_ffma_tflops"] == pytest.approx(152 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12)
+    assert pk["source"] in ("measured", "fallback")
+
+
+def test_job_throughput_weak_scaling():
+    # two ranks, 10 steps of 1e12 FLOP each, slowest rank 2 s -> 10 TFLOP/s
+    assert bench.job_throughput(1e12, 2, 10, 2000.0, 1e12) == pytest.approx(10.0)
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def _rank_main(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    local = 100.0 + 50.0 * rank          # rank 1 is the slow one
+    m = bench.max_over_ranks(local, world)
+    v = bench.job_throughput(1e9, world, 4, m, 1e12)
+    out.put((rank, m, v))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, m, v in res:
+        assert m == 150.0                   # every rank sees the slowest rank's time
+        assert v == pytest.approx(2 * 1e9 * 4 / 0.150 / 1e12)
+
+
+def test_reference_arm_rank0_only_under_torchrun():
+    # two CPU ranks: rank 0 prints the reference line, rank 1 exits quietly
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(28500 + os.getpid() % 1000),
+           os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "fp32_256",
+           "--gpus", "2", "--steps", "1", "--warmup", "0"]
+    res = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT,
+                         env={**os.environ, "OMP_NUM_THREADS": "2"})
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0
