@@ -398,6 +398,203 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
     }
 }
 
+// ---- the CTA-pair kernel (floating point) ---------------------------------------
+//
+// A cluster of two CTAs computes one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): CTA r (r = 0, 1) loads
+// rows [128r, 128r + 128) of the tile's A panel and rows [128r, 128r + 128) of
+// its B panel (half of N) into its own shared memory, and its TMEM receives
+// rows [128r, 128r + 128) of the accumulator (all 256 columns).  Compared with
+// one CTA per 128 x 256 tile, each SM loads half as much B per MMA, so the
+// same 192 KB ring holds 6 stages instead of 4.
+//
+// Roles and barriers (the even CTA is the leader):
+//   * each CTA's TMA warp loads into its own ring; every copy counts its
+//     bytes on the LEADER's full[s] barrier (cta_group::2 bulk tensor copy),
+//     and the leader's producer announces the bytes of both CTAs;
+//   * the leader's MMA thread issues the pair MMAs and commits, multicast to
+//     both CTAs, to empty[s] (ring slot free) and acc_full[b] (accumulator
+//     ready);
+//   * each CTA's four epilogue warps drain their own TMEM and arrive (one lane
+//     per warp) on the leader's acc_empty[b], which counts all eight warps.
+
+constexpr int kPairStages = 6;
+constexpr int kPairBN = 256;
+
+struct PairSmem {
+    static constexpr uint32_t kABytes = 128 * BK * 2;
+    static constexpr uint32_t kBBytes = (kPairBN / 2) * BK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kRing = kPairStages * kStageBytes;
+    static constexpr uint32_t kBarOffset = kRing;
+    // full[S], empty[S], acc_full[2], acc_empty[2], drain, then tmem slot + abort flag
+    static constexpr uint32_t kBarBytes = (2 * kPairStages + 5) * 8 + 16;
+    static constexpr uint32_t kEpiOffset = (kBarOffset + kBarBytes + 127) / 128 * 128;
+    static constexpr uint32_t kEpiWarpBytes = 32 * 33 * 4;
+    static constexpr uint32_t kTotal = kEpiOffset + 4 * kEpiWarpBytes;
+    static constexpr uint32_t kLaunchBytes = kTotal + 1024;
+};
+
+template <bool kBf16, typename TOut>
+__global__ void __launch_bounds__(192, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, TcParams p) {
+    using S = PairSmem;
+    constexpr uint32_t kTmemCols = 2 * kPairBN;  // two accumulators
+    constexpr uint32_t kIdesc = idesc_f16(kBf16, 256, kPairBN);
+    constexpr uint16_t kBothCtas = 0x3;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + S::kBarOffset);
+    uint64_t* empty = full + kPairStages;
+    uint64_t* acc_full = empty + kPairStages;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < kPairStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 2 * 4);  // one lane of each epilogue warp of both CTAs
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    __syncwarp();
+    cluster_sync();  // barriers of both CTAs initialised before any remote arrive
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t cluster_id = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer (both CTAs)
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (uint32_t t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
+                uint32_t tm, tn;
+                tile_coords(t, p, tm, tn);
+                const int32_t a_row = static_cast<int32_t>(tm * 256 + rank * 128);
+                const int32_t b_row = static_cast<int32_t>(tn * kPairBN + rank * (kPairBN / 2));
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded<true>(&empty[stage], phase ^ 1, abort_flag,
+                                                 kWaitLimitNs)) {
+                        record_failure(kRoleProducer, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* a_dst = smem + stage * S::kStageBytes;
+                    uint8_t* b_dst = a_dst + S::kABytes;
+                    if (leader) mbar_arrive_expect_tx(&full[stage], 2 * S::kStageBytes);
+                    const uint32_t bar = map_to_cta(smem_u32(&full[stage]), 0);
+                    tma_load_2d_pair(a_dst, &tmA, bar, static_cast<int32_t>(kb * BK), a_row);
+                    tma_load_2d_pair(b_dst, &tmB, bar, static_cast<int32_t>(kb * BK), b_row);
+                    if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) __nanosleep(20000);  // let copies already issued land before teardown
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        if (leader && lane == 0) {
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (uint32_t t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
+                if (!mbar_wait_bounded<true>(&acc_empty[acc], acc_phase ^ 1, abort_flag,
+                                             kWaitLimitNs)) {
+                    record_failure(kRoleMma, abort_flag);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kPairBN;
+                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                    if (!mbar_wait_bounded<true>(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                        record_failure(kRoleMma, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * S::kStageBytes);
+                    const uint64_t a_desc = smem_desc_kmajor_sw128(a_addr);
+                    const uint64_t b_desc = smem_desc_kmajor_sw128(a_addr + S::kABytes);
+#pragma unroll
+                    for (int k = 0; k < BK / UK; ++k)
+                        tc_mma_f16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
+                    tc_commit_pair_multicast(&empty[stage], kBothCtas);
+                    if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                tc_commit_pair_multicast(&acc_full[acc], kBothCtas);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            }
+            // every pair MMA issued so far must finish before TMEM is freed
+            tc_commit_pair_multicast(drain, 0x1);
+            volatile int never = 0;
+            mbar_wait_bounded(drain, 0, &never, kWaitLimitNs);
+        }
+    } else {
+        // ------------------------------------------------ epilogue warps (both CTAs)
+        const int ew = warp - 2;
+        const int quarter = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        uint32_t* stage = reinterpret_cast<uint32_t*>(smem + S::kEpiOffset + ew * S::kEpiWarpBytes);
+        uint32_t acc = 0, acc_phase = 0;
+        for (uint32_t t = cluster_id; t < p.num_tiles; t += n_clusters) {
+            uint32_t tm, tn;
+            tile_coords(t, p, tm, tn);
+            const int64_t row_base = static_cast<int64_t>(tm) * 256 + rank * 128 + quarter * 32;
+            const int64_t col0 = static_cast<int64_t>(tn) * kPairBN;
+            if (!mbar_wait_bounded<true>(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
+                record_failure(kRoleEpilogue, abort_flag);
+                break;
+            }
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < kPairBN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + c * 32, r);
+                tmem_ld_wait();
+                store_block_staged<TOut>(p, stage, lane, row_base, col0 + c * 32, r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&acc_empty[acc]), 0));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    __syncwarp();
+    cluster_sync();  // no CTA frees TMEM or exits while its peer may still touch it
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
 // ---- self-test of the bounded wait ----------------------------------------------
 //
 // Waits on an mbarrier that nothing ever arrives at, with the same bounded
@@ -579,8 +776,8 @@ PackPlan plan_for_sizes(const GemmArgs& a) {
 // the A panels of one group should stay in L2 (half of it, leaving room for
 // the streamed B panels and C), and the larger the group the fewer times B
 // is read from DRAM.
-uint32_t raster_group_rows(int64_t K, uint32_t tiles_m) {
-    const double a_panel = static_cast<double>(BM) * K * 2;  // bytes of one A tile row
+uint32_t raster_group_rows(int64_t K, uint32_t tiles_m, int tile_rows) {
+    const double a_panel = static_cast<double>(tile_rows) * K * 2;  // bytes of one A tile row
     const double budget = 32.0 * 1024 * 1024;  // measured best: 16 tile rows at K = 8192
     uint32_t g = static_cast<uint32_t>(budget / a_panel);
     g = std::max<uint32_t>(8, std::min<uint32_t>(g, 64));
@@ -598,6 +795,57 @@ cudaError_t launch_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const Tc
     const unsigned grid = static_cast<unsigned>(std::min<uint32_t>(p.num_tiles, dev.sm_count));
     kern<<<grid, kI8 ? 576 : 192, smem, s>>>(ma, mb, p);
     return cudaGetLastError();
+}
+
+// Clusters of two that fit at once on this device (queried once per kernel).
+template <typename Kern>
+int max_pair_clusters(Kern kern, int smem, const DeviceInfo& dev) {
+    static int cached[64] = {};
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev.ordinal >= 0 && dev.ordinal < 64 && cached[dev.ordinal] > 0) return cached[dev.ordinal];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (dev.sm_count / 2));
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = dev.sm_count / 2;
+    }
+    if (dev.ordinal >= 0 && dev.ordinal < 64) cached[dev.ordinal] = n;
+    return n;
+}
+
+template <bool kBf16, typename TOut>
+cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
+                               const DeviceInfo& dev, cudaStream_t s) {
+    auto kern = tc_gemm_pair_kernel<kBf16, TOut>;
+    const int smem = static_cast<int>(PairSmem::kLaunchBytes);
+    if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int clusters = std::min<int64_t>(p.num_tiles, max_pair_clusters(kern, smem, dev));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * std::max(clusters, 1)));
+    cfg.blockDim = dim3(192);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
 }
 
 template <typename TSrc>
@@ -669,11 +917,14 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
         B = dst;
         ldb = pl.kp;
     }
-    const int BN = i8 ? kBnI8 : kBnFloat;
+    // Floating point with more than one 128-row tile: the CTA-pair kernel
+    // (256 x 256 tiles, each CTA loading half of B).
+    const bool pair = !i8 && a.M > BM;
+    const int BN = i8 ? kBnI8 : (pair ? kPairBN : kBnFloat);
     CUtensorMap ma, mb;
     e = make_kmajor_map(&ma, A, a.M, a.K, lda, BM, bf16);
     if (e != cudaSuccess) return e;
-    e = make_kmajor_map(&mb, B, a.N, a.K, ldb, BN, bf16);
+    e = make_kmajor_map(&mb, B, a.N, a.K, ldb, pair ? kPairBN / 2 : BN, bf16);
     if (e != cudaSuccess) return e;
 
     TcParams p{};
@@ -688,13 +939,18 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     p.beta_i = a.beta_i;
     const int out_size = (a.out_dtype == DGA_F32 || a.out_dtype == DGA_I32) ? 4 : 2;
     p.vec_c = ((a.ldc * out_size) % 16 == 0 && aligned(a.C, 16)) ? 1 : 0;
-    p.tiles_m = static_cast<uint32_t>((a.M + BM - 1) / BM);
+    const int tile_m = pair ? 2 * BM : BM;
+    p.tiles_m = static_cast<uint32_t>((a.M + tile_m - 1) / tile_m);
     p.tiles_n = static_cast<uint32_t>((a.N + BN - 1) / BN);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.num_kb = static_cast<uint32_t>((a.K + BK - 1) / BK);
-    p.group_m = raster_group_rows(a.K, p.tiles_m);
+    p.group_m = raster_group_rows(a.K, p.tiles_m, tile_m);
 
     if (i8) e = launch_kernel<true, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream);
+    else if (pair && bf16 && a.out_dtype == DGA_F32) e = launch_pair_kernel<true, float>(ma, mb, p, dev, a.stream);
+    else if (pair && bf16) e = launch_pair_kernel<true, __nv_bfloat16>(ma, mb, p, dev, a.stream);
+    else if (pair && a.out_dtype == DGA_F32) e = launch_pair_kernel<false, float>(ma, mb, p, dev, a.stream);
+    else if (pair) e = launch_pair_kernel<false, __half>(ma, mb, p, dev, a.stream);
     else if (bf16 && a.out_dtype == DGA_F32) e = launch_kernel<true, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
     else if (bf16) e = launch_kernel<true, false, kBnFloat, __nv_bfloat16>(ma, mb, p, dev, a.stream);
     else if (a.out_dtype == DGA_F32) e = launch_kernel<false, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
