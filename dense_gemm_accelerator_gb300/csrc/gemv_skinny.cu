@@ -9,28 +9,27 @@
 // by HBM bandwidth ("Matrix multiplication: arithmetic intensity, tiling and
 // Tensor Core", section 5.1, the matrix-vector row of its table, and section
 // 5.6).  The design therefore only has to (1) read every weight byte exactly
-// once, with enough loads in flight to saturate HBM, and (2) keep the
-// arithmetic off the critical path.
+// once, in the access pattern HBM serves best, with enough bytes in flight,
+// and (2) keep the arithmetic off the critical path.
 //
-//  * Each weight element is loaded once, 16 bytes per lane, with
-//    ld.global.nc.L1::no_allocate (streamed, never re-read) and an L2
-//    prefetch size of 256 bytes, so DRAM sees whole 256-byte requests for
-//    rows that a warp walks 64 bytes at a time.
-//  * The loads of several K steps are kept in flight per warp (a software
-//    pipeline over a register ring), since the whole kernel is a single
-//    pass over the weight.
-//  * The M <= 16 activation rows are the "B" operand of an mma.sync
-//    m16n8k16 (fp32 accumulate) and the weight rows its "A" operand, so a
-//    warp computes 16 weight rows x 8 activation rows per instruction; the
-//    FP32 FMA pipe alone could not keep up at M = 16 (2 M FLOP per weight
-//    element at ~7 TB/s is ~110 TFLOP/s).
-//  * No shuffles: a lane loads 8 consecutive k of one weight row and the same
-//    8 k of one activation row.  The dot product over k does not depend on
-//    the order of k, so these 8 values are fed to two MMAs as k-slots
-//    {2t, 2t+1, 2t+8, 2t+9} (t = lane % 4) -- the same permutation on both
-//    operands, hence the same sum.
-//  * A CTA owns RT*16 weight rows; its warps split K, and the partial tiles
-//    are summed in shared memory before the fused alpha/beta epilogue.
+//  * Streaming: each CTA owns 64 consecutive weight rows (one contiguous
+//    64 x K block) and walks K in stages of 256.  Every cp.async of a warp
+//    copies 512 contiguous bytes of one row (16 bytes per lane, 256-byte L2
+//    prefetch size) into a shared-memory ring of kStages stages; on GB300
+//    this pattern streams a single pass over 128 MB at ~96% of the measured
+//    copy bandwidth, where per-lane row-strided loads reach ~84%.  The M <= 16
+//    activation rows of the same K range ride along in the same stage.
+//  * Arithmetic: weight rows are the "A" operand and activation rows the "B"
+//    operand of mma.sync m16n8k16 (fp32 accumulate), so a warp computes 16
+//    weight rows x 8 activation rows per instruction, with fragments read by
+//    ldmatrix from rows padded by 16 bytes (no bank conflicts).  The FP32
+//    FMA pipe alone could not keep up at M = 16 (2 M FLOP per weight element
+//    at ~7 TB/s is ~110 TFLOP/s).
+//  * The 16 k-steps of a stage are spread over the 8 warps; at the end the
+//    warps' partial tiles are summed in shared memory and the fused
+//    alpha/beta epilogue writes Y.  Each CTA starts its walk over K at a
+//    different stage, so the CTAs do not all read the same activation lines
+//    at the same moment.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -39,6 +38,11 @@
 
 namespace dga {
 namespace {
+
+constexpr int kWarps = 8;
+constexpr int kKStage = 256;       // K per pipeline stage
+constexpr int kStageCount = 4;     // stages in the shared-memory ring
+constexpr int kRowBytes = kKStage * 2 + 16;  // padded shared-memory row (528 bytes)
 
 struct Params {
     int64_t M, N, K;
@@ -51,85 +55,116 @@ struct Params {
     float alpha, beta;
 };
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
+// 16-byte async copy with zero fill: src_bytes (0 or 16) bytes are read, the
+// rest of the 16 written as zeros.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, int src_bytes) {
+    asm volatile(
+        "cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;" ::"r"(
+            static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+        "l"(gmem), "r"(src_bytes)
+        : "memory");
 }
 
-__device__ __forceinline__ uint4 ld_cached(const void* p) {
-    uint4 v;
-    asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* smem) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))));
+}
+
+__device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], const void* smem) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))));
 }
 
 template <bool kBf16>
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
     if constexpr (kBf16) {
         asm volatile(
             "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
             "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     } else {
         asm volatile(
             "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
             "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
             : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     }
 }
 
-// One 32-element K step of a warp: RT weight tiles (two 16-byte loads per
-// lane each: rows g and g+8) and MT activation tiles (one load per lane).
-template <int RT, int MT>
-struct Step {
-    uint4 w[RT][2];
-    uint4 x[MT];
+// Shared memory: kStages x (kRows weight rows + 8*MT activation rows) padded
+// rows.  The cross-warp reduction reuses the ring once the pipeline drains,
+// keeping the footprint at two CTAs per SM.
+template <int MT, int kRows>
+struct SkinnySmem {
+    static constexpr int kStages = kStageCount;
+    static constexpr int kXRows = 8 * MT;
+    static constexpr int kStageBytes = (kRows + kXRows) * kRowBytes;
+    static constexpr int kRingBytes = kStages * kStageBytes;
+    static constexpr int kRedBytes = kWarps * kRows * (MT * 8 + 1) * 4;
+    static_assert(kRedBytes <= kRingBytes, "the reduction area lives in the ring");
+    static constexpr int kTotal = kRingBytes;
 };
 
 // MT = number of 8-row activation tiles (1 for M <= 8, 2 for M <= 16);
-// RT = 16-row weight tiles per CTA; WARPS split K; PF = K steps of loads
-// kept in flight per warp (software pipeline depth).
-template <bool kBf16, int MT, typename TOut, int RT, int WARPS, int PF>
-__global__ void __launch_bounds__(WARPS * 32) skinny_kernel(Params p) {
-    __shared__ float red[WARPS][RT * 16][MT * 8 + 1];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, t = lane & 3;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * (RT * 16);
-
-    // This warp's K range, in whole 32-element steps.
-    const int64_t steps = (p.K + 31) / 32;
-    const int64_t per_warp = (steps + WARPS - 1) / WARPS;
-    const int64_t s_begin = warp * per_warp;
-    const int64_t s_end = min(steps, s_begin + per_warp);
-
+// kRows = weight rows per CTA (a multiple of 16).
+template <bool kBf16, int MT, int kRows, typename TOut>
+__global__ void __launch_bounds__(kWarps * 32) skinny_kernel(Params p) {
+    using S = SkinnySmem<MT, kRows>;
+    constexpr int RT = kRows / 16;
+    constexpr int kStages = S::kStages;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kRows;
+    const int64_t n_stages = (p.K + kKStage - 1) / kKStage;
     const char* W = static_cast<const char*>(p.W);
     const char* X = static_cast<const char*>(p.X);
-    // Row pointers (clamped when the row does not exist; such loads are skipped).
-    const char* wrow[RT][2];
-    bool wok[RT][2];
+
+    // Stage s: weight rows n0 .. n0+31 and activation rows 0 .. 8*MT-1, k in
+    // [s*256, s*256 + 256).  Chunk c of 16 bytes: row c / 32, column c % 32;
+    // a warp's 32 lanes copy one row's 512 contiguous bytes.
+    // CTAs start their walk over K at different stages, so that at any moment
+    // they read different activation lines (all of them reading the same
+    // lines at once makes those L2 lines a hot spot).  The order is fixed per
+    // CTA, so results stay deterministic.
+    const int64_t k_start = static_cast<int64_t>(blockIdx.x) % n_stages;
+    auto load_stage = [&](int64_t s, int slot) {
+        uint8_t* base = smem + slot * S::kStageBytes;
+        int64_t ks = s + k_start;
+        if (ks >= n_stages) ks -= n_stages;
+        const int64_t k0 = ks * kKStage;
 #pragma unroll
-    for (int r = 0; r < RT; ++r)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t n = n0 + r * 16 + g + h * 8;
-            wok[r][h] = n < p.N;
-            wrow[r][h] = W + (wok[r][h] ? n : 0) * p.ldw * 2;
+        for (int i = 0; i < (kRows + S::kXRows) * 32 / (kWarps * 32); ++i) {
+            const int c = i * kWarps * 32 + tid;
+            const int row = c >> 5, col = c & 31;
+            const int64_t k = k0 + col * 8;
+            const bool kok = k < p.K;  // K % 8 == 0: a chunk is wholly in or out
+            const char* src;
+            bool ok;
+            if (row < kRows) {
+                const int64_t n = n0 + row;
+                ok = kok && n < p.N;
+                src = W + ((ok ? n : 0) * p.ldw + (ok ? k : 0)) * 2;
+            } else {
+                const int64_t m = row - kRows;
+                ok = kok && m < p.M;
+                src = X + ((ok ? m : 0) * p.ldx + (ok ? k : 0)) * 2;
+            }
+            cp_async16(base + row * kRowBytes + col * 16, src, ok ? 16 : 0);
         }
-    const char* xrow[MT];
-    bool xok[MT];
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        const int64_t row = m * 8 + g;
-        xok[m] = row < p.M;
-        xrow[m] = X + (xok[m] ? row : 0) * p.ldx * 2;
-    }
+    };
 
     float acc[RT][MT][4];
 #pragma unroll
@@ -139,48 +174,48 @@ __global__ void __launch_bounds__(WARPS * 32) skinny_kernel(Params p) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) acc[r][m][i] = 0.0f;
 
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    auto load = [&](Step<RT, MT>& st, int64_t s) {
-        const int64_t k = s * 32 + t * 8;  // this lane's 8 consecutive k (K % 8 == 0)
-        const bool kok = s < s_end && k < p.K;
+    // ldmatrix row addresses: A (16 x 16 tile) lane -> row lane%16, k half lane/16;
+    // B (8 activation rows x 16 k) lane -> row lane%8, k half (lane/8)%2.
+    const int a_row = lane & 15, a_kh = lane >> 4;
+    const int b_row = lane & 7, b_kh = (lane >> 3) & 1;
+
 #pragma unroll
-        for (int r = 0; r < RT; ++r)
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < n_stages) load_stage(s, s);
+        cp_async_commit();
+    }
+    for (int64_t s = 0; s < n_stages; ++s) {
+        cp_async_wait<kStages - 2>();  // stage s has landed (for this thread's copies)
+        __syncthreads();               // ... and for everyone's; slot (s-1) is free
+        const int64_t next = s + kStages - 1;
+        if (next < n_stages) load_stage(next, static_cast<int>(next % kStages));
+        cp_async_commit();
+
+        const uint8_t* base = smem + static_cast<int>(s % kStages) * S::kStageBytes;
+        const uint8_t* xbase = base + kRows * kRowBytes;
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-                st.w[r][h] = (kok && wok[r][h]) ? ld_stream(wrow[r][h] + k * 2) : zero;
+        for (int j = 0; j < kKStage / 16 / kWarps; ++j) {
+            const int kk = (warp * (kKStage / 16 / kWarps) + j) * 16;  // k offset in the stage
+            uint32_t a[RT][4];
 #pragma unroll
-        for (int m = 0; m < MT; ++m) st.x[m] = (kok && xok[m]) ? ld_cached(xrow[m] + k * 2) : zero;
-    };
-    auto compute = [&](const Step<RT, MT>& st) {
-#pragma unroll
-        for (int r = 0; r < RT; ++r)
+            for (int r = 0; r < RT; ++r)
+                ldmatrix_x4(a[r], base + (r * 16 + a_row) * kRowBytes + (kk + a_kh * 8) * 2);
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
-                // k-slots {2t,2t+1 | 2t+8,2t+9} <- this lane's k {0,1 | 2,3}, then {4,5 | 6,7}
-                mma16816<kBf16>(acc[r][m], st.w[r][0].x, st.w[r][1].x, st.w[r][0].y,
-                                st.w[r][1].y, st.x[m].x, st.x[m].y);
-                mma16816<kBf16>(acc[r][m], st.w[r][0].z, st.w[r][1].z, st.w[r][0].w,
-                                st.w[r][1].w, st.x[m].z, st.x[m].w);
-            }
-    };
-
-    // Software pipeline: PF steps of loads in flight; ring slots are indexed
-    // by compile-time constants so they stay in registers.
-    Step<RT, MT> ring[PF];
+                uint32_t b[2];
+                ldmatrix_x2(b, xbase + (m * 8 + b_row) * kRowBytes + (kk + b_kh * 8) * 2);
 #pragma unroll
-    for (int u = 0; u < PF; ++u) load(ring[u], s_begin + u);
-    for (int64_t s0 = s_begin; s0 < s_end; s0 += PF) {
-#pragma unroll
-        for (int u = 0; u < PF; ++u) {
-            if (s0 + u < s_end) {
-                compute(ring[u]);
-                load(ring[u], s0 + u + PF);
+                for (int r = 0; r < RT; ++r) mma16816<kBf16>(acc[r][m], a[r], b[0], b[1]);
             }
         }
     }
+    cp_async_wait<0>();
+    __syncthreads();  // every warp is done with the ring before it becomes `red`
 
     // D fragment: (row g, cols 2t, 2t+1) and (row g+8, same cols); rows are
     // weight rows (output columns n), columns are activation rows (m).
+    float (*red)[kRows][MT * 8 + 1] = reinterpret_cast<float (*)[kRows][MT * 8 + 1]>(smem);
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
@@ -193,30 +228,40 @@ __global__ void __launch_bounds__(WARPS * 32) skinny_kernel(Params p) {
     __syncthreads();
 
     TOut* Y = static_cast<TOut*>(p.Y);
-    for (int e = threadIdx.x; e < RT * 16 * MT * 8; e += WARPS * 32) {
-        const int nl = e % (RT * 16), m = e / (RT * 16);  // consecutive threads: consecutive n
+    for (int e = tid; e < kRows * MT * 8; e += kWarps * 32) {
+        const int nl = e % kRows, m = e / kRows;  // consecutive threads: consecutive n
         const int64_t n = n0 + nl;
         if (m >= p.M || n >= p.N) continue;
         float sum = 0.0f;
 #pragma unroll
-        for (int w = 0; w < WARPS; ++w) sum += red[w][nl][m];
+        for (int w = 0; w < kWarps; ++w) sum += red[w][nl][m];
         TOut* dst = Y + m * p.ldy + n;
         const float old = p.beta != 0.0f ? OutT<TOut>::load(dst) : 0.0f;
         OutT<TOut>::store(dst, axpby(p.alpha, sum, p.beta, old));
     }
 }
 
-// Chosen shape (measured on GB300 at N = K = 8192): 32 weight rows per CTA,
-// 8 warps splitting K, 4 K-steps of loads in flight for M <= 8 and 3 for
-// M <= 16 (where a deeper pipeline no longer fits the register budget).
-constexpr int kRT = 2, kWarps = 8, kPF1 = 4, kPF2 = 3;
+template <bool kBf16, int MT, int kRows, typename TOut>
+cudaError_t launch_mt(const Params& p, cudaStream_t s) {
+    auto kern = skinny_kernel<kBf16, MT, kRows, TOut>;
+    const int smem = SkinnySmem<MT, kRows>::kTotal;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(static_cast<unsigned>((p.N + kRows - 1) / kRows));
+    kern<<<grid, kWarps * 32, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+// Weight rows per CTA.  Each CTA also streams the activation rows of its K
+// range, so activation bytes are (M / rows) of the weight bytes; 64 rows
+// (one CTA per SM, 128 CTAs at N = 8192) measured fastest on GB300 for every
+// M <= 16, e.g. M = 16: 5.06 TB/s with 64 rows against 4.46 TB/s with 32.
+constexpr int kRowsPerCta = 64;
 
 template <bool kBf16, typename TOut>
 cudaError_t launch_typed(const Params& p, cudaStream_t s) {
-    dim3 grid(static_cast<unsigned>((p.N + kRT * 16 - 1) / (kRT * 16)));
-    if (p.M <= 8) skinny_kernel<kBf16, 1, TOut, kRT, kWarps, kPF1><<<grid, kWarps * 32, 0, s>>>(p);
-    else skinny_kernel<kBf16, 2, TOut, kRT, kWarps, kPF2><<<grid, kWarps * 32, 0, s>>>(p);
-    return cudaGetLastError();
+    return p.M <= 8 ? launch_mt<kBf16, 1, kRowsPerCta, TOut>(p, s)
+                    : launch_mt<kBf16, 2, kRowsPerCta, TOut>(p, s);
 }
 
 }  // namespace
@@ -226,7 +271,7 @@ bool skinny_supports(const GemmArgs& a) {
                        (a.in_dtype == DGA_F16 && (a.out_dtype == DGA_F32 || a.out_dtype == DGA_F16));
     return types && a.layout_b == DGA_COL_MAJOR && a.M >= 1 && a.M <= 16 && a.K % 8 == 0 &&
            a.lda % 8 == 0 && a.ldb % 8 == 0 && aligned(a.A, 16) && aligned(a.B, 16) &&
-           (a.N + kRT * 16 - 1) / (kRT * 16) <= 0x7fffffff;
+           (a.N + 15) / 16 <= 0x7fffffff;
 }
 
 cudaError_t skinny_launch(const GemmArgs& a, int* launches) {
