@@ -99,6 +99,11 @@ class Oracle:
         ci = ctypes.c_int
         lib.oracle_gemm_fp.argtypes = [ci, ci, ci, i64, i64, i64, f64, vp, i64, vp, i64, f64,
                                        vp, i64, vp, vp]
+        lib.oracle_gemm_fp_ex.argtypes = [ci, ci, ci, ci, i64, i64, i64, f64, vp, i64, vp, i64,
+                                          f64, vp, i64, vp, vp, vp]
+        lib.oracle_gemm_i8_ex.argtypes = [ci, ci, i64, i64, i64, i32, vp, i64, vp, i64, i32, vp,
+                                          i64, vp, vp]
+        lib.oracle_sum_rows.argtypes = [ci, i64, i64, vp, i64, vp, vp]
         lib.oracle_gemm_fp_sampled.argtypes = [ci, ci, ci, i64, f64, vp, i64, vp, i64, f64, vp,
                                                i64, i64, vp, vp, vp, vp]
         lib.oracle_gemm_i8.argtypes = [ci, i64, i64, i64, i32, vp, i64, vp, i64, i32, vp, i64, vp]
@@ -137,6 +142,46 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle_gemm_fp: unsupported dtype pair ({in_dtype}, {out_dtype})")
         return ref, bound
+
+    def gemm_fp_ex(self, in_dtype, out_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
+                   beta, C=None, ldc=None, bias=None):
+        """gemm_fp with A's layout (0 row-major M x K, 1 stored K x M) and an
+        optional bias row of N output-dtype elements added to every row."""
+        a = _buf(A, _FP_NP[in_dtype], "A")
+        b = _buf(B, _FP_NP[in_dtype], "B")
+        c = None if C is None else _buf(C, _FP_NP[out_dtype], "C")
+        bi = None if bias is None else _buf(bias, _FP_NP[out_dtype], "bias")
+        if c is None and beta != 0:
+            raise ValueError("beta != 0 needs C")
+        ref = np.empty((M, N), np.float64)
+        bound = np.empty((M, N), np.float64)
+        rc = self.lib.oracle_gemm_fp_ex(in_dtype, out_dtype, layout_a, layout_b, M, N, K,
+                                        float(alpha), _ptr(a), lda, _ptr(b), ldb, float(beta),
+                                        _ptr(c), ldc or N, _ptr(bi), _ptr(ref), _ptr(bound))
+        if rc != 0:
+            raise ValueError(f"oracle_gemm_fp_ex: unsupported dtype pair ({in_dtype}, {out_dtype})")
+        return ref, bound
+
+    def gemm_i8_ex(self, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb, beta=0, C=None,
+                   ldc=None, bias=None):
+        a = _buf(A, np.int8, "A")
+        b = _buf(B, np.int8, "B")
+        c = None if C is None else _buf(C, np.int32, "C")
+        bi = None if bias is None else _buf(bias, np.int32, "bias")
+        out = np.empty((M, N), np.int32)
+        self.lib.oracle_gemm_i8_ex(layout_a, layout_b, M, N, K, int(alpha), _ptr(a), lda, _ptr(b),
+                                   ldb, int(beta), _ptr(c), ldc or N, _ptr(bi), _ptr(out))
+        return out
+
+    def sum_rows(self, dtype, rows, cols, G, ldg=None):
+        """(sums, bound): column j summed over the rows of G, in fp64."""
+        g = _buf(G, _FP_NP[dtype], "G")
+        out = np.empty(cols, np.float64)
+        bound = np.empty(cols, np.float64)
+        if self.lib.oracle_sum_rows(dtype, rows, cols, _ptr(g), ldg or cols, _ptr(out),
+                                    _ptr(bound)) != 0:
+            raise ValueError("oracle_sum_rows: unsupported dtype")
+        return out, bound
 
     def gemm_fp_sampled(self, in_dtype, out_dtype, layout_b, K, alpha, A, lda, B, ldb, beta,
                         C, ldc, rows, cols):
@@ -237,6 +282,18 @@ def gemm_i8(*args, **kw):
 
 def gemm_i8_sampled(*args, **kw):
     return default().gemm_i8_sampled(*args, **kw)
+
+
+def gemm_fp_ex(*args, **kw):
+    return default().gemm_fp_ex(*args, **kw)
+
+
+def gemm_i8_ex(*args, **kw):
+    return default().gemm_i8_ex(*args, **kw)
+
+
+def sum_rows(*args, **kw):
+    return default().sum_rows(*args, **kw)
 
 
 def round_bf16(x):

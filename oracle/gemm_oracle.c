@@ -18,10 +18,17 @@
  * every stored operand is first decoded exactly to fp64.
  *
  * Layout (same page, section "Row-major order": offset = row*ld + col):
- *   A(i,k) = A[i*lda + k]                   (row-major)
+ *   A(i,k) = A[i*lda + k]   if layout_a==0  (row-major, M x K)
+ *          = A[k*lda + i]   if layout_a==1  (column-major, i.e. stored K x M)
  *   B(k,j) = B[k*ldb + j]   if layout_b==0  (row-major, K x N)
  *          = B[j*ldb + k]   if layout_b==1  (column-major, i.e. stored N x K)
  *   C(i,j) = C[i*ldc + j]                   (row-major)
+ *
+ * Optional bias row (the _ex entry points), the fully-connected layer of the
+ * same page, section "Fully-connected layer" (Y = X W^T + b, the bias added
+ * to every row):  ref(i,j) += bias[j], bias stored in the output type.  The
+ * same section's bias gradient, the sum over the batch of the output
+ * gradient, is oracle_sum_rows.
  *
  * BLAS conventions (readings where the pages are silent):
  *   beta == 0  -> C is not read (NaN/Inf in C do not reach the result);
@@ -92,16 +99,20 @@ static int64_t b_index(int layout_b, int64_t k, int64_t j, int64_t ldb) {
     return layout_b == OR_COL_MAJOR ? j * ldb + k : k * ldb + j;
 }
 
+static int64_t a_index(int layout_a, int64_t i, int64_t k, int64_t lda) {
+    return layout_a == OR_COL_MAJOR ? k * lda + i : i * lda + k;
+}
+
 /* ---- one output element, floating point --------------------------------- */
 
-static void fp_element(int in_dtype, int out_dtype, int layout_b, int64_t K,
+static void fp_element(int in_dtype, int out_dtype, int layout_a, int layout_b, int64_t K,
                        double alpha, const void* A, int64_t lda, const void* B,
                        int64_t ldb, double beta, const void* C, int64_t ldc,
-                       int64_t i, int64_t j, double* ref, double* bound) {
+                       const void* bias, int64_t i, int64_t j, double* ref, double* bound) {
     double sum = 0.0, abs_sum = 0.0;
     if (alpha != 0.0) {
         for (int64_t k = 0; k < K; ++k) {
-            double a = load_fp(in_dtype, A, i * lda + k);
+            double a = load_fp(in_dtype, A, a_index(layout_a, i, k, lda));
             double b = load_fp(in_dtype, B, b_index(layout_b, k, j, ldb));
             sum += a * b;            /* exact product for fp32/bf16/fp16 inputs */
             abs_sum += fabs(a * b);
@@ -110,27 +121,29 @@ static void fp_element(int in_dtype, int out_dtype, int layout_b, int64_t K,
     }
     double cterm = 0.0;
     if (beta != 0.0) cterm = beta * load_fp(out_dtype, C, i * ldc + j);
-    *ref = alpha * sum + cterm;
-    *bound = 1e-4 * fabs(alpha) * abs_sum + fabs(cterm) * ldexp(1.0, -22);
+    double bterm = bias ? load_fp(out_dtype, bias, j) : 0.0;
+    *ref = alpha * sum + cterm + bterm;
+    *bound = 1e-4 * fabs(alpha) * abs_sum + (fabs(cterm) + fabs(bterm)) * ldexp(1.0, -22);
 }
 
 /* ---- one output element, INT8 x INT8 -> INT32 ---------------------------- */
 
 /* (alpha*sum + beta*c) evaluated in int64, then reduced mod 2^32 to int32
  * two's complement.  Unsigned arithmetic keeps the wrap well defined. */
-static int32_t i8_element(int layout_b, int64_t K, int32_t alpha,
+static int32_t i8_element(int layout_a, int layout_b, int64_t K, int32_t alpha,
                           const int8_t* A, int64_t lda, const int8_t* B,
                           int64_t ldb, int32_t beta, const int32_t* C,
-                          int64_t ldc, int64_t i, int64_t j) {
+                          int64_t ldc, const int32_t* bias, int64_t i, int64_t j) {
     int64_t sum = 0;
     if (alpha != 0) {
         for (int64_t k = 0; k < K; ++k) {
-            sum += (int64_t)A[i * lda + k] * (int64_t)B[b_index(layout_b, k, j, ldb)];
+            sum += (int64_t)A[a_index(layout_a, i, k, lda)] * (int64_t)B[b_index(layout_b, k, j, ldb)];
             COUNT_MAC();
         }
     }
     uint64_t r = (uint64_t)((int64_t)alpha) * (uint64_t)sum;
     if (beta != 0) r += (uint64_t)((int64_t)beta) * (uint64_t)((int64_t)C[i * ldc + j]);
+    if (bias) r += (uint64_t)((int64_t)bias[j]);
     uint32_t low = (uint32_t)r;
     int32_t out;
     memcpy(&out, &low, sizeof out);
@@ -139,20 +152,30 @@ static int32_t i8_element(int layout_b, int64_t K, int32_t alpha,
 
 /* ---- public entry points ------------------------------------------------- */
 
-/* Full matrix, floating-point inputs.  ref and bound are M x N row-major fp64
- * arrays with leading dimension N.  Returns 0, or -1 on an unsupported dtype. */
-int oracle_gemm_fp(int in_dtype, int out_dtype, int layout_b, int64_t M,
-                   int64_t N, int64_t K, double alpha, const void* A,
-                   int64_t lda, const void* B, int64_t ldb, double beta,
-                   const void* C, int64_t ldc, double* ref, double* bound) {
+/* Full matrix, floating-point inputs, both operand layouts and an optional
+ * bias row (NULL: none).  ref and bound are M x N row-major fp64 arrays with
+ * leading dimension N.  Returns 0, or -1 on an unsupported dtype. */
+int oracle_gemm_fp_ex(int in_dtype, int out_dtype, int layout_a, int layout_b, int64_t M,
+                      int64_t N, int64_t K, double alpha, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, double beta, const void* C, int64_t ldc,
+                      const void* bias, double* ref, double* bound) {
     if (in_dtype != OR_F32 && in_dtype != OR_BF16 && in_dtype != OR_F16) return -1;
     if (out_dtype != OR_F32 && out_dtype != OR_BF16 && out_dtype != OR_F16) return -1;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j)
-            fp_element(in_dtype, out_dtype, layout_b, K, alpha, A, lda, B, ldb,
-                       beta, C, ldc, i, j, &ref[i * N + j], &bound[i * N + j]);
+            fp_element(in_dtype, out_dtype, layout_a, layout_b, K, alpha, A, lda, B, ldb,
+                       beta, C, ldc, bias, i, j, &ref[i * N + j], &bound[i * N + j]);
     return 0;
+}
+
+/* The same with A row-major and no bias. */
+int oracle_gemm_fp(int in_dtype, int out_dtype, int layout_b, int64_t M,
+                   int64_t N, int64_t K, double alpha, const void* A,
+                   int64_t lda, const void* B, int64_t ldb, double beta,
+                   const void* C, int64_t ldc, double* ref, double* bound) {
+    return oracle_gemm_fp_ex(in_dtype, out_dtype, OR_ROW_MAJOR, layout_b, M, N, K, alpha, A,
+                             lda, B, ldb, beta, C, ldc, NULL, ref, bound);
 }
 
 /* Selected elements only: for s < n_samples, element (rows[s], cols[s]). */
@@ -166,21 +189,30 @@ int oracle_gemm_fp_sampled(int in_dtype, int out_dtype, int layout_b, int64_t K,
     if (out_dtype != OR_F32 && out_dtype != OR_BF16 && out_dtype != OR_F16) return -1;
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t s = 0; s < n_samples; ++s)
-        fp_element(in_dtype, out_dtype, layout_b, K, alpha, A, lda, B, ldb,
-                   beta, C, ldc, rows[s], cols[s], &ref[s], &bound[s]);
+        fp_element(in_dtype, out_dtype, OR_ROW_MAJOR, layout_b, K, alpha, A, lda, B, ldb,
+                   beta, C, ldc, NULL, rows[s], cols[s], &ref[s], &bound[s]);
     return 0;
 }
 
-/* Full matrix, INT8 inputs, INT32 output (M x N, leading dimension N). */
-int oracle_gemm_i8(int layout_b, int64_t M, int64_t N, int64_t K, int32_t alpha,
-                   const int8_t* A, int64_t lda, const int8_t* B, int64_t ldb,
-                   int32_t beta, const int32_t* C, int64_t ldc, int32_t* out) {
+/* Full matrix, INT8 inputs, INT32 output (M x N, leading dimension N), both
+ * operand layouts and an optional int32 bias row. */
+int oracle_gemm_i8_ex(int layout_a, int layout_b, int64_t M, int64_t N, int64_t K,
+                      int32_t alpha, const int8_t* A, int64_t lda, const int8_t* B,
+                      int64_t ldb, int32_t beta, const int32_t* C, int64_t ldc,
+                      const int32_t* bias, int32_t* out) {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j)
-            out[i * N + j] = i8_element(layout_b, K, alpha, A, lda, B, ldb, beta,
-                                        C, ldc, i, j);
+            out[i * N + j] = i8_element(layout_a, layout_b, K, alpha, A, lda, B, ldb, beta,
+                                        C, ldc, bias, i, j);
     return 0;
+}
+
+int oracle_gemm_i8(int layout_b, int64_t M, int64_t N, int64_t K, int32_t alpha,
+                   const int8_t* A, int64_t lda, const int8_t* B, int64_t ldb,
+                   int32_t beta, const int32_t* C, int64_t ldc, int32_t* out) {
+    return oracle_gemm_i8_ex(OR_ROW_MAJOR, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                             ldc, NULL, out);
 }
 
 int oracle_gemm_i8_sampled(int layout_b, int64_t K, int32_t alpha,
@@ -190,8 +222,29 @@ int oracle_gemm_i8_sampled(int layout_b, int64_t K, int32_t alpha,
                            const int64_t* cols, int32_t* out) {
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t s = 0; s < n_samples; ++s)
-        out[s] = i8_element(layout_b, K, alpha, A, lda, B, ldb, beta, C, ldc,
-                            rows[s], cols[s]);
+        out[s] = i8_element(OR_ROW_MAJOR, layout_b, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                            NULL, rows[s], cols[s]);
+    return 0;
+}
+
+/* out[j] = sum over i < rows of G(i, j), G row-major with leading dimension
+ * ldg, in fp64 (ascending i), and bound[j] = 1e-4 * sum_i |G(i, j)|: the bias
+ * gradient of "AI Programming: Matrix Product", section "Fully-connected
+ * layer" (the output gradient summed over the batch). */
+int oracle_sum_rows(int dtype, int64_t rows, int64_t cols, const void* G, int64_t ldg,
+                    double* out, double* bound) {
+    if (dtype != OR_F32 && dtype != OR_BF16 && dtype != OR_F16) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < cols; ++j) {
+        double s = 0.0, a = 0.0;
+        for (int64_t i = 0; i < rows; ++i) {
+            double g = load_fp(dtype, G, i * ldg + j);
+            s += g;
+            a += fabs(g);
+        }
+        out[j] = s;
+        bound[j] = 1e-4 * a;
+    }
     return 0;
 }
 

@@ -335,5 +335,67 @@ def pin_ulp_bf16(o):
     assert np.array_equal(got, np.array(list(cases.values())))
 
 
+# ---------------------------------------------- A layout, bias, row sums --
+
+def pin_transposed_a(o):
+    """A stored K x M (column-major A) must give the same result as the same
+    matrix stored M x K; a permutation A detects a transposition."""
+    g = _rng(9)
+    M, K, N = 7, 11, 5
+    A = _f32((M, K), g)
+    B = _f32((K, N), g)
+    At = np.ascontiguousarray(A.T)
+    r_row, _ = o.gemm_fp_ex(F32, F32, ROW, ROW, M, N, K, 1.0, A, K, B, N, 0.0)
+    r_col, _ = o.gemm_fp_ex(F32, F32, COL, ROW, M, N, K, 1.0, At, M, B, N, 0.0)
+    assert np.array_equal(r_row, r_col), "column-major A"
+    rows = torch.randperm(K, generator=g).numpy()[:M]
+    P = np.zeros((M, K), np.float32)
+    P[np.arange(M), rows] = 1.0
+    ref, _ = o.gemm_fp_ex(F32, F32, COL, ROW, M, N, K, 1.0, np.ascontiguousarray(P.T), M, B, N, 0.0)
+    assert np.array_equal(ref, B[rows].astype(np.float64)), "P^T stored column-major"
+    # INT8 too, with padded leading dimension
+    Ai = torch.randint(-128, 128, (K, M + 3), generator=g, dtype=torch.int8)
+    Bi = torch.randint(-128, 128, (K, N), generator=g, dtype=torch.int8)
+    got = o.gemm_i8_ex(COL, ROW, M, N, K, 1, Ai.numpy(), M + 3, Bi.numpy(), N)
+    want = _py_gemm(Ai[:, :M].t().tolist(), Bi.tolist(), None, 1, 0, ROW)
+    assert np.array_equal(got, np.array(want, np.int64)), "int8 column-major A"
+
+
+def pin_bias(o):
+    """The bias row is added once to every row; with alpha = beta = 0 the
+    result is the bias itself (the Linear layer's Y = X W^T + b)."""
+    g = _rng(10)
+    M, K, N = 6, 9, 8
+    A = torch.randint(-4, 5, (M, K), generator=g).float().numpy()
+    W = torch.randint(-4, 5, (N, K), generator=g).float().numpy()    # [out, in]
+    bias = torch.randint(-50, 51, (N,), generator=g).float().numpy()
+    ref, _ = o.gemm_fp_ex(F32, F32, ROW, COL, M, N, K, 1.0, A, K, W, K, 0.0, bias=bias)
+    want = _py_gemm(A.astype(int).tolist(), W.astype(int).tolist(), None, 1, 0, COL)
+    want = np.array(want, np.float64) + bias[None, :]
+    assert np.array_equal(ref, want), "X W^T + b"
+    ref, _ = o.gemm_fp_ex(F32, F32, ROW, COL, M, N, K, 0.0, A, K, W, K, 0.0, bias=bias)
+    assert np.array_equal(ref, np.broadcast_to(bias, (M, N))), "bias alone"
+    Ai = torch.randint(-128, 128, (M, K), generator=g, dtype=torch.int8)
+    Bi = torch.randint(-128, 128, (K, N), generator=g, dtype=torch.int8)
+    bi = torch.randint(-1000, 1000, (N,), generator=g, dtype=torch.int32)
+    got = o.gemm_i8_ex(ROW, ROW, M, N, K, 1, Ai.numpy(), K, Bi.numpy(), N, bias=bi.numpy())
+    want = np.array(_py_gemm(Ai.tolist(), Bi.tolist(), None, 1, 0, ROW), np.int64) + bi.numpy()[None, :]
+    assert np.array_equal(got, want), "int8 bias"
+
+
+def pin_sum_rows(o):
+    """Column sums against Python integers (the bias gradient)."""
+    g = _rng(11)
+    R, Cc = 37, 13
+    G = torch.randint(-20, 21, (R, Cc + 2), generator=g).float()
+    got, bound = o.sum_rows(F32, R, Cc, G.numpy(), Cc + 2)
+    want = [sum(int(G[i, j]) for i in range(R)) for j in range(Cc)]
+    assert np.array_equal(got, np.array(want, np.float64))
+    assert np.allclose(bound, 1e-4 * G[:, :Cc].abs().sum(0).double().numpy())
+    got_b, _ = o.sum_rows(BF16, R, Cc, _bf16_bits(G), Cc + 2)
+    assert np.array_equal(got_b, got)
+
+
 ALL_PINS = [pin_identity, pin_permutation, pin_alpha_beta, pin_small_integers, pin_int8,
-            pin_tiny_rational, pin_bf16_decode, pin_f16_decode, pin_bf16_round, pin_ulp_bf16]
+            pin_tiny_rational, pin_bf16_decode, pin_f16_decode, pin_bf16_round, pin_ulp_bf16,
+            pin_transposed_a, pin_bias, pin_sum_rows]

@@ -17,7 +17,13 @@ from tests import oracle_pins
 MUTANTS = [
     ("b_layout_swapped", "j * ldb + k : k * ldb + j", "k * ldb + j : j * ldb + k", 0),
     ("beta_term_dropped", "cterm = beta * load_fp(out_dtype, C, i * ldc + j);", "cterm = 0.0 * beta;", 0),
-    ("alpha_scales_c", "*ref = alpha * sum + cterm;", "*ref = alpha * (sum + cterm);", 0),
+    ("alpha_scales_c", "*ref = alpha * sum + cterm + bterm;", "*ref = alpha * (sum + cterm) + bterm;", 0),
+    ("alpha_scales_bias", "*ref = alpha * sum + cterm + bterm;", "*ref = alpha * (sum + bterm) + cterm;", 0),
+    ("bias_dropped", "*ref = alpha * sum + cterm + bterm;", "*ref = alpha * sum + cterm;", 0),
+    ("bias_indexed_by_row", "load_fp(out_dtype, bias, j)", "load_fp(out_dtype, bias, i)", 0),
+    ("i8_bias_dropped", "if (bias) r +=", "if (0) r +=", 0),
+    ("a_layout_swapped", "? k * lda + i : i * lda + k", "? i * lda + k : k * lda + i", 0),
+    ("sum_rows_skips_last", "for (int64_t i = 0; i < rows; ++i) {", "for (int64_t i = 0; i + 1 < rows; ++i) {", 0),
     ("k_loop_short_fp", "for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 0; k + 1 < K; ++k) {", 0),
     ("k_loop_short_i8", "for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = 0; k + 1 < K; ++k) {", 1),
     ("product_sign", "sum += a * b;", "sum -= a * b;", 0),
@@ -29,8 +35,8 @@ MUTANTS = [
     ("f16_bias", "e - 25);", "e - 24);", 0),
     ("beta_zero_reads_c", "if (beta != 0.0) cterm", "if (1) cterm", 0),
     ("alpha_zero_reads_ab", "if (alpha != 0.0) {", "if (1) {", 0),
-    ("lda_ignored", "load_fp(in_dtype, A, i * lda + k)", "load_fp(in_dtype, A, i * K + k)", 0),
-    ("i8_lda_ignored", "A[i * lda + k]", "A[i * K + k]", 0),
+    ("lda_ignored", "a_index(layout_a, i, k, lda)", "a_index(layout_a, i, k, K)", 0),
+    ("i8_lda_ignored", "a_index(layout_a, i, k, lda)", "a_index(layout_a, i, k, K)", 1),
 ]
 
 
