@@ -44,6 +44,11 @@ SIGNATURES = {
     "dga_status_string": (ctypes.c_char_p, [_CI]),
     "dga_version": (_CI, []),
     "dga_selftest_bounded_wait": (_CI, [_I64, _VP]),
+    "dga_gemm_general": (_CI, [_CI, _CI, _CI, _CI, _I64, _I64, _I64, _VP, _VP, _I64, _VP, _I64,
+                               _VP, _VP, _I64, _VP, _VP, _SZ, _CI, _VP]),
+    "dga_gemm_general_workspace_size": (_SZ, [_CI, _CI, _CI, _CI, _I64, _I64, _I64, _I64, _I64,
+                                              _I64, _CI]),
+    "dga_sum_rows": (_CI, [_CI, _I64, _I64, _VP, _I64, _VP, _VP]),
     "dga_gemm_i8_noalloc": (_CI, [_CI, _I64, _I64, _I64, _VP, _VP, _I64, _VP, _I64, _VP, _VP,
                                   _I64, _VP]),
 }
@@ -91,6 +96,23 @@ def dga_gemm_ex(in_dtype, out_dtype, layout_b, M, N, K, alpha, A, lda, B, ldb, b
                 workspace, workspace_bytes, path, stream):
     return lib().dga_gemm_ex(in_dtype, out_dtype, layout_b, M, N, K, alpha, A, lda, B, ldb,
                              beta, C, ldc, workspace, workspace_bytes, path, stream)
+
+
+def dga_gemm_general(in_dtype, out_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B, ldb,
+                     beta, C, ldc, bias, workspace, workspace_bytes, path, stream):
+    return lib().dga_gemm_general(in_dtype, out_dtype, layout_a, layout_b, M, N, K, alpha, A, lda,
+                                  B, ldb, beta, C, ldc, bias, workspace, workspace_bytes, path,
+                                  stream)
+
+
+def dga_gemm_general_workspace_size(in_dtype, out_dtype, layout_a, layout_b, M, N, K, lda, ldb,
+                                    ldc, path):
+    return lib().dga_gemm_general_workspace_size(in_dtype, out_dtype, layout_a, layout_b, M, N, K,
+                                                 lda, ldb, ldc, path)
+
+
+def dga_sum_rows(dtype, rows, cols, G, ldg, out, stream):
+    return lib().dga_sum_rows(dtype, rows, cols, G, ldg, out, stream)
 
 
 def dga_gemm_workspace_size(in_dtype, out_dtype, layout_b, M, N, K, lda, ldb, ldc, path):
@@ -151,9 +173,19 @@ def scalar(value, in_dtype):
     return ctypes.c_int32(int(value)) if in_dtype == I8 else ctypes.c_float(float(value))
 
 
+def _layout_of(T, name):
+    """(layout, ld) of a 2-D tensor viewed as rows x cols: row-major when its
+    columns are contiguous, column-major when its rows are; else an error."""
+    if T.stride(1) == 1 or T.size(1) <= 1:
+        return ROW_MAJOR, max(T.stride(0), max(T.size(1), 1))
+    if T.stride(0) == 1:
+        return COL_MAJOR, max(T.stride(1), max(T.size(0), 1))
+    raise ValueError(f"{name} must be row-major or column-major")
+
+
 def operand_layout(A, B, C):
-    """(lda, layout_b, ldb, ldc) from tensor strides; raises on layouts the ABI
-    cannot express (no copies are made)."""
+    """(lda, layout_b, ldb, ldc) from tensor strides for a row-major A;
+    raises on layouts the ABI cannot express (no copies are made)."""
     if A.dim() != 2 or B.dim() != 2 or C.dim() != 2:
         raise ValueError("A, B and C must be 2-D")
     if A.stride(1) != 1 and A.size(1) > 1:
@@ -172,18 +204,21 @@ def operand_layout(A, B, C):
 
 
 def gemm(A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, path=PATH_AUTO, workspace=None,
-         stream=None):
-    """C <- alpha * A @ B + beta * C on the GPU; returns C.
+         stream=None, bias=None):
+    """C <- alpha * A @ B + beta * C (+ bias) on the GPU; returns C.
 
-    A: (M, K) row-major CUDA tensor.  B: (K, N), row- or column-major (a
-    transposed view of an (N, K) tensor is column-major).  C: (M, N) row-major,
-    allocated when None (then beta must be 0).  The workspace, when the chosen
+    A: (M, K) and B: (K, N) CUDA tensors, each row- or column-major (a
+    transposed view of a contiguous tensor is column-major).  C: (M, N)
+    row-major, allocated when None (then beta must be 0).  bias: optional (N,)
+    tensor of C's dtype added to every row.  The workspace, when the chosen
     path needs one, is allocated from PyTorch's caching allocator unless given.
     """
     import torch
     in_dtype = _dtype_code(A)
     if _dtype_code(B) != in_dtype:
         raise TypeError("A and B must have the same dtype")
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
     M, K = A.shape
     N = B.shape[1]
     if B.shape[0] != K:
@@ -197,22 +232,62 @@ def gemm(A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, path=PATH_AUTO, work
                                        F16: torch.float16, I32: torch.int32}[out_dtype],
                         device=A.device)
     out_dtype = _dtype_code(C)
-    if tuple(C.shape) != (M, N):
-        raise ValueError(f"C has shape {tuple(C.shape)}, expected {(M, N)}")
-    lda, layout_b, ldb, ldc = operand_layout(A, B, C)
+    if tuple(C.shape) != (M, N) or C.dim() != 2 or (C.stride(1) != 1 and N > 1):
+        raise ValueError(f"C must be a row-major ({M}, {N}) tensor")
+    layout_a, lda = _layout_of(A, "A")
+    layout_b, ldb = _layout_of(B, "B")
+    ldc = max(C.stride(0), max(N, 1))
+    if bias is not None:
+        if bias.dim() != 1 or bias.numel() != N or bias.stride(0) != 1 or _dtype_code(bias) != out_dtype:
+            raise ValueError("bias must be a contiguous (N,) tensor of C's dtype")
     if stream is None:
         stream = torch.cuda.current_stream(A.device).cuda_stream
-    ws_bytes = dga_gemm_workspace_size(in_dtype, out_dtype, layout_b, M, N, K, lda, ldb, ldc,
-                                       path)
+    ws_bytes = dga_gemm_general_workspace_size(in_dtype, out_dtype, layout_a, layout_b, M, N, K,
+                                               lda, ldb, ldc, path)
     if ws_bytes and workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=A.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_have = workspace.numel() * workspace.element_size() if workspace is not None else 0
     a = scalar(alpha, in_dtype)
     b = scalar(beta, in_dtype)
-    st = dga_gemm_ex(in_dtype, out_dtype, layout_b, M, N, K, ctypes.byref(a), A.data_ptr(), lda,
-                     B.data_ptr(), ldb, ctypes.byref(b), C.data_ptr(), ldc, ws_ptr, ws_have, path,
-                     stream)
+    st = dga_gemm_general(in_dtype, out_dtype, layout_a, layout_b, M, N, K, ctypes.byref(a),
+                          A.data_ptr(), lda, B.data_ptr(), ldb, ctypes.byref(b), C.data_ptr(), ldc,
+                          bias.data_ptr() if bias is not None else None, ws_ptr, ws_have, path,
+                          stream)
     if st != OK:
-        raise DgaError(st, "dga_gemm_ex")
+        raise DgaError(st, "dga_gemm_general")
     return C
+
+
+def sum_rows(G, out=None, stream=None):
+    """fp32 column sums of a row-major 2-D tensor G (the batch sum of an output
+    gradient); returns out."""
+    import torch
+    rows, cols = G.shape
+    if G.stride(1) != 1 and cols > 1:
+        raise ValueError("G must be row-major")
+    if out is None:
+        out = torch.empty(cols, dtype=torch.float32, device=G.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(G.device).cuda_stream
+    st = dga_sum_rows(_dtype_code(G), rows, cols, G.data_ptr(), max(G.stride(0), max(cols, 1)),
+                      out.data_ptr(), stream)
+    if st != OK:
+        raise DgaError(st, "dga_sum_rows")
+    return out
+
+
+def linear_forward(X, W, bias=None, Y=None):
+    """Y = X @ W^T + bias for X [batch, in], W [out, in] (PyTorch's Linear
+    layout), bias [out]: one dga_gemm_general call (W^T is column-major)."""
+    return gemm(X, W.t(), Y, bias=bias)
+
+
+def linear_backward(X, W, G, need_bias=True):
+    """Gradients of Y = X W^T + b for the output gradient G [batch, out]:
+    dX = G W, dW = G^T X, db = the batch sum of G (fp32).  Two
+    dga_gemm_general calls and one dga_sum_rows call."""
+    dX = gemm(G, W)
+    dW = gemm(G.t(), X)
+    db = sum_rows(G) if need_bias else None
+    return dX, dW, db

@@ -49,24 +49,35 @@ void span(const void* p, int64_t rows, int64_t cols, int64_t ld, size_t es, uint
 
 bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
+// 1-based positions of the checked arguments in one entry point's list, so
+// that argument errors come back as -(position) in that entry point's terms.
+struct ArgPos {
+    int M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, ws;
+};
+constexpr ArgPos kPosEx{4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15};
+constexpr ArgPos kPosGeneral{5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 17};
+
 // Validates everything but the pointers' alignment; fills *g.  Without
 // `with_pointers` (size queries), matrix pointers are neither required nor
 // checked for overlap.
-int check_args(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M, int64_t N,
-               int64_t K, const void* alpha, const void* A, int64_t lda, const void* B,
-               int64_t ldb, const void* beta, void* C, int64_t ldc, void* ws, size_t ws_bytes,
-               GemmArgs* g, bool with_pointers = true) {
+int check_args(const ArgPos& pos, dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_a,
+               dga_layout layout_b, int64_t M, int64_t N, int64_t K, const void* alpha,
+               const void* A, int64_t lda, const void* B, int64_t ldb, const void* beta, void* C,
+               int64_t ldc, const void* bias, void* ws, size_t ws_bytes, GemmArgs* g,
+               bool with_pointers = true) {
     if (in_dtype < DGA_F32 || in_dtype > DGA_I32 || out_dtype < DGA_F32 || out_dtype > DGA_I32)
         return DGA_ERR_UNSUPPORTED;
+    if (layout_a != DGA_ROW_MAJOR && layout_a != DGA_COL_MAJOR) return DGA_ERR_UNSUPPORTED;
     if (layout_b != DGA_ROW_MAJOR && layout_b != DGA_COL_MAJOR) return DGA_ERR_UNSUPPORTED;
     if (!pair_supported(in_dtype, out_dtype)) return DGA_ERR_UNSUPPORTED;
-    if (M < 0) return -4;
-    if (N < 0) return -5;
-    if (K < 0) return -6;
-    if (!alpha) return -7;
-    if (!beta) return -12;
+    if (M < 0) return -pos.M;
+    if (N < 0) return -pos.N;
+    if (K < 0) return -pos.K;
+    if (!alpha) return -pos.alpha;
+    if (!beta) return -pos.beta;
     g->in_dtype = in_dtype;
     g->out_dtype = out_dtype;
+    g->layout_a = layout_a;
     g->layout_b = layout_b;
     g->M = M;
     g->N = N;
@@ -83,28 +94,36 @@ int check_args(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int
         g->beta_i = 0;
     }
     const bool reads_ab = with_pointers && M > 0 && N > 0 && K > 0 && !alpha_is_zero(*g);
-    if (reads_ab && !A) return -8;
-    if (lda < (K > 1 ? K : 1)) return -9;
-    if (reads_ab && !B) return -10;
+    if (reads_ab && !A) return -pos.A;
+    const int64_t min_lda = layout_a == DGA_ROW_MAJOR ? (K > 1 ? K : 1) : (M > 1 ? M : 1);
+    if (lda < min_lda) return -pos.lda;
+    if (reads_ab && !B) return -pos.B;
     const int64_t min_ldb = layout_b == DGA_ROW_MAJOR ? (N > 1 ? N : 1) : (K > 1 ? K : 1);
-    if (ldb < min_ldb) return -11;
-    if (with_pointers && M > 0 && N > 0 && !C) return -13;
-    if (ldc < (N > 1 ? N : 1)) return -14;
-    if (ws_bytes > 0 && !ws) return -15;
+    if (ldb < min_ldb) return -pos.ldb;
+    if (with_pointers && M > 0 && N > 0 && !C) return -pos.C;
+    if (ldc < (N > 1 ? N : 1)) return -pos.ldc;
+    if (ws_bytes > 0 && !ws) return -pos.ws;
     g->A = A;
     g->lda = lda;
     g->B = B;
     g->ldb = ldb;
     g->C = C;
     g->ldc = ldc;
+    g->bias = bias;
     g->ws = ws;
     g->ws_bytes = ws_bytes;
     if (with_pointers && M > 0 && N > 0) {
         uintptr_t c0, c1;
         span(C, M, N, ldc, elem_size(out_dtype), &c0, &c1);
+        if (bias) {
+            uintptr_t v0, v1;
+            span(bias, 1, N, N, elem_size(out_dtype), &v0, &v1);
+            if (overlaps(c0, c1, v0, v1)) return DGA_ERR_OVERLAP;
+        }
         if (reads_ab) {
             uintptr_t a0, a1, b0, b1;
-            span(A, M, K, lda, elem_size(in_dtype), &a0, &a1);
+            if (layout_a == DGA_ROW_MAJOR) span(A, M, K, lda, elem_size(in_dtype), &a0, &a1);
+            else span(A, K, M, lda, elem_size(in_dtype), &a0, &a1);
             if (layout_b == DGA_ROW_MAJOR) span(B, K, N, ldb, elem_size(in_dtype), &b0, &b1);
             else span(B, N, K, ldb, elem_size(in_dtype), &b0, &b1);
             if (overlaps(c0, c1, a0, a1) || overlaps(c0, c1, b0, b1)) return DGA_ERR_OVERLAP;
@@ -193,16 +212,16 @@ cudaError_t current_device_info(DeviceInfo* out) {
 
 using namespace dga;
 
-extern "C" {
+namespace {
 
-int dga_gemm_ex(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M, int64_t N,
-                int64_t K, const void* alpha, const void* A, int64_t lda, const void* B,
-                int64_t ldb, const void* beta, void* C, int64_t ldc, void* workspace,
-                size_t workspace_bytes, dga_path path, dga_stream_t stream) {
-    if (path < DGA_PATH_AUTO || path > DGA_PATH_SKINNY) return -17;
+int gemm_impl(const ArgPos& pos, dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_a,
+              dga_layout layout_b, int64_t M, int64_t N, int64_t K, const void* alpha,
+              const void* A, int64_t lda, const void* B, int64_t ldb, const void* beta, void* C,
+              int64_t ldc, const void* bias, void* workspace, size_t workspace_bytes,
+              dga_path path, dga_stream_t stream) {
     GemmArgs g{};
-    int st = check_args(in_dtype, out_dtype, layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C,
-                        ldc, workspace, workspace_bytes, &g);
+    int st = check_args(pos, in_dtype, out_dtype, layout_a, layout_b, M, N, K, alpha, A, lda, B,
+                        ldb, beta, C, ldc, bias, workspace, workspace_bytes, &g);
     if (st != DGA_OK) return st;
     g.stream = reinterpret_cast<cudaStream_t>(stream);
     t_last_path = DGA_PATH_AUTO;
@@ -232,6 +251,29 @@ int dga_gemm_ex(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, in
     return DGA_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+int dga_gemm_general(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_a,
+                     dga_layout layout_b, int64_t M, int64_t N, int64_t K, const void* alpha,
+                     const void* A, int64_t lda, const void* B, int64_t ldb, const void* beta,
+                     void* C, int64_t ldc, const void* bias, void* workspace,
+                     size_t workspace_bytes, dga_path path, dga_stream_t stream) {
+    if (path < DGA_PATH_AUTO || path > DGA_PATH_SKINNY) return -19;
+    return gemm_impl(kPosGeneral, in_dtype, out_dtype, layout_a, layout_b, M, N, K, alpha, A, lda,
+                     B, ldb, beta, C, ldc, bias, workspace, workspace_bytes, path, stream);
+}
+
+int dga_gemm_ex(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M, int64_t N,
+                int64_t K, const void* alpha, const void* A, int64_t lda, const void* B,
+                int64_t ldb, const void* beta, void* C, int64_t ldc, void* workspace,
+                size_t workspace_bytes, dga_path path, dga_stream_t stream) {
+    if (path < DGA_PATH_AUTO || path > DGA_PATH_SKINNY) return -17;
+    return gemm_impl(kPosEx, in_dtype, out_dtype, DGA_ROW_MAJOR, layout_b, M, N, K, alpha, A, lda,
+                     B, ldb, beta, C, ldc, nullptr, workspace, workspace_bytes, path, stream);
+}
+
 int dga_gemm(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M, int64_t N,
              int64_t K, const void* alpha, const void* A, int64_t lda, const void* B, int64_t ldb,
              const void* beta, void* C, int64_t ldc, void* workspace, size_t workspace_bytes,
@@ -240,15 +282,31 @@ int dga_gemm(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64
                        workspace, workspace_bytes, DGA_PATH_AUTO, stream);
 }
 
-size_t dga_gemm_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
-                               int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                               int64_t ldc, dga_path path) {
+int dga_sum_rows(dga_dtype dtype, int64_t rows, int64_t cols, const void* G, int64_t ldg,
+                 float* out, dga_stream_t stream) {
+    if (dtype != DGA_F32 && dtype != DGA_BF16 && dtype != DGA_F16) return DGA_ERR_UNSUPPORTED;
+    if (rows < 0) return -2;
+    if (cols < 0) return -3;
+    if (cols == 0) return DGA_OK;
+    if (rows > 0 && !G) return -4;
+    if (ldg < (cols > 1 ? cols : 1)) return -5;
+    if (!out) return -6;
+    cudaError_t e = sum_rows_launch(dtype, rows, cols, G, ldg, out,
+                                    reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DGA_OK : fail_cuda(e);
+}
+
+size_t dga_gemm_general_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype,
+                                       dga_layout layout_a, dga_layout layout_b, int64_t M,
+                                       int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                       int64_t ldc, dga_path path) {
     GemmArgs g{};
     const float one = 1.0f;
     const int32_t one_i = 1;
     const void* alpha = in_dtype == DGA_I8 ? static_cast<const void*>(&one_i) : &one;
-    if (check_args(in_dtype, out_dtype, layout_b, M, N, K, alpha, nullptr, lda, nullptr, ldb,
-                   alpha, nullptr, ldc, nullptr, 0, &g, /*with_pointers=*/false) != DGA_OK)
+    if (check_args(kPosGeneral, in_dtype, out_dtype, layout_a, layout_b, M, N, K, alpha, nullptr,
+                   lda, nullptr, ldb, alpha, nullptr, ldc, nullptr, nullptr, 0, &g,
+                   /*with_pointers=*/false) != DGA_OK)
         return 0;
     if (M == 0 || N == 0 || K == 0) return 0;
     // Pointer-free query: operands are assumed 16-byte aligned.
@@ -263,6 +321,13 @@ size_t dga_gemm_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype, dga_layo
     return workspace_wanted(chosen, g);
 }
 
+size_t dga_gemm_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
+                               int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                               int64_t ldc, dga_path path) {
+    return dga_gemm_general_workspace_size(in_dtype, out_dtype, DGA_ROW_MAJOR, layout_b, M, N, K,
+                                           lda, ldb, ldc, path);
+}
+
 int dga_select_path(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b, int64_t M,
                     int64_t N, int64_t K, const void* A, int64_t lda, const void* B, int64_t ldb,
                     const void* C, int64_t ldc) {
@@ -270,8 +335,8 @@ int dga_select_path(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b
     const float one = 1.0f;
     const int32_t one_i = 1;
     const void* alpha = in_dtype == DGA_I8 ? static_cast<const void*>(&one_i) : &one;
-    int st = check_args(in_dtype, out_dtype, layout_b, M, N, K, alpha, A, lda, B, ldb, alpha,
-                        const_cast<void*>(C), ldc, nullptr, 0, &g);
+    int st = check_args(kPosEx, in_dtype, out_dtype, DGA_ROW_MAJOR, layout_b, M, N, K, alpha, A,
+                        lda, B, ldb, alpha, const_cast<void*>(C), ldc, nullptr, nullptr, 0, &g);
     if (st != DGA_OK) return st < 0 ? st : -st;
     return choose_path(g);
 }

@@ -14,7 +14,7 @@ namespace dga {
 // One validated GEMM call.  alpha/beta are kept both as float (floating-point
 // inputs) and as int32 (INT8 inputs); only the one matching in_dtype is used.
 struct GemmArgs {
-    int in_dtype, out_dtype, layout_b;
+    int in_dtype, out_dtype, layout_a, layout_b;
     int64_t M, N, K;
     float alpha_f, beta_f;
     int32_t alpha_i, beta_i;
@@ -24,6 +24,7 @@ struct GemmArgs {
     int64_t ldb;
     void* C;
     int64_t ldc;
+    const void* bias;  // N elements of the output type (int32 for INT8), or null
     void* ws;
     size_t ws_bytes;
     cudaStream_t stream;
@@ -52,6 +53,10 @@ inline bool alpha_is_zero(const GemmArgs& a) {
 
 // ---- kernel families: supports() says whether the family can run the
 // arguments; launch() enqueues its kernels and adds their count to *launches.
+
+// Column sums of a rows x cols matrix into fp32 (the bias gradient).
+cudaError_t sum_rows_launch(int dtype, int64_t rows, int64_t cols, const void* G, int64_t ldg,
+                            float* out, cudaStream_t stream);
 
 bool generic_supports(const GemmArgs& a);
 cudaError_t generic_launch(const GemmArgs& a, int* launches);

@@ -9,9 +9,10 @@
 // A and B staged through shared memory one K-slice at a time, out-of-range
 // elements loaded as zero, stores masked -- widened here with a 2 x 2
 // register tile per thread (32 x 32 outputs per 16 x 16 block), a
-// layout-aware B load, and the dtype-generic epilogue.  K == 0 or alpha == 0
-// skips the loads entirely (C <- beta*C; beta == 0 writes zeros without
-// reading C).
+// layout-aware A and B loads, and the dtype-generic epilogue (with the
+// optional bias row of the fully-connected layer, same page, section
+// "Fully-connected layer").  K == 0 or alpha == 0 skips the loads entirely
+// (C <- beta*C + bias; beta == 0 writes without reading C).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -53,7 +54,8 @@ struct Params {
     int64_t ldb;
     void* C;
     int64_t ldc;
-    int layout_b;
+    const void* bias;  // N output-type elements added to every row, or null
+    int layout_a, layout_b;
     float alpha_f, beta_f;
     int32_t alpha_i, beta_i;
     int skip_product;  // alpha == 0 or K == 0
@@ -67,14 +69,19 @@ __device__ __forceinline__ void finish<int32_t, int32_t>(const Params& p, int32_
                                                          int64_t r, int64_t c) {
     int32_t* C = static_cast<int32_t*>(p.C) + r * p.ldc + c;
     int32_t old = p.beta_i != 0 ? *C : 0;
-    *C = axpby_i32(p.alpha_i, acc, p.beta_i, old);
+    int32_t v = axpby_i32(p.alpha_i, acc, p.beta_i, old);
+    if (p.bias) v = static_cast<int32_t>(static_cast<uint32_t>(v) +
+                                         static_cast<uint32_t>(static_cast<const int32_t*>(p.bias)[c]));
+    *C = v;
 }
 
 template <typename TAcc, typename TOut>
 __device__ __forceinline__ void finish(const Params& p, TAcc acc, int64_t r, int64_t c) {
     TOut* C = static_cast<TOut*>(p.C) + r * p.ldc + c;
     float old = p.beta_f != 0.0f ? OutT<TOut>::load(C) : 0.0f;
-    OutT<TOut>::store(C, axpby(p.alpha_f, static_cast<float>(acc), p.beta_f, old));
+    float v = axpby(p.alpha_f, static_cast<float>(acc), p.beta_f, old);
+    if (p.bias) v += OutT<TOut>::load(static_cast<const TOut*>(p.bias) + c);
+    OutT<TOut>::store(C, v);
 }
 
 template <typename TIn, typename TOut>
@@ -94,9 +101,12 @@ __global__ void __launch_bounds__(kThreads* kThreads) gemm_generic_kernel(Params
         for (int64_t k0 = 0; k0 < p.K; k0 += kTK) {
             // 32 x 16 elements of A and 16 x 32 of B; 256 threads, 2 each.
             for (int e = tid; e < kT * kTK; e += kThreads * kThreads) {
-                int m = e / kTK, k = e % kTK;  // consecutive threads walk K of one A row
+                int m, k;  // consecutive threads walk the contiguous direction of A
+                if (p.layout_a == DGA_ROW_MAJOR) { m = e / kTK; k = e % kTK; }
+                else { k = e / kT; m = e % kT; }
                 int64_t gr = row0 + m, gk = k0 + k;
-                As[k][m] = (gr < p.M && gk < p.K) ? InT<TIn>::get(A + gr * p.lda + gk) : Acc(0);
+                const TIn* src = p.layout_a == DGA_ROW_MAJOR ? A + gr * p.lda + gk : A + gk * p.lda + gr;
+                As[k][m] = (gr < p.M && gk < p.K) ? InT<TIn>::get(src) : Acc(0);
             }
             for (int e = tid; e < kT * kTK; e += kThreads * kThreads) {
                 int k, n;
@@ -137,7 +147,46 @@ cudaError_t launch_typed(const Params& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Column sums out[j] = sum_i G(i, j) in fp32: the bias gradient of the
+// fully-connected layer ("AI Programming: Matrix Product", section
+// "Fully-connected layer": the output gradient summed over the batch).  A
+// block covers 32 columns; its 8 warps take every 8th row, and the 8 partial
+// sums are added in a fixed order, so the result does not depend on timing.
+template <typename TIn>
+__global__ void __launch_bounds__(256) sum_rows_kernel(const TIn* __restrict__ G, int64_t rows,
+                                                       int64_t cols, int64_t ldg,
+                                                       float* __restrict__ out) {
+    __shared__ float part[8][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int64_t j = static_cast<int64_t>(blockIdx.x) * 32 + tx;
+    float s = 0.0f;
+    if (j < cols)
+        for (int64_t i = ty; i < rows; i += 8) s += static_cast<float>(InT<TIn>::get(G + i * ldg + j));
+    part[ty][tx] = s;
+    __syncthreads();
+    if (ty == 0 && j < cols) {
+        float t = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t += part[q][tx];
+        out[j] = t;
+    }
+}
+
 }  // namespace
+
+cudaError_t sum_rows_launch(int dtype, int64_t rows, int64_t cols, const void* G, int64_t ldg,
+                            float* out, cudaStream_t stream) {
+    const int64_t blocks = (cols + 31) / 32;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    const dim3 grid(static_cast<unsigned>(blocks));
+    if (dtype == DGA_F32)
+        sum_rows_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(G), rows, cols, ldg, out);
+    else if (dtype == DGA_BF16)
+        sum_rows_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(G), rows, cols, ldg, out);
+    else
+        sum_rows_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<const __half*>(G), rows, cols, ldg, out);
+    return cudaGetLastError();
+}
 
 bool generic_supports(const GemmArgs& a) {
     // grid.y limit: 65535 tiles of 32 rows
@@ -145,7 +194,7 @@ bool generic_supports(const GemmArgs& a) {
 }
 
 cudaError_t generic_launch(const GemmArgs& a, int* launches) {
-    Params p{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, a.C, a.ldc, a.layout_b,
+    Params p{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, a.C, a.ldc, a.bias, a.layout_a, a.layout_b,
              a.alpha_f, a.beta_f, a.alpha_i, a.beta_i, (a.K == 0 || alpha_is_zero(a)) ? 1 : 0};
     cudaError_t e = cudaErrorInvalidValue;
     if (a.in_dtype == DGA_F32 && a.out_dtype == DGA_F32) e = launch_typed<float, float>(p, a.stream);

@@ -29,9 +29,9 @@
 //     returning (read with dga_sync_status()).
 //
 // Operands reach the kernel K-major (A row-major, B column-major).  Other
-// layouts -- row-major B, a leading dimension TMA cannot express, or INT8
-// inputs (encoded exactly as bf16, see below) -- are first repacked into the
-// caller's workspace by pack_rows_kernel / pack_transposed_kernel.
+// layouts -- column-major A, row-major B, a leading dimension TMA cannot
+// express, or INT8 inputs (encoded exactly as bf16, see below) -- are first
+// repacked into the caller's workspace by pack_rows_kernel / pack_transposed_kernel.
 //
 // INT8 x INT8 -> INT32 (tcgen05 has no integer MMA on sm_103a: ptxas rejects
 // kind::i8 for this target).  Every int8 value is an exact bf16, every
@@ -77,7 +77,7 @@ struct TcParams {
     int64_t ldc;
     float alpha, beta;
     int32_t alpha_i, beta_i;
-    int vec_c;  // C 16-byte aligned and ldc a multiple of 16 bytes
+    const void* bias;  // N output-type (int32 for INT8) values added to every row, or null
     uint32_t tiles_m, tiles_n, num_tiles, num_kb;
     uint32_t group_m;  // tile rows per raster group
 };
@@ -137,13 +137,14 @@ __device__ __forceinline__ void store_block_staged(const TcParams& p, uint32_t* 
     __syncwarp();
     const int64_t col = col_base + lane;
     const bool col_ok = col < p.N;
+    const float bv = (p.bias != nullptr && col_ok) ? OutT<TOut>::load(static_cast<const TOut*>(p.bias) + col) : 0.0f;
 #pragma unroll 4
     for (int i = 0; i < 32; ++i) {
         const int64_t row = row_base + i;
         if (col_ok && row < p.M) {
             TOut* dst = static_cast<TOut*>(p.C) + row * p.ldc + col;
             const float old = p.beta != 0.0f ? OutT<TOut>::load(dst) : 0.0f;
-            OutT<TOut>::store(dst, axpby(p.alpha, __uint_as_float(stage[i * 33 + lane]), p.beta, old));
+            OutT<TOut>::store(dst, axpby(p.alpha, __uint_as_float(stage[i * 33 + lane]), p.beta, old) + bv);
         }
     }
     __syncwarp();  // the next block reuses the square
@@ -157,13 +158,15 @@ __device__ __forceinline__ void store_block_staged_i32(const TcParams& p, uint32
     __syncwarp();
     const int64_t col = col_base + lane;
     const bool col_ok = col < p.N;
+    const uint32_t bv = (p.bias != nullptr && col_ok) ? static_cast<uint32_t>(static_cast<const int32_t*>(p.bias)[col]) : 0u;
 #pragma unroll 4
     for (int i = 0; i < 32; ++i) {
         const int64_t row = row_base + i;
         if (col_ok && row < p.M) {
             int32_t* dst = static_cast<int32_t*>(p.C) + row * p.ldc + col;
             const int32_t old = p.beta_i != 0 ? *dst : 0;
-            *dst = axpby_i32(p.alpha_i, static_cast<int32_t>(stage[i * 33 + lane]), p.beta_i, old);
+            const int32_t v = axpby_i32(p.alpha_i, static_cast<int32_t>(stage[i * 33 + lane]), p.beta_i, old);
+            *dst = static_cast<int32_t>(static_cast<uint32_t>(v) + bv);
         }
     }
     __syncwarp();
@@ -747,7 +750,7 @@ PackPlan plan_for(const GemmArgs& a) {
     PackPlan pl{};
     pl.kp = round_up(a.K, 8);
     const bool i8 = a.in_dtype == DGA_I8;
-    pl.pack_a = i8 || a.lda % 8 != 0 || !aligned(a.A, 16);
+    pl.pack_a = i8 || a.layout_a != DGA_ROW_MAJOR || a.lda % 8 != 0 || !aligned(a.A, 16);
     pl.pack_b = i8 || a.layout_b != DGA_COL_MAJOR || a.ldb % 8 != 0 || !aligned(a.B, 16);
     pl.a_bytes = pl.pack_a ? round_up(a.M * pl.kp * 2, kWsAlign) : 0;
     pl.b_bytes = pl.pack_b ? round_up(a.N * pl.kp * 2, kWsAlign) : 0;
@@ -890,9 +893,10 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     if (pl.pack_a) {
         void* dst = ws;
-        if (i8) e = launch_pack<int8_t>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
-        else if (bf16) e = launch_pack<__nv_bfloat16>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
-        else e = launch_pack<__half>(a.A, a.lda, false, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        const bool tr = a.layout_a == DGA_COL_MAJOR;  // A(i, k) = A[k*lda + i]: transpose to M x K
+        if (i8) e = launch_pack<int8_t>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        else if (bf16) e = launch_pack<__nv_bfloat16>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        else e = launch_pack<__half>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
         if (e != cudaSuccess) return e;
         ++*launches;
         A = dst;
@@ -929,8 +933,7 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     p.beta = a.beta_f;
     p.alpha_i = a.alpha_i;
     p.beta_i = a.beta_i;
-    const int out_size = (a.out_dtype == DGA_F32 || a.out_dtype == DGA_I32) ? 4 : 2;
-    p.vec_c = ((a.ldc * out_size) % 16 == 0 && aligned(a.C, 16)) ? 1 : 0;
+    p.bias = a.bias;
     const int tile_m = pair ? 2 * BM : BM;
     p.tiles_m = static_cast<uint32_t>((a.M + tile_m - 1) / tile_m);
     p.tiles_n = static_cast<uint32_t>((a.N + BN - 1) / BN);

@@ -53,6 +53,7 @@ struct Params {
     void* Y;
     int64_t ldy;
     float alpha, beta;
+    const void* bias;  // N output-type values added to every row, or null
 };
 
 // 16-byte async copy with zero fill: src_bytes (0 or 16) bytes are read, the
@@ -237,7 +238,9 @@ __global__ void __launch_bounds__(kWarps * 32) skinny_kernel(Params p) {
         for (int w = 0; w < kWarps; ++w) sum += red[w][nl][m];
         TOut* dst = Y + m * p.ldy + n;
         const float old = p.beta != 0.0f ? OutT<TOut>::load(dst) : 0.0f;
-        OutT<TOut>::store(dst, axpby(p.alpha, sum, p.beta, old));
+        float v = axpby(p.alpha, sum, p.beta, old);
+        if (p.bias) v += OutT<TOut>::load(static_cast<const TOut*>(p.bias) + n);
+        OutT<TOut>::store(dst, v);
     }
 }
 
@@ -269,13 +272,14 @@ cudaError_t launch_typed(const Params& p, cudaStream_t s) {
 bool skinny_supports(const GemmArgs& a) {
     const bool types = (a.in_dtype == DGA_BF16 && (a.out_dtype == DGA_F32 || a.out_dtype == DGA_BF16)) ||
                        (a.in_dtype == DGA_F16 && (a.out_dtype == DGA_F32 || a.out_dtype == DGA_F16));
-    return types && a.layout_b == DGA_COL_MAJOR && a.M >= 1 && a.M <= 16 && a.K % 8 == 0 &&
+    return types && a.layout_a == DGA_ROW_MAJOR && a.layout_b == DGA_COL_MAJOR && a.M >= 1 &&
+           a.M <= 16 && a.K % 8 == 0 &&
            a.lda % 8 == 0 && a.ldb % 8 == 0 && aligned(a.A, 16) && aligned(a.B, 16) &&
            (a.N + 15) / 16 <= 0x7fffffff;
 }
 
 cudaError_t skinny_launch(const GemmArgs& a, int* launches) {
-    Params p{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, a.C, a.ldc, a.alpha_f, a.beta_f};
+    Params p{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, a.C, a.ldc, a.alpha_f, a.beta_f, a.bias};
     cudaError_t e = cudaErrorInvalidValue;
     const bool bf = a.in_dtype == DGA_BF16;
     if (a.out_dtype == DGA_F32) e = bf ? launch_typed<true, float>(p, a.stream) : launch_typed<false, float>(p, a.stream);

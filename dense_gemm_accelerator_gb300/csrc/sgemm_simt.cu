@@ -19,6 +19,10 @@
 //     warp stages 32 consecutive rows at one k, so the transposing stores hit
 //     32 consecutive words (no bank conflicts), and the 8 A values a thread
 //     needs per k are two 128-bit broadcast loads;
+//   * both operand layouts: a column-major A arrives k-major and is copied
+//     with 128-bit stores, a column-major B (N x K, e.g. the W^T of a
+//     fully-connected layer) takes the transposing stores of a row-major A;
+//     the epilogue adds an optional bias row;
 //   * tiles that lie wholly inside the matrices (and a K range that is a
 //     whole number of slices) run a copy of the main loop without any bounds
 //     checks; edge tiles load zeros outside M, N and K and mask their stores;
@@ -41,7 +45,7 @@ namespace {
 
 constexpr int BM = 128, BN = 128, BK = 8;
 constexpr int kThreads = 256;
-constexpr int kAStride = BM + 4;  // floats per k-row of the transposed A tile
+constexpr int kAStride = BM + 4;  // floats per k-row of the A and B tiles (BM == BN)
 constexpr int kSimtBlocksPerSm = 2;  // register budget: 65536 / (256 * 2) = 128 per thread
 
 struct Params {
@@ -63,11 +67,12 @@ struct Params {
     int64_t tiles_n, full_tiles, part_k;
     int parts;
     float* partials;
+    const float* bias;  // N values added to every row, or null
 };
 
 struct Smem {
     float A[2][BK][kAStride];  // A[buf][k][m]
-    float B[2][BK][BN];        // B[buf][k][n]
+    float B[2][BK][kAStride];  // B[buf][k][n] (padded like A: see the staging roles)
 };
 
 __device__ __forceinline__ float4 ld_f4(const float* p) {
@@ -88,41 +93,85 @@ __device__ __forceinline__ float4 ld_f4_checked(const float* row, int64_t col, i
 // tiles wholly inside M, N whose K range is a whole number of slices, with
 // 16-byte-friendly A and B.  `partial` non-null: write the raw accumulators
 // there (BM x BN, row-major) instead of the alpha/beta epilogue.
-template <bool kChecked, int kReadC = -1>
+// kTransA: A is stored K x M (column-major A), so its K-slice arrives
+// already k-major and is copied like row-major B, without the transposing
+// stores.  kTransB: B is stored N x K (column-major B); its slice is staged
+// the way row-major A is, through transposing stores.
+// kRunPtr: interior slices walk A and B with running pointers instead of
+// recomputing the addresses; measured faster for a column-major B and with a
+// bias row, slower for the plain row-major case (the register allocation at
+// 128 per thread differs), so the launcher chooses it per variant.
+template <bool kChecked, bool kTransA, bool kTransB, int kReadC = -1, int kBias = -1,
+          bool kRunPtr = false>
 __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t row0, int64_t col0,
                                            int64_t k_begin, int64_t k_end, float* partial) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
 
     // staging roles (one float4 of A and one of B per thread and slice):
-    // A row (lane + 32*(warp/2)) at k offset 4*(warp%2) -- a warp stages 32
-    // consecutive rows at one k, so the transposing stores are conflict-free;
-    // B row k = warp, columns 4*lane .. 4*lane + 3.
-    const int a_k = (warp & 1) * 4;
-    const int a_r = lane + 32 * (warp >> 1);
-    const int b_k = warp, b_c = lane * 4;
-    const bool a_ok = !kChecked || row0 + a_r < p.M;
-    const float* a_src = p.A + (a_ok ? row0 + a_r : 0) * p.lda;
-    const float* b_src = p.B + col0 + b_c;
+    // row-major A: row 16*warp + lane/2 at k offset 4*(lane%2) -- a lane pair
+    // reads one whole 32-byte sector of a row, and the transposing stores of
+    // a warp (16 rows, k and k+4; the padded stride puts k+4 16 banks away)
+    // hit 32 different banks; row-major B: row k = warp, columns 4*lane ..
+    // 4*lane + 3.  Column-major A is staged like row-major B (k = warp, rows
+    // 4*lane .. 4*lane + 3), column-major B like row-major A.  The lane-pair
+    // sectors measured 5-10% faster on GB300 than one float4 per row per warp.
+    const int a_k = kTransA ? warp : (lane & 1) * 4;
+    const int a_r = kTransA ? lane * 4 : warp * 16 + (lane >> 1);
+    const int b_k = kTransB ? (lane & 1) * 4 : warp;
+    const int b_c = kTransB ? warp * 16 + (lane >> 1) : lane * 4;
+    const bool a_ok = kTransA || !kChecked || row0 + a_r < p.M;
+    const bool b_ok = !kTransB || !kChecked || col0 + b_c < p.N;
+    const float* a_src = kTransA ? p.A + row0 + a_r : p.A + (a_ok ? row0 + a_r : 0) * p.lda;
+    const float* b_src = kTransB ? p.B + (b_ok ? col0 + b_c : 0) * p.ldb : p.B + col0 + b_c;
     const bool vec_a = p.vec_a != 0, vec_b = p.vec_b != 0;
+    const float* a_run = kTransA ? a_src + (k_begin + a_k) * p.lda : a_src + k_begin + a_k;
+    const float* b_run = kTransB ? b_src + k_begin + b_k : b_src + (k_begin + b_k) * p.ldb;
+    const int64_t a_step = kTransA ? BK * p.lda : BK;
+    const int64_t b_step = kTransB ? BK : BK * p.ldb;
 
     float4 ra, rb;
     auto fetch = [&](int64_t k0) {
-        if constexpr (!kChecked) {
-            ra = ld_f4(a_src + k0 + a_k);
-            rb = ld_f4(b_src + (k0 + b_k) * p.ldb);
+        if constexpr (!kChecked && kRunPtr) {
+            ra = ld_f4(a_run);
+            a_run += a_step;
+            rb = ld_f4(b_run);
+            b_run += b_step;
+        } else if constexpr (!kChecked) {
+            ra = kTransA ? ld_f4(a_src + (k0 + a_k) * p.lda) : ld_f4(a_src + k0 + a_k);
+            rb = kTransB ? ld_f4(b_src + k0 + b_k) : ld_f4(b_src + (k0 + b_k) * p.ldb);
         } else {
-            ra = ld_f4_checked(a_src, k0 + a_k, k_end, a_ok, vec_a);
-            const bool kok = k0 + b_k < k_end;
-            rb = ld_f4_checked(p.B + (kok ? k0 + b_k : 0) * p.ldb, col0 + b_c, p.N, kok, vec_b);
+            if constexpr (kTransA) {
+                const bool kok = k0 + a_k < k_end;
+                ra = ld_f4_checked(p.A + (kok ? k0 + a_k : 0) * p.lda, row0 + a_r, p.M, kok, vec_a);
+            } else {
+                ra = ld_f4_checked(a_src, k0 + a_k, k_end, a_ok, vec_a);
+            }
+            if constexpr (kTransB) {
+                rb = ld_f4_checked(b_src, k0 + b_k, k_end, b_ok, vec_b);
+            } else {
+                const bool kok = k0 + b_k < k_end;
+                rb = ld_f4_checked(p.B + (kok ? k0 + b_k : 0) * p.ldb, col0 + b_c, p.N, kok, vec_b);
+            }
         }
     };
     auto stash = [&](int buf) {
-        sm.A[buf][a_k + 0][a_r] = ra.x;
-        sm.A[buf][a_k + 1][a_r] = ra.y;
-        sm.A[buf][a_k + 2][a_r] = ra.z;
-        sm.A[buf][a_k + 3][a_r] = ra.w;
-        *reinterpret_cast<float4*>(&sm.B[buf][b_k][b_c]) = rb;
+        if constexpr (kTransA) {
+            *reinterpret_cast<float4*>(&sm.A[buf][a_k][a_r]) = ra;
+        } else {
+            sm.A[buf][a_k + 0][a_r] = ra.x;
+            sm.A[buf][a_k + 1][a_r] = ra.y;
+            sm.A[buf][a_k + 2][a_r] = ra.z;
+            sm.A[buf][a_k + 3][a_r] = ra.w;
+        }
+        if constexpr (kTransB) {
+            sm.B[buf][b_k + 0][b_c] = rb.x;
+            sm.B[buf][b_k + 1][b_c] = rb.y;
+            sm.B[buf][b_k + 2][b_c] = rb.z;
+            sm.B[buf][b_k + 3][b_c] = rb.w;
+        } else {
+            *reinterpret_cast<float4*>(&sm.B[buf][b_k][b_c]) = rb;
+        }
     };
 
     // compute roles: 2 (M) x 4 (N) warp tiles of 64 x 32; lane = lm*4 + ln
@@ -185,6 +234,19 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
     // that C takes float4 stores), -1 to decide at run time.
     const bool vec_c = kReadC >= 0 || p.vec_c != 0;
     const bool read_c = kReadC >= 0 ? kReadC == 1 : p.beta != 0.0f;
+    // the bias row (fully-connected layer): this thread's 8 columns, once.
+    // kBias: 1 / 0 when the caller knows whether there is one (the kernel
+    // without it then keeps the register allocation of a plain GEMM, which
+    // measured 5% faster at 4096^3 than a run-time test), -1 to test here.
+    const bool has_bias = kBias >= 0 ? kBias == 1 : p.bias != nullptr;
+    float bv[8];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t c = col0 + (h == 0 ? bn0 : bn1) + j;
+            bv[h * 4 + j] = (has_bias && (!kChecked || c < p.N)) ? p.bias[c] : 0.0f;
+        }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int64_t r = row0 + (i < 4 ? am0 + i : am1 + (i - 4));
@@ -202,13 +264,20 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
                 o.y = axpby(p.alpha, v[1], p.beta, o.y);
                 o.z = axpby(p.alpha, v[2], p.beta, o.z);
                 o.w = axpby(p.alpha, v[3], p.beta, o.w);
+                if (has_bias) {  // (x + 0 is not x for x = -0, so no add without a bias)
+                    o.x += bv[h * 4 + 0];
+                    o.y += bv[h * 4 + 1];
+                    o.z += bv[h * 4 + 2];
+                    o.w += bv[h * 4 + 3];
+                }
                 *dst = o;
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     if (!kChecked || c + j < p.N) {
                         const float old = read_c ? crow[c + j] : 0.0f;
-                        crow[c + j] = axpby(p.alpha, v[j], p.beta, old);
+                        const float o = axpby(p.alpha, v[j], p.beta, old);
+                        crow[c + j] = has_bias ? o + bv[h * 4 + j] : o;
                     }
                 }
             }
@@ -233,7 +302,7 @@ __device__ __forceinline__ void grouped_tile(int64_t t, int64_t tiles_m, int64_t
 
 // The general kernel: any shape, edge tiles, optional K split (1-D grid over
 // the tile schedule).
-template <int kMinBlocks>
+template <int kMinBlocks, bool kTransA, bool kTransB>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) sgemm_128x128_kernel(Params p) {
     __shared__ __align__(16) Smem sm;
     const int64_t b = blockIdx.x;
@@ -254,21 +323,22 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sgemm_128x128_kernel(Par
     const int64_t col0 = tn * BN;
     const bool interior = row0 + BM <= p.M && col0 + BN <= p.N && (k_end - k_begin) % BK == 0 &&
                           p.vec_a && p.vec_b;
-    if (interior) block_tile<false>(p, sm, row0, col0, k_begin, k_end, partial);
-    else block_tile<true>(p, sm, row0, col0, k_begin, k_end, partial);
+    if (interior) block_tile<false, kTransA, kTransB, -1, -1, kTransB>(p, sm, row0, col0, k_begin, k_end, partial);
+    else block_tile<true, kTransA, kTransB>(p, sm, row0, col0, k_begin, k_end, partial);
 }
 
 // The same tile code, specialised for problems made only of interior tiles
 // (M, N multiples of 128, K of 8, 16-byte-friendly A, B and C) with no K
 // split: one code path, a 2-D grid and the C read decided at compile time,
 // which measured faster on GB300 than the general kernel at 4096^3.
-template <int kMinBlocks, int kReadC>
+template <int kMinBlocks, bool kTransA, bool kTransB, int kReadC, int kBias>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) sgemm_128x128_interior_kernel(Params p) {
     __shared__ __align__(16) Smem sm;
     int64_t tm, tn;
     grouped_tile(static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x, gridDim.y, gridDim.x,
                  tm, tn);
-    block_tile<false, kReadC>(p, sm, tm * BM, tn * BN, 0, p.K, nullptr);
+    block_tile<false, kTransA, kTransB, kReadC, kBias, kTransB || kBias == 1>(p, sm, tm * BM, tn * BN,
+                                                                            0, p.K, nullptr);
 }
 
 // Sums the K-range partials of each tail tile in part order (so the result
@@ -298,7 +368,8 @@ __global__ void __launch_bounds__(kThreads) sgemm_tail_reduce(Params p) {
         for (int j = 0; j < 4; ++j) {
             if (col + j < p.N) {
                 const float old = p.beta != 0.0f ? crow[col + j] : 0.0f;
-                crow[col + j] = axpby(p.alpha, v[j], p.beta, old);
+                const float o = axpby(p.alpha, v[j], p.beta, old);
+                crow[col + j] = p.bias ? o + p.bias[col + j] : o;
             }
         }
     }
@@ -342,8 +413,32 @@ Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int sm_count) {
 }  // namespace
 
 bool simt_supports(const GemmArgs& a) {
-    return a.in_dtype == DGA_F32 && a.out_dtype == DGA_F32 && a.layout_b == DGA_ROW_MAJOR;
+    return a.in_dtype == DGA_F32 && a.out_dtype == DGA_F32;
 }
+
+namespace {
+
+template <bool kTransA, bool kTransB>
+void launch_simt_kernels(const Params& p, const GemmArgs& a, const Schedule& sc, bool all_interior,
+                         int64_t blocks) {
+    if (all_interior) {
+        dim3 grid(static_cast<unsigned>(a.N / BN), static_cast<unsigned>(a.M / BM));
+        const bool rc = a.beta_f != 0.0f, bias = a.bias != nullptr;
+        if (rc && bias)
+            sgemm_128x128_interior_kernel<kSimtBlocksPerSm, kTransA, kTransB, 1, 1><<<grid, kThreads, 0, a.stream>>>(p);
+        else if (rc)
+            sgemm_128x128_interior_kernel<kSimtBlocksPerSm, kTransA, kTransB, 1, 0><<<grid, kThreads, 0, a.stream>>>(p);
+        else if (bias)
+            sgemm_128x128_interior_kernel<kSimtBlocksPerSm, kTransA, kTransB, 0, 1><<<grid, kThreads, 0, a.stream>>>(p);
+        else
+            sgemm_128x128_interior_kernel<kSimtBlocksPerSm, kTransA, kTransB, 0, 0><<<grid, kThreads, 0, a.stream>>>(p);
+    } else {
+        sgemm_128x128_kernel<kSimtBlocksPerSm, kTransA, kTransB>
+            <<<static_cast<unsigned>(blocks), kThreads, 0, a.stream>>>(p);
+    }
+}
+
+}  // namespace
 
 size_t simt_workspace_size(const GemmArgs& a, int sm_count) {
     return plan_schedule(a.M, a.N, a.K, sm_count).partial_bytes;
@@ -362,22 +457,18 @@ cudaError_t simt_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches)
              a.alpha_f, a.beta_f, (a.ldc % 4 == 0 && aligned(a.C, 16)) ? 1 : 0,
              (a.lda % 4 == 0 && aligned(a.A, 16)) ? 1 : 0, (a.ldb % 4 == 0 && aligned(a.B, 16)) ? 1 : 0,
              sc.tiles_n, sc.full_tiles, sc.part_k, sc.parts,
-             sc.parts > 1 ? static_cast<float*>(a.ws) : nullptr};
+             sc.parts > 1 ? static_cast<float*>(a.ws) : nullptr, static_cast<const float*>(a.bias)};
     const int64_t tail = sc.tiles - sc.full_tiles;
     const int64_t blocks = sc.full_tiles + tail * sc.parts;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
     const bool all_interior = sc.parts == 1 && a.M % BM == 0 && a.N % BN == 0 && a.K % BK == 0 &&
                               p.vec_a && p.vec_b && p.vec_c && a.M / BM <= 65535 &&
                               a.N / BN <= 0x7fffffff;
-    if (all_interior) {
-        dim3 grid(static_cast<unsigned>(a.N / BN), static_cast<unsigned>(a.M / BM));
-        if (a.beta_f != 0.0f)
-            sgemm_128x128_interior_kernel<kSimtBlocksPerSm, 1><<<grid, kThreads, 0, a.stream>>>(p);
-        else
-            sgemm_128x128_interior_kernel<kSimtBlocksPerSm, 0><<<grid, kThreads, 0, a.stream>>>(p);
-    } else {
-        sgemm_128x128_kernel<kSimtBlocksPerSm><<<static_cast<unsigned>(blocks), kThreads, 0, a.stream>>>(p);
-    }
+    const bool ta = a.layout_a == DGA_COL_MAJOR, tb = a.layout_b == DGA_COL_MAJOR;
+    if (ta && tb) launch_simt_kernels<true, true>(p, a, sc, all_interior, blocks);
+    else if (ta) launch_simt_kernels<true, false>(p, a, sc, all_interior, blocks);
+    else if (tb) launch_simt_kernels<false, true>(p, a, sc, all_interior, blocks);
+    else launch_simt_kernels<false, false>(p, a, sc, all_interior, blocks);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     ++*launches;

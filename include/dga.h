@@ -120,6 +120,50 @@ int dga_gemm(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
              void* C, int64_t ldc,
              void* workspace, size_t workspace_bytes, dga_stream_t stream);
 
+/*
+ * dga_gemm_general -- the general form:
+ *     C <- alpha * op(A) * op(B) + beta * C + bias
+ * with the layout of A as well as of B, and an optional bias row, which is
+ * the fully-connected layer of "AI Programming: Matrix Product", section
+ * "Fully-connected layer" (Y = X W^T + b).
+ *   layout_a   DGA_ROW_MAJOR: A(i, k) = A[i*lda + k], lda >= max(1, K)
+ *              DGA_COL_MAJOR: A(i, k) = A[k*lda + i], lda >= max(1, M)
+ *              (A stored K x M; e.g. the G^T of a weight gradient G^T X)
+ *   bias       device pointer to N elements of the output type (int32_t for
+ *              DGA_I8 inputs) added to every row of the result, or NULL.
+ *              With alpha == 0 or K == 0 the result is beta*C + bias.
+ * Argument errors are -(position in this list): -5 M, -6 N, -7 K, -8 alpha,
+ * -9 A, -10 lda, -11 B, -12 ldb, -13 beta, -14 C, -15 ldc, -17 workspace,
+ * -19 path; the bias must not overlap C (DGA_ERR_OVERLAP).  Other arguments
+ * as for dga_gemm_ex.  The SKINNY family needs a row-major A; the tensor-core
+ * family repacks a column-major A into the workspace.
+ */
+int dga_gemm_general(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_a,
+                     dga_layout layout_b, int64_t M, int64_t N, int64_t K,
+                     const void* alpha, const void* A, int64_t lda,
+                     const void* B, int64_t ldb, const void* beta,
+                     void* C, int64_t ldc, const void* bias,
+                     void* workspace, size_t workspace_bytes, dga_path path,
+                     dga_stream_t stream);
+
+/* Workspace for dga_gemm_general, as dga_gemm_workspace_size is for dga_gemm_ex. */
+size_t dga_gemm_general_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype,
+                                       dga_layout layout_a, dga_layout layout_b,
+                                       int64_t M, int64_t N, int64_t K,
+                                       int64_t lda, int64_t ldb, int64_t ldc, dga_path path);
+
+/*
+ * dga_sum_rows -- out[j] = sum over i < rows of G(i, j), j < cols, in fp32:
+ * the bias gradient of the fully-connected layer (same page and section: the
+ * output gradient summed over the batch).  G is row-major (G(i, j) =
+ * G[i*ldg + j], ldg >= max(1, cols)) of DGA_F32, DGA_BF16 or DGA_F16; out is
+ * a device array of cols floats.  The summation order is fixed, so results
+ * are reproducible.  Errors: -2 rows < 0, -3 cols < 0, -4 G NULL, -5 ldg too
+ * small, -6 out NULL; DGA_ERR_UNSUPPORTED for other dtypes.
+ */
+int dga_sum_rows(dga_dtype dtype, int64_t rows, int64_t cols, const void* G, int64_t ldg,
+                 float* out, dga_stream_t stream);
+
 /* dga_gemm with the kernel family forced (argument 17).  Same semantics. */
 int dga_gemm_ex(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
                 int64_t M, int64_t N, int64_t K,

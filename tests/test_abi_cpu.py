@@ -112,3 +112,73 @@ def test_binding_layout_from_strides():
         dga.operand_layout(A.t(), torch.empty(5, 7), torch.empty(5, 7))
     with pytest.raises(ValueError):
         dga.operand_layout(A, torch.empty(10, 14)[::2, ::2], C)
+
+
+def _call_general(**over):
+    one, zero = ctypes.c_float(1.0), ctypes.c_float(0.0)
+    args = dict(in_dtype=gen.F32, out_dtype=gen.F32, layout_a=gen.ROW_MAJOR,
+                layout_b=gen.ROW_MAJOR, M=4, N=4, K=4, alpha=ctypes.byref(one), A=0x1000, lda=4,
+                B=0x2000, ldb=4, beta=ctypes.byref(zero), C=0x3000, ldc=4, bias=None,
+                workspace=None, workspace_bytes=0, path=dga.PATH_AUTO, stream=None)
+    args.update(over)
+    return dga.dga_gemm_general(*args.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(M=-1), -5), (dict(N=-1), -6), (dict(K=-1), -7), (dict(alpha=None), -8),
+    (dict(A=None), -9), (dict(lda=3), -10), (dict(B=None), -11), (dict(ldb=3), -12),
+    (dict(beta=None), -13), (dict(C=None), -14), (dict(ldc=3), -15),
+    (dict(workspace=None, workspace_bytes=16), -17), (dict(path=9), -19),
+    (dict(layout_a=5), dga.ERR_UNSUPPORTED),
+    (dict(C=0x1004), dga.ERR_OVERLAP),
+    (dict(bias=0x3008), dga.ERR_OVERLAP),   # bias inside C
+])
+def test_general_argument_errors(lib, over, code):
+    assert _call_general(**over) == code
+
+
+def test_general_col_major_lda_rule(lib):
+    # column-major A is stored K x M: lda >= M, not >= K
+    assert _call_general(layout_a=gen.COL_MAJOR, M=8, K=4, lda=4, ldc=4, C=0x9000) == -10
+
+
+def test_general_m_zero_is_a_no_op(lib):
+    assert _call_general(M=0, A=None, C=None, layout_a=gen.COL_MAJOR) == dga.OK
+
+
+def test_general_workspace_size_query(lib):
+    # column-major A on the tensor cores is transposed into the workspace
+    ws = dga.dga_gemm_general_workspace_size(gen.BF16, gen.F32, gen.COL_MAJOR, gen.COL_MAJOR,
+                                             256, 512, 1024, 256, 1024, 512, dga.PATH_TCGEN05)
+    assert ws >= 256 * 1024 * 2
+    assert dga.dga_gemm_general_workspace_size(gen.BF16, gen.F32, gen.ROW_MAJOR, gen.COL_MAJOR,
+                                               256, 512, 1024, 1024, 1024, 512,
+                                               dga.PATH_TCGEN05) == 0
+    # the row-major-A query agrees with the older entry point
+    assert dga.dga_gemm_general_workspace_size(
+        gen.I8, gen.I32, gen.ROW_MAJOR, gen.ROW_MAJOR, 100, 200, 300, 300, 200, 200,
+        dga.PATH_TCGEN05) == dga.dga_gemm_workspace_size(
+        gen.I8, gen.I32, gen.ROW_MAJOR, 100, 200, 300, 300, 200, 200, dga.PATH_TCGEN05)
+
+
+@pytest.mark.parametrize("args,code", [
+    ((gen.I8, 4, 4, 0x1000, 4, 0x2000), dga.ERR_UNSUPPORTED),
+    ((gen.F32, -1, 4, 0x1000, 4, 0x2000), -2),
+    ((gen.F32, 4, -1, 0x1000, 4, 0x2000), -3),
+    ((gen.F32, 4, 4, None, 4, 0x2000), -4),
+    ((gen.F32, 4, 4, 0x1000, 3, 0x2000), -5),
+    ((gen.F32, 4, 4, 0x1000, 4, None), -6),
+    ((gen.BF16, 4, 0, None, 1, None), dga.OK),   # no columns: nothing to do
+])
+def test_sum_rows_argument_errors(lib, args, code):
+    assert dga.dga_sum_rows(*args, None) == code
+
+
+def test_binding_general_layouts():
+    # a transposed view is column-major with its storage row length as ld
+    W = torch.empty(7, 5)
+    assert dga._layout_of(W, "W") == (gen.ROW_MAJOR, 5)
+    assert dga._layout_of(W.t(), "W") == (gen.COL_MAJOR, 5)
+    assert dga._layout_of(torch.empty(10, 14)[:, :6], "W") == (gen.ROW_MAJOR, 14)
+    with pytest.raises(ValueError):
+        dga._layout_of(torch.empty(10, 14)[::2, ::2], "W")
