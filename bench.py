@@ -9,9 +9,11 @@ step touches are never in L2 from the step before (the rotation spans more
 than 2x the 129 MB L2).  Rank 0 prints ONE JSON line.
 
 Extra keys beside the contract's: `per_dtype` (the other hot-path workloads
--- BF16 8192^3 on tcgen05, skinny M in {1, 8, 16}, INT8 4093x4099x4096 --
-each timed the same way, with its roofline fraction) and `peaks` (where every
-denominator came from).
+-- BF16 8192^3 on tcgen05, skinny M in {1, 8, 16}, INT8 4093x4099x4096, FP16
+8192^3, BF16 8192^3 with a row-major B, and one fully-connected layer step
+(forward, both gradient GEMMs and the bias gradient) in bf16 at 8192 and in
+fp32 at 4096 -- each timed the same way, with its roofline fraction) and
+`peaks` (where every denominator came from).
 
 `--impl reference` times the CPU oracle (plain fp64 triple loop, as it
 stands) on the host cores, on a bounded sample of the same workload.
@@ -64,7 +66,25 @@ def tile_intensity(T, elem_bytes=4):
     return (2 * T ** 3) / (elem_bytes * 2 * T ** 2)
 
 
+def fc_accounting(w):
+    """One fully-connected layer step ("AI Programming: Matrix Product",
+    section "Fully-connected layer"): batch b = M, n_in = K, n_out = N.
+    Three GEMMs of 2*b*n_in*n_out FLOPs each (Y = X W^T, dX = G W,
+    dW = G^T X) plus b*n_out adds for db.  Bytes: each GEMM's operands once
+    (X, W, Y + the bias row; G, W, dX; G, X, dW) and G read once more for db."""
+    b, n_in, n_out = w.M, w.K, w.N
+    e, o = DTYPE_BYTES[w.in_dtype], DTYPE_BYTES[w.out_dtype]
+    fl = 3 * gemm_flops(b, n_out, n_in) + b * n_out
+    by = (gemm_bytes(b, n_out, n_in, e, o, False) + o * n_out      # forward + bias row
+          + gemm_bytes(b, n_in, n_out, e, o, False)                 # dX
+          + gemm_bytes(n_out, n_in, b, e, o, False)                 # dW
+          + e * b * n_out + 4 * n_out)                              # db
+    return fl, by
+
+
 def workload_accounting(w):
+    if w.kind == "fc":
+        return fc_accounting(w)
     fl = gemm_flops(w.M, w.N, w.K)
     by = gemm_bytes(w.M, w.N, w.K, DTYPE_BYTES[w.in_dtype], DTYPE_BYTES[w.out_dtype], w.beta != 0)
     return fl, by
@@ -219,10 +239,82 @@ class Runner:
         return dga.dga_last_launch_count()
 
 
+class FcRunner:
+    """Device-resident inputs of one fully-connected layer step and the four
+    library calls that make it: Y = X W^T + b (W^T is the column-major view
+    of W [n_out, n_in]), dX = G W, dW = G^T X (G^T is the column-major view
+    of G [batch, n_out]) and db = the batch sum of G."""
+
+    def __init__(self, w, device, sets, seed=0):
+        import torch
+
+        import dense_gemm_accelerator_gb300 as dga
+        from dense_gemm_accelerator_gb300 import inputs as gen
+        self.w, self.dga, self.gen = w, dga, gen
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        b, n_in, n_out = w.M, w.K, w.N
+        draw = Runner._draw
+        self.sets = []
+        for _ in range(sets):
+            X = draw((b, n_in), w.dist_a, w.in_dtype, g, device)
+            W = draw((n_out, n_in), w.dist_b, w.in_dtype, g, device)
+            bias = draw((n_out,), w.dist_b, w.out_dtype, g, device)
+            G = draw((b, n_out), w.dist_c, w.in_dtype, g, device)
+            self.sets.append((X, W, bias, G))
+        odt = gen.TORCH_DTYPE[w.out_dtype]
+        self.Y = torch.empty((b, n_out), dtype=odt, device=device)
+        self.dX = torch.empty((b, n_in), dtype=odt, device=device)
+        self.dW = torch.empty((n_out, n_in), dtype=odt, device=device)
+        self.db = torch.empty((n_out,), dtype=torch.float32, device=device)
+        R, C = gen.ROW_MAJOR, gen.COL_MAJOR
+        # (layout_a, layout_b, M, N, K, lda, ldb, ldc) of forward, dX, dW
+        self.shapes = [(R, C, b, n_out, n_in, n_in, n_in, n_out),
+                       (R, R, b, n_in, n_out, n_out, n_in, n_in),
+                       (C, R, n_out, n_in, b, n_out, n_in, n_in)]
+        self.ws_bytes = max(dga.dga_gemm_general_workspace_size(w.in_dtype, w.out_dtype, *sh,
+                                                                dga.PATH_AUTO)
+                            for sh in self.shapes)
+        self.ws = torch.empty(max(self.ws_bytes, 1), dtype=torch.uint8, device=device)
+        self.one = dga.scalar(1.0, w.in_dtype)
+        self.zero = dga.scalar(0.0, w.in_dtype)
+        self.paths = []
+
+    def call(self, i, stream):
+        import ctypes
+        X, W, bias, G = self.sets[i % len(self.sets)]
+        w, dga = self.w, self.dga
+        operands = [(X, W, self.Y, bias), (G, W, self.dX, None), (G, X, self.dW, None)]
+        launches = 0
+        self.paths = []
+        for sh, (A, B, C, bv) in zip(self.shapes, operands):
+            la, lb, M, N, K, lda, ldb, ldc = sh
+            st = dga.dga_gemm_general(w.in_dtype, w.out_dtype, la, lb, M, N, K,
+                                      ctypes.byref(self.one), A.data_ptr(), lda, B.data_ptr(), ldb,
+                                      ctypes.byref(self.zero), C.data_ptr(), ldc,
+                                      bv.data_ptr() if bv is not None else None,
+                                      self.ws.data_ptr(), self.ws_bytes, dga.PATH_AUTO, stream)
+            if st != dga.OK:
+                raise dga.DgaError(st, f"dga_gemm_general ({w.name})")
+            launches += dga.dga_last_launch_count()
+            self.paths.append(dga.PATH_NAMES[dga.dga_last_path()])
+        st = dga.dga_sum_rows(w.in_dtype, w.M, w.N, G.data_ptr(), w.N, self.db.data_ptr(), stream)
+        if st != dga.OK:
+            raise dga.DgaError(st, f"dga_sum_rows ({w.name})")
+        return launches + 1
+
+
+def runner_for(w, device, sets, seed=0):
+    return (FcRunner if w.kind == "fc" else Runner)(w, device, sets, seed)
+
+
 def sets_for(w, min_sets=2):
     """Enough input sets that one rotation spans > 2x L2."""
     from dense_gemm_accelerator_gb300 import inputs as gen
-    per = DTYPE_BYTES[w.in_dtype] * (w.M * w.K + w.K * w.N) + DTYPE_BYTES[w.out_dtype] * w.M * w.N
+    if w.kind == "fc":  # X, W, G (the outputs are shared by all sets)
+        per = DTYPE_BYTES[w.in_dtype] * (w.M * w.K + w.N * w.K + w.M * w.N)
+    else:
+        per = DTYPE_BYTES[w.in_dtype] * (w.M * w.K + w.K * w.N) + DTYPE_BYTES[w.out_dtype] * w.M * w.N
     n = max(min_sets, -(-2 * L2_BYTES // per) + 1)
     del gen
     return int(n)
@@ -263,7 +355,9 @@ def roofline_for(w, ms_mean, peaks, sustained=False):
     pk = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
     return {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s" if w.in_dtype != gen.I8 else "TOP/s",
             "frac": ach / pk, "algorithmic_flops": fl,
-            "peak_kind": "bf16 tensor (INT8 runs as exact bf16 products)" if w.in_dtype == gen.I8 else "bf16 tensor"}
+            "peak_kind": {gen.I8: "bf16 tensor (INT8 runs as exact bf16 products)",
+                          gen.F16: "bf16 tensor (fp16 has the same nominal rate)"}.get(
+                              w.in_dtype, "bf16 tensor")}
 
 
 def traffic_record(kernel_src, workload):
@@ -540,18 +634,23 @@ def main():
     if rank == 0 and world == 1 and not args.no_extras:
         line["e2e"] = e2e_leg(w, max(3, args.steps // 3), 2, device)
         per = {}
-        for name in ("bf16_8192", "skinny_m1", "skinny_m8", "skinny_m16", "int8_ragged"):
+        for name in ("bf16_8192", "skinny_m1", "skinny_m8", "skinny_m16", "int8_ragged",
+                     "f16_8192", "bf16_8192_rowb", "fc_bf16_8192", "fc_f32_4096"):
             if name == w.name:
                 continue
             ow = gen.WORKLOADS[name]
-            r = Runner(ow, device, sets_for(ow, 3 if name.startswith("skinny") else 2))
-            iters = 200 if name.startswith("skinny") else 30
-            ms, nl = time_kernel(r, iters, 5)
+            r = runner_for(ow, device, sets_for(ow, 3 if name.startswith("skinny") else 2))
+            iters = 200 if name.startswith("skinny") else (10 if ow.kind == "fc" else 30)
+            ms, nl = time_kernel(r, iters, 5 if ow.kind != "fc" else 2)
             rf = roofline_for(ow, ms, peaks)
-            rf["traffic"] = traffic_record(source_of(ow), name)
+            rf["traffic"] = traffic_record(source_of(ow), name) if ow.kind == "gemm" else None
             rf["ms_mean"] = ms
             rf["launches_per_call"] = nl / iters
-            rf["path"] = dga.PATH_NAMES[dga.dga_last_path()]
+            if ow.kind == "fc":
+                rf["paths"] = r.paths
+                rf["algorithmic_bytes"] = workload_accounting(ow)[1]
+            else:
+                rf["path"] = dga.PATH_NAMES[dga.dga_last_path()]
             if rf["bound"] == "tensor":
                 rf["frac_of_sustained"] = rf["achieved"] / peaks["bf16_tflops_sustained"]
             per[name] = rf

@@ -28,10 +28,15 @@
 //     drains its outstanding copies and MMAs and frees its TMEM before
 //     returning (read with dga_sync_status()).
 //
-// Operands reach the kernel K-major (A row-major, B column-major).  Other
-// layouts -- column-major A, row-major B, a leading dimension TMA cannot
-// express, or INT8 inputs (encoded exactly as bf16, see below) -- are first
-// repacked into the caller's workspace by pack_rows_kernel / pack_transposed_kernel.
+// Operands reach the tensor cores in their own layout: K-major (A row-major,
+// B column-major) as 64 x rows boxes, or MN-major (A column-major, B
+// row-major: the G^T and W of a fully-connected layer's gradients) as boxes of
+// 64 MN-elements x 64 k, one per 64 rows of the tile, read by the MMA through
+// MN-major descriptors (transpose bits of the instruction descriptor).  Only
+// a leading dimension TMA cannot express (not a multiple of 16 bytes, or an
+// unaligned base) and INT8 inputs (encoded exactly as bf16, see below) are
+// first repacked into the caller's workspace by pack_rows_kernel /
+// pack_transposed_kernel.
 //
 // INT8 x INT8 -> INT32 (tcgen05 has no integer MMA on sm_103a: ptxas rejects
 // kind::i8 for this target).  Every int8 value is an exact bf16, every
@@ -68,6 +73,13 @@ constexpr int UK = 16;   // K per tcgen05.mma (kind::f16)
 constexpr int kStages = 4;
 constexpr int kI8ChunkBlocks = 16;  // INT8: K blocks per exact fp32 chunk (16 x 64 = 1024)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
+constexpr uint32_t kMnAtom = 64;                        // MN-elements per MN-major box
+constexpr uint32_t kMnBoxBytes = kMnAtom * BK * 2;      // one 64 x 64 box: 8 KB
+// Descriptor start-address steps (16-byte units) per K = 16 MMA: 32 bytes
+// along the swizzle row when K-major, 16 k-rows of 128 bytes when MN-major.
+constexpr uint32_t kStepKMajor = (UK * 2) >> 4;
+constexpr uint32_t kStepMnMajor = (UK * 128) >> 4;
+static_assert(BM % kMnAtom == 0, "MN-major A boxes tile the block rows");
 
 enum : int { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3, kRoleSelfTest = 4 };
 
@@ -78,6 +90,7 @@ struct TcParams {
     float alpha, beta;
     int32_t alpha_i, beta_i;
     const void* bias;  // N output-type (int32 for INT8) values added to every row, or null
+    uint32_t a_mn, b_mn;  // operand stored MN-major (column-major A / row-major B)
     uint32_t tiles_m, tiles_n, num_tiles, num_kb;
     uint32_t group_m;  // tile rows per raster group
 };
@@ -182,6 +195,7 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    TcParams p) {
     constexpr int kEpiWarps = kI8 ? 16 : 4;
+    static_assert(BN % kMnAtom == 0, "MN-major B boxes tile the block columns");
     using S = Smem<BN, kI8 ? 8 : 4>;
     constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
     constexpr uint32_t kIdesc = idesc_f16(kBf16, BM, BN);
@@ -243,10 +257,21 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                     uint8_t* a_dst = smem + stage * S::kStageBytes;
                     uint8_t* b_dst = a_dst + S::kABytes;
                     mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
-                    tma_load_2d(a_dst, &tmA, &full[stage], static_cast<int32_t>(kb * BK),
-                                static_cast<int32_t>(tm * BM));
-                    tma_load_2d(b_dst, &tmB, &full[stage], static_cast<int32_t>(kb * BK),
-                                static_cast<int32_t>(tn * BN));
+                    const int32_t k0 = static_cast<int32_t>(kb * BK);
+                    if (p.a_mn) {
+                        for (uint32_t j = 0; j < BM / kMnAtom; ++j)
+                            tma_load_2d(a_dst + j * kMnBoxBytes, &tmA, &full[stage],
+                                        static_cast<int32_t>(tm * BM + j * kMnAtom), k0);
+                    } else {
+                        tma_load_2d(a_dst, &tmA, &full[stage], k0, static_cast<int32_t>(tm * BM));
+                    }
+                    if (p.b_mn) {
+                        for (uint32_t j = 0; j < BN / kMnAtom; ++j)
+                            tma_load_2d(b_dst + j * kMnBoxBytes, &tmB, &full[stage],
+                                        static_cast<int32_t>(tn * BN + j * kMnAtom), k0);
+                    } else {
+                        tma_load_2d(b_dst, &tmB, &full[stage], k0, static_cast<int32_t>(tn * BN));
+                    }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
                     if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -263,6 +288,9 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            const uint32_t idesc = idesc_major(kIdesc, p.a_mn, p.b_mn);
+            const uint32_t a_step = p.a_mn ? kStepMnMajor : kStepKMajor;
+            const uint32_t b_step = p.b_mn ? kStepMnMajor : kStepKMajor;
             bool ok = true;
             for (uint32_t t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
                 const uint32_t n_chunks = kI8 ? (p.num_kb + kI8ChunkBlocks - 1) / kI8ChunkBlocks : 1;
@@ -284,12 +312,14 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                         }
                         tc_fence_after();
                         const uint32_t a_addr = smem_u32(smem + stage * S::kStageBytes);
-                        const uint64_t a_desc = smem_desc_kmajor_sw128(a_addr);
-                        const uint64_t b_desc = smem_desc_kmajor_sw128(a_addr + S::kABytes);
+                        const uint64_t a_desc = p.a_mn ? smem_desc_mnmajor_sw128(a_addr, kMnBoxBytes)
+                                                       : smem_desc_kmajor_sw128(a_addr);
+                        const uint64_t b_desc =
+                            p.b_mn ? smem_desc_mnmajor_sw128(a_addr + S::kABytes, kMnBoxBytes)
+                                   : smem_desc_kmajor_sw128(a_addr + S::kABytes);
 #pragma unroll
                         for (int k = 0; k < BK / UK; ++k) {
-                            // +32 bytes along K inside the 128-byte swizzle row
-                            tc_mma_f16(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc,
+                            tc_mma_f16(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc,
                                        (kb > kb_begin || k > 0) ? 1u : 0u);
                         }
                         tc_commit(&empty[stage]);
@@ -502,8 +532,21 @@ __global__ void __launch_bounds__(192, 1)
                     uint8_t* b_dst = a_dst + S::kABytes;
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * S::kStageBytes);
                     const uint32_t bar = map_to_cta(smem_u32(&full[stage]), 0);
-                    tma_load_2d_pair(a_dst, &tmA, bar, static_cast<int32_t>(kb * BK), a_row);
-                    tma_load_2d_pair(b_dst, &tmB, bar, static_cast<int32_t>(kb * BK), b_row);
+                    const int32_t k0 = static_cast<int32_t>(kb * BK);
+                    if (p.a_mn) {
+                        for (uint32_t j = 0; j < BM / kMnAtom; ++j)
+                            tma_load_2d_pair(a_dst + j * kMnBoxBytes, &tmA, bar,
+                                             a_row + static_cast<int32_t>(j * kMnAtom), k0);
+                    } else {
+                        tma_load_2d_pair(a_dst, &tmA, bar, k0, a_row);
+                    }
+                    if (p.b_mn) {
+                        for (uint32_t j = 0; j < (kPairBN / 2) / kMnAtom; ++j)
+                            tma_load_2d_pair(b_dst + j * kMnBoxBytes, &tmB, bar,
+                                             b_row + static_cast<int32_t>(j * kMnAtom), k0);
+                    } else {
+                        tma_load_2d_pair(b_dst, &tmB, bar, k0, b_row);
+                    }
                     if (++stage == kPairStages) { stage = 0; phase ^= 1; }
                 }
             }
@@ -513,6 +556,9 @@ __global__ void __launch_bounds__(192, 1)
         // ------------------------------------------------ MMA issuer (leader only)
         if (leader && lane == 0) {
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            const uint32_t idesc = idesc_major(kIdesc, p.a_mn, p.b_mn);
+            const uint32_t a_step = p.a_mn ? kStepMnMajor : kStepKMajor;
+            const uint32_t b_step = p.b_mn ? kStepMnMajor : kStepKMajor;
             bool ok = true;
             for (uint32_t t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
                 if (!mbar_wait_bounded<true>(&acc_empty[acc], acc_phase ^ 1, abort_flag,
@@ -530,11 +576,14 @@ __global__ void __launch_bounds__(192, 1)
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + stage * S::kStageBytes);
-                    const uint64_t a_desc = smem_desc_kmajor_sw128(a_addr);
-                    const uint64_t b_desc = smem_desc_kmajor_sw128(a_addr + S::kABytes);
+                    const uint64_t a_desc = p.a_mn ? smem_desc_mnmajor_sw128(a_addr, kMnBoxBytes)
+                                                   : smem_desc_kmajor_sw128(a_addr);
+                    const uint64_t b_desc =
+                        p.b_mn ? smem_desc_mnmajor_sw128(a_addr + S::kABytes, kMnBoxBytes)
+                               : smem_desc_kmajor_sw128(a_addr + S::kABytes);
 #pragma unroll
                     for (int k = 0; k < BK / UK; ++k)
-                        tc_mma_f16_pair(d_tmem, a_desc + 2 * k, b_desc + 2 * k, kIdesc,
+                        tc_mma_f16_pair(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     tc_commit_pair_multicast(&empty[stage], kBothCtas);
                     if (++stage == kPairStages) { stage = 0; phase ^= 1; }
@@ -733,6 +782,23 @@ cudaError_t make_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, in
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// MN-major operand: MN x K elements of 2 bytes with MN contiguous, k-row
+// stride ld elements; boxes of 64 MN-elements x 64 k.
+cudaError_t make_mnmajor_map(CUtensorMap* map, const void* base, int64_t mn, int64_t K,
+                             int64_t ld, bool bf16) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(mn), static_cast<cuuint64_t>(K)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    cuuint32_t box[2] = {kMnAtom, static_cast<cuuint32_t>(BK)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 constexpr int kBnFloat = 256;
 constexpr int kBnI8 = 256;
 constexpr size_t kWsAlign = 256;
@@ -742,6 +808,7 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 // Which operands need repacking into the workspace.
 struct PackPlan {
     bool pack_a, pack_b;
+    bool a_mn, b_mn;  // read in place MN-major (column-major A / row-major B)
     int64_t kp;  // padded K of packed operands (multiple of 8 elements = 16 bytes)
     size_t a_bytes, b_bytes;
 };
@@ -750,8 +817,12 @@ PackPlan plan_for(const GemmArgs& a) {
     PackPlan pl{};
     pl.kp = round_up(a.K, 8);
     const bool i8 = a.in_dtype == DGA_I8;
-    pl.pack_a = i8 || a.layout_a != DGA_ROW_MAJOR || a.lda % 8 != 0 || !aligned(a.A, 16);
-    pl.pack_b = i8 || a.layout_b != DGA_COL_MAJOR || a.ldb % 8 != 0 || !aligned(a.B, 16);
+    // TMA needs 16-byte row strides and a 16-byte aligned base; INT8 is
+    // always re-encoded (as bf16, K-major).
+    pl.pack_a = i8 || a.lda % 8 != 0 || !aligned(a.A, 16);
+    pl.pack_b = i8 || a.ldb % 8 != 0 || !aligned(a.B, 16);
+    pl.a_mn = !pl.pack_a && a.layout_a == DGA_COL_MAJOR;
+    pl.b_mn = !pl.pack_b && a.layout_b == DGA_ROW_MAJOR;
     pl.a_bytes = pl.pack_a ? round_up(a.M * pl.kp * 2, kWsAlign) : 0;
     pl.b_bytes = pl.pack_b ? round_up(a.N * pl.kp * 2, kWsAlign) : 0;
     return pl;
@@ -918,9 +989,11 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     const bool pair = !i8 && a.M > BM;
     const int BN = i8 ? kBnI8 : (pair ? kPairBN : kBnFloat);
     CUtensorMap ma, mb;
-    e = make_kmajor_map(&ma, A, a.M, a.K, lda, BM, bf16);
+    e = pl.a_mn ? make_mnmajor_map(&ma, A, a.M, a.K, lda, bf16)
+                : make_kmajor_map(&ma, A, a.M, a.K, lda, BM, bf16);
     if (e != cudaSuccess) return e;
-    e = make_kmajor_map(&mb, B, a.N, a.K, ldb, pair ? kPairBN / 2 : BN, bf16);
+    e = pl.b_mn ? make_mnmajor_map(&mb, B, a.N, a.K, ldb, bf16)
+                : make_kmajor_map(&mb, B, a.N, a.K, ldb, pair ? kPairBN / 2 : BN, bf16);
     if (e != cudaSuccess) return e;
 
     TcParams p{};
@@ -934,6 +1007,8 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     p.alpha_i = a.alpha_i;
     p.beta_i = a.beta_i;
     p.bias = a.bias;
+    p.a_mn = pl.a_mn ? 1u : 0u;
+    p.b_mn = pl.b_mn ? 1u : 0u;
     const int tile_m = pair ? 2 * BM : BM;
     p.tiles_m = static_cast<uint32_t>((a.M + tile_m - 1) / tile_m);
     p.tiles_n = static_cast<uint32_t>((a.N + BN - 1) / BN);

@@ -192,6 +192,23 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand (M or N the
+// contiguous dimension) in the 128-byte swizzle layout that a TMA load of a
+// box of 64 MN-elements x 64 k writes: each k is one 128-byte row holding 64
+// consecutive MN-elements, 8 k-rows make one 1024-byte swizzle atom.
+//   leading-dimension byte offset: between atoms along MN (64 elements apart)
+//   stride-dimension byte offset:  between atoms along K (8 k-rows apart: 1024)
+// Other fields as for the K-major form.
+__device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_atom_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((mn_atom_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
 // Instruction descriptor for kind::f16:
 //   bits 4-5 D format (1 = f32), bits 7-9 A format, bits 10-12 B format
 //   (0 = f16, 1 = bf16), bit 15/16 A/B major (0 = K-major),
@@ -199,6 +216,10 @@ __device__ __forceinline__ uint64_t smem_desc_kmajor_sw128(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, uint32_t m, uint32_t n) {
     return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
            ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+// The same with A and/or B MN-major (bits 15 and 16 set).
+__host__ __device__ constexpr uint32_t idesc_major(uint32_t idesc, uint32_t a_mn, uint32_t b_mn) {
+    return idesc | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
 }
 
 // ------------------------------------------------- CTA pairs (cta_group::2) --

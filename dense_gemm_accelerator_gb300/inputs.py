@@ -47,6 +47,11 @@ class Workload:
     dist_c: tuple = ("uniform",)
     seed: int = 0
     note: str = field(default="", compare=False)
+    # "gemm": one C <- alpha*A*B + beta*C.  "fc": one fully-connected layer
+    # step with batch M, N outputs and K inputs -- forward Y = X W^T + b and
+    # backward dX = G W, dW = G^T X, db = sum over the batch of G; dist_a
+    # draws X, dist_b W and b, dist_c the output gradient G.
+    kind: str = "gemm"
 
 
 WORKLOADS = {
@@ -69,6 +74,18 @@ WORKLOADS = {
     "int8_ragged": Workload("int8_ragged", I8, I32, ROW_MAJOR, 4093, 4099, 4096, 1, 0,
                             ("int8",), ("int8",), ("int8",),
                             note="INT8 x INT8 -> INT32, M=4093 N=4099 K=4096"),
+    "f16_8192": Workload("f16_8192", F16, F32, COL_MAJOR, 8192, 8192, 8192, 1.0, 0.0,
+                         ("normal", 1.0), ("normal", 1.0),
+                         note="FP16 in, FP32 out, M=N=K=8192, B column-major"),
+    "bf16_8192_rowb": Workload("bf16_8192_rowb", BF16, F32, ROW_MAJOR, 8192, 8192, 8192, 1.0,
+                               0.0, ("normal", 1.0), ("normal", 1.0),
+                               note="BF16 in, FP32 out, M=N=K=8192, B row-major"),
+    "fc_bf16_8192": Workload("fc_bf16_8192", BF16, BF16, COL_MAJOR, 8192, 8192, 8192, 1.0, 0.0,
+                             ("normal", 1.0), ("normal", 0.02), ("normal", 1.0), kind="fc",
+                             note="fully-connected layer step, bf16, batch 8192, 8192 -> 8192"),
+    "fc_f32_4096": Workload("fc_f32_4096", F32, F32, COL_MAJOR, 4096, 4096, 4096, 1.0, 0.0,
+                            kind="fc",
+                            note="fully-connected layer step, fp32, batch 4096, 4096 -> 4096"),
 }
 
 

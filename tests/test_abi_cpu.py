@@ -94,9 +94,12 @@ def test_workspace_size_query(lib):
     w = W["bf16_8192"]
     assert dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
                                        w.K, w.N, dga.PATH_TCGEN05) == 0
-    # row-major B is transposed into the workspace
+    # row-major B is read in place (MN-major) unless TMA cannot express its
+    # leading dimension; then it is transposed into the workspace
     assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.ROW_MAJOR, 256, 512, 100, 104,
-                                       512, 512, dga.PATH_TCGEN05) >= 512 * 104 * 2
+                                       512, 512, dga.PATH_TCGEN05) == 0
+    assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.ROW_MAJOR, 256, 512, 100, 104,
+                                       513, 512, dga.PATH_TCGEN05) >= 512 * 104 * 2
     assert dga.dga_gemm_workspace_size(gen.F32, gen.F32, gen.ROW_MAJOR, 64, 64, 64, 64, 64, 64,
                                        dga.PATH_SIMT) == 0
 
@@ -147,9 +150,13 @@ def test_general_m_zero_is_a_no_op(lib):
 
 
 def test_general_workspace_size_query(lib):
-    # column-major A on the tensor cores is transposed into the workspace
+    # column-major A on the tensor cores is read in place (MN-major), or
+    # transposed into the workspace when lda is not a multiple of 16 bytes
+    assert dga.dga_gemm_general_workspace_size(gen.BF16, gen.F32, gen.COL_MAJOR, gen.COL_MAJOR,
+                                               256, 512, 1024, 256, 1024, 512,
+                                               dga.PATH_TCGEN05) == 0
     ws = dga.dga_gemm_general_workspace_size(gen.BF16, gen.F32, gen.COL_MAJOR, gen.COL_MAJOR,
-                                             256, 512, 1024, 256, 1024, 512, dga.PATH_TCGEN05)
+                                             256, 512, 1024, 257, 1024, 512, dga.PATH_TCGEN05)
     assert ws >= 256 * 1024 * 2
     assert dga.dga_gemm_general_workspace_size(gen.BF16, gen.F32, gen.ROW_MAJOR, gen.COL_MAJOR,
                                                256, 512, 1024, 1024, 1024, 512,

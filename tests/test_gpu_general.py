@@ -272,3 +272,42 @@ def test_sum_rows_deterministic():
     first = dga.sum_rows(Gd).clone()
     for _ in range(3):
         assert torch.equal(dga.sum_rows(Gd), first)
+
+
+def test_linear_full_size_sampled():
+    """The bf16 fully-connected step at batch 8192, 8192 -> 8192 (the size the
+    benchmark times, through the same calls): sampled rows and columns of Y,
+    dX and dW against the oracle on the matching sub-problems, and every
+    element of db."""
+    dev = torch.device("cuda")
+    b = n_in = n_out = 8192
+    g = torch.Generator(device=dev).manual_seed(11)
+    X = (torch.randn(b, n_in, generator=g, device=dev)).to(torch.bfloat16)
+    W = (torch.randn(n_out, n_in, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    bias = (torch.randn(n_out, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    G = (torch.randn(b, n_out, generator=g, device=dev)).to(torch.bfloat16)
+    Y = dga.linear_forward(X, W, bias)
+    dX, dW, db = dga.linear_backward(X, W, G)
+    torch.cuda.synchronize()
+    pick = torch.Generator().manual_seed(12)
+    rows = torch.cat([torch.tensor([0, 8191]), torch.randint(0, 8192, (14,), generator=pick)])
+    cols = torch.cat([torch.tensor([0, 8191]), torch.randint(0, 8192, (62,), generator=pick)])
+    Xh, Wh, Gh = X.cpu(), W.cpu(), G.cpu()
+    BF = gen.BF16
+    # Y[rows, cols] = X[rows] W[cols]^T + bias[cols]
+    ref, bound = oracle.gemm_fp_ex(BF, BF, gen.ROW_MAJOR, gen.COL_MAJOR, len(rows), len(cols), n_in,
+                                   1.0, Xh[rows], n_in, Wh[cols], n_in, 0.0, None, len(cols),
+                                   bias.cpu()[cols])
+    assert_close(Y.cpu()[rows][:, cols], ref, bound, BF, "Y sampled")
+    # dX[rows, cols] = G[rows] W[:, cols]
+    ref, bound = oracle.gemm_fp_ex(BF, BF, gen.ROW_MAJOR, gen.ROW_MAJOR, len(rows), len(cols),
+                                   n_out, 1.0, Gh[rows], n_out, Wh[:, cols].contiguous(), len(cols),
+                                   0.0)
+    assert_close(dX.cpu()[rows][:, cols], ref, bound, BF, "dX sampled")
+    # dW[rows, cols] = G[:, rows]^T X[:, cols]: A = G[:, rows] stored batch x len(rows)
+    ref, bound = oracle.gemm_fp_ex(BF, BF, gen.COL_MAJOR, gen.ROW_MAJOR, len(rows), len(cols), b,
+                                   1.0, Gh[:, rows].contiguous(), len(rows),
+                                   Xh[:, cols].contiguous(), len(cols), 0.0)
+    assert_close(dW.cpu()[rows][:, cols], ref, bound, BF, "dW sampled")
+    ref, bound = oracle.sum_rows(BF, b, n_out, Gh)
+    assert_close(db.cpu(), ref, bound, gen.F32, "db")

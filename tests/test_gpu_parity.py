@@ -294,7 +294,7 @@ def _sample(M, N, n, seed):
 
 
 @pytest.mark.parametrize("name", ["fp32_4096", "bf16_8192", "skinny_m1", "skinny_m8",
-                                  "skinny_m16", "int8_ragged"])
+                                  "skinny_m16", "int8_ragged", "f16_8192", "bf16_8192_rowb"])
 def test_full_size_workload(name):
     import oracle
     w = gen.WORKLOADS[name]
