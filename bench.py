@@ -509,6 +509,10 @@ def reference_arm(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    if w.kind != "gemm":
+        print(json.dumps({"impl": "reference", "unavailable":
+                          f"the oracle arm times single GEMM workloads; {w.name} is a layer step"}))
+        return 0
     # each step is a bounded sample, sized so the whole run stays within minutes
     per_step_s = max(0.5, min(4.0, 150.0 / (args.steps + args.warmup)))
     sampler = OracleSample(w)
@@ -572,7 +576,7 @@ def main():
     props = torch.cuda.get_device_properties(device)
     peaks = load_peaks(props.multi_processor_count)
 
-    runner = Runner(w, device, sets_for(w), seed=rank)
+    runner = runner_for(w, device, sets_for(w), seed=rank)
     stream = torch.cuda.current_stream()
     s = stream.cuda_stream
     for i in range(args.warmup):
@@ -623,7 +627,8 @@ def main():
             "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
                        "beta": w.beta, "layout_b": "col" if w.layout_b else "row",
-                       "path": dga.PATH_NAMES[dga.dga_last_path()],
+                       "path": (",".join(runner.paths) if w.kind == "fc"
+                                else dga.PATH_NAMES[dga.dga_last_path()]),
                        "l2": f"inputs rotated over {len(runner.sets)} resident sets (> 2x L2 per rotation)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": roof, "gpu_launches": launches,
@@ -631,7 +636,9 @@ def main():
     del runner
     torch.cuda.empty_cache()
 
-    if rank == 0 and world == 1 and not args.no_extras:
+    # (a fully-connected workload as the main one is for profiling: its
+    # extras -- e2e, the oracle sample -- are defined for single GEMMs)
+    if rank == 0 and world == 1 and not args.no_extras and w.kind == "gemm":
         line["e2e"] = e2e_leg(w, max(3, args.steps // 3), 2, device)
         per = {}
         for name in ("bf16_8192", "skinny_m1", "skinny_m8", "skinny_m16", "int8_ragged",
@@ -641,11 +648,18 @@ def main():
             ow = gen.WORKLOADS[name]
             r = runner_for(ow, device, sets_for(ow, 3 if name.startswith("skinny") else 2))
             iters = 200 if name.startswith("skinny") else (10 if ow.kind == "fc" else 30)
+            leg_clocks = ClockSampler(local)
+            leg_clocks.start()
+            time.sleep(0.15)
+            t0 = time.time()
             ms, nl = time_kernel(r, iters, 5 if ow.kind != "fc" else 2)
+            t1 = time.time()
+            leg_clocks.stop()
             rf = roofline_for(ow, ms, peaks)
             rf["traffic"] = traffic_record(source_of(ow), name) if ow.kind == "gemm" else None
             rf["ms_mean"] = ms
             rf["launches_per_call"] = nl / iters
+            rf["clocks"] = leg_clocks.summary(t0 - 0.05, t1 + 0.05)
             if ow.kind == "fc":
                 rf["paths"] = r.paths
                 rf["algorithmic_bytes"] = workload_accounting(ow)[1]

@@ -147,46 +147,7 @@ cudaError_t launch_typed(const Params& p, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// Column sums out[j] = sum_i G(i, j) in fp32: the bias gradient of the
-// fully-connected layer ("AI Programming: Matrix Product", section
-// "Fully-connected layer": the output gradient summed over the batch).  A
-// block covers 32 columns; its 8 warps take every 8th row, and the 8 partial
-// sums are added in a fixed order, so the result does not depend on timing.
-template <typename TIn>
-__global__ void __launch_bounds__(256) sum_rows_kernel(const TIn* __restrict__ G, int64_t rows,
-                                                       int64_t cols, int64_t ldg,
-                                                       float* __restrict__ out) {
-    __shared__ float part[8][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int64_t j = static_cast<int64_t>(blockIdx.x) * 32 + tx;
-    float s = 0.0f;
-    if (j < cols)
-        for (int64_t i = ty; i < rows; i += 8) s += static_cast<float>(InT<TIn>::get(G + i * ldg + j));
-    part[ty][tx] = s;
-    __syncthreads();
-    if (ty == 0 && j < cols) {
-        float t = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) t += part[q][tx];
-        out[j] = t;
-    }
-}
-
 }  // namespace
-
-cudaError_t sum_rows_launch(int dtype, int64_t rows, int64_t cols, const void* G, int64_t ldg,
-                            float* out, cudaStream_t stream) {
-    const int64_t blocks = (cols + 31) / 32;
-    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
-    const dim3 grid(static_cast<unsigned>(blocks));
-    if (dtype == DGA_F32)
-        sum_rows_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float*>(G), rows, cols, ldg, out);
-    else if (dtype == DGA_BF16)
-        sum_rows_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(G), rows, cols, ldg, out);
-    else
-        sum_rows_kernel<__half><<<grid, 256, 0, stream>>>(static_cast<const __half*>(G), rows, cols, ldg, out);
-    return cudaGetLastError();
-}
 
 bool generic_supports(const GemmArgs& a) {
     // grid.y limit: 65535 tiles of 32 rows

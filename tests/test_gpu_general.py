@@ -252,10 +252,15 @@ def test_linear_forward_backward(batch, n_in, n_out, dtype):
 # ------------------------------------------------------------- sum_rows --
 
 @pytest.mark.parametrize("dtype", [gen.F32, gen.BF16, gen.F16])
-@pytest.mark.parametrize("rows,cols", [(1, 1), (0, 40), (7, 33), (1000, 4099), (8192, 64)])
-def test_sum_rows(dtype, rows, cols):
+@pytest.mark.parametrize("rows,cols", [(1, 1), (0, 40), (7, 33), (1000, 4099), (8192, 64),
+                                       (4097, 520)])
+@pytest.mark.parametrize("aligned_ld", [False, True])
+def test_sum_rows(dtype, rows, cols, aligned_ld):
+    # aligned_ld: rows start on 16-byte boundaries (whole 16-byte loads, with
+    # element-wise loads only for the ragged last columns); else every load
+    # is element-wise
     g = torch.Generator().manual_seed(rows * 7 + cols)
-    ldg = cols + 5
+    ldg = (cols + 7) // 8 * 8 if aligned_ld else cols + 5
     Gh = gen.random_matrix((max(rows, 1), ldg), dtype, g)
     out = torch.full((cols,), float("nan"), device="cuda")
     st = dga.dga_sum_rows(dtype, rows, cols, Gh.cuda().data_ptr(), ldg, out.data_ptr(),
