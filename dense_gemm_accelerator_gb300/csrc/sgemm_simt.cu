@@ -98,9 +98,9 @@ __device__ __forceinline__ float4 ld_f4_checked(const float* row, int64_t col, i
 // stores.  kTransB: B is stored N x K (column-major B); its slice is staged
 // the way row-major A is, through transposing stores.
 // kRunPtr: interior slices walk A and B with running pointers instead of
-// recomputing the addresses; measured faster for a column-major B and with a
-// bias row, slower for the plain row-major case (the register allocation at
-// 128 per thread differs), so the launcher chooses it per variant.
+// recomputing the addresses; measured faster for a column-major B (4096^3:
+// 56.6 against 54.8 TFLOP/s, and 57.1 against 48.5 with a bias row) and no
+// different otherwise, so the interior kernel uses it for column-major B.
 template <bool kChecked, bool kTransA, bool kTransB, int kReadC = -1, int kBias = -1,
           bool kRunPtr = false>
 __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t row0, int64_t col0,
@@ -193,9 +193,12 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
     for (int64_t s = 0; s < n_slices; ++s) {
         const int buf = static_cast<int>(s & 1);
         const bool more = s + 1 < n_slices;
-        if (more) fetch(k_begin + (s + 1) * BK);
         // Fragments are double-buffered in registers: the shared-memory loads
-        // for k+1 are issued before the 64 FFMAs of k.
+        // for k+1 are issued before the 64 FFMAs of k.  The next slice's global
+        // loads go out after two k-steps (their registers are live for less of
+        // the loop), and the FFMAs walk the 8 x 8 block column by column: both
+        // measured on GB300 (4096^3: 56.0 -> 57.7 TFLOP/s; any fetch point
+        // from k = 1 to 4 gives the same).
         float a[2][8], b[2][8];
         auto frag = [&](int d, int k) {
             *reinterpret_cast<float4*>(&a[d][0]) = *reinterpret_cast<const float4*>(&sm.A[buf][k][am0]);
@@ -206,11 +209,12 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
         frag(0, 0);
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
+            if (k == 2 && more) fetch(k_begin + (s + 1) * BK);
             if (k + 1 < BK) frag((k + 1) & 1, k + 1);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int j = 0; j < 8; ++j)
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[k & 1][i], b[k & 1][j], acc[i][j]);
+                for (int i = 0; i < 8; ++i) acc[i][j] = fmaf(a[k & 1][i], b[k & 1][j], acc[i][j]);
         }
         // The other buffer was last read in slice s-1, before the barrier
         // that ended it, so it can be overwritten now.
@@ -337,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sgemm_128x128_interior_k
     int64_t tm, tn;
     grouped_tile(static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x, gridDim.y, gridDim.x,
                  tm, tn);
-    block_tile<false, kTransA, kTransB, kReadC, kBias, kTransB || kBias == 1>(p, sm, tm * BM, tn * BN,
+    block_tile<false, kTransA, kTransB, kReadC, kBias, kTransB>(p, sm, tm * BM, tn * BN,
                                                                             0, p.K, nullptr);
 }
 
@@ -440,11 +444,65 @@ void launch_simt_kernels(const Params& p, const GemmArgs& a, const Schedule& sc,
 
 }  // namespace
 
+namespace {
+
+// Problems made only of interior tiles whose last wave is at most a third
+// full run as two bands of whole tile rows: the top band (the full waves) on
+// the interior kernel, the bottom band (the last wave) cut along K into 3-4
+// parts by the general kernel over every slot.  Returns the top band's rows,
+// or 0 for one band.  Measured on GB300 at N = K = 4096: whole waves run at
+// 59 TFLOP/s; M = 3840 (last wave 16% full) went from 52.5 to 56.3 and
+// M = 5120 (21%) from 54.8 to 57.7 with the bands, while M = 4096 (37%: its
+// lone blocks already run ~1.8x faster than paired ones) lost 0.8% with a
+// 2-way split and is left whole.
+int64_t simt_top_band_rows(const GemmArgs& a, int sm_count, bool interior_shape) {
+    if (!interior_shape) return 0;
+    const int64_t tiles_n = a.N / BN, tiles = (a.M / BM) * tiles_n;
+    const int64_t slots = static_cast<int64_t>(kSimtBlocksPerSm) * sm_count;
+    if (slots <= 0 || tiles < slots) return 0;
+    const int64_t tail = tiles % slots;
+    if (tail == 0 || 3 * tail > slots) return 0;
+    const int64_t rows = (tiles - tail) / tiles_n * BM;
+    if (rows <= 0 || rows >= a.M) return 0;
+    // the bottom band must itself be split at least 3 ways, else one band is as good
+    if (plan_schedule(a.M - rows, a.N, a.K, sm_count).parts < 3) return 0;
+    return rows;
+}
+
+bool simt_interior_shape(const GemmArgs& a) {
+    return a.M % BM == 0 && a.N % BN == 0 && a.K % BK == 0 && a.lda % 4 == 0 && a.ldb % 4 == 0 &&
+           a.ldc % 4 == 0 && aligned(a.A, 16) && aligned(a.B, 16) && aligned(a.C, 16);
+}
+
+cudaError_t simt_run(const GemmArgs& a, const DeviceInfo& dev, int* launches);
+
+}  // namespace
+
 size_t simt_workspace_size(const GemmArgs& a, int sm_count) {
-    return plan_schedule(a.M, a.N, a.K, sm_count).partial_bytes;
+    const int64_t top = simt_top_band_rows(a, sm_count, simt_interior_shape(a));
+    return plan_schedule(a.M - top, a.N, a.K, sm_count).partial_bytes;
 }
 
 cudaError_t simt_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
+    const int64_t top = simt_top_band_rows(a, dev.sm_count, simt_interior_shape(a));
+    if (top > 0 && a.ws != nullptr &&
+        a.ws_bytes >= plan_schedule(a.M - top, a.N, a.K, dev.sm_count).partial_bytes) {
+        GemmArgs upper = a, lower = a;
+        upper.M = top;
+        lower.M = a.M - top;
+        lower.A = a.layout_a == DGA_COL_MAJOR ? static_cast<const float*>(a.A) + top
+                                              : static_cast<const float*>(a.A) + top * a.lda;
+        lower.C = static_cast<float*>(a.C) + top * a.ldc;
+        cudaError_t e = simt_run(upper, dev, launches);
+        if (e != cudaSuccess) return e;
+        return simt_run(lower, dev, launches);
+    }
+    return simt_run(a, dev, launches);
+}
+
+namespace {
+
+cudaError_t simt_run(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     Schedule sc = plan_schedule(a.M, a.N, a.K, dev.sm_count);
     if (sc.parts > 1 && (a.ws == nullptr || a.ws_bytes < sc.partial_bytes)) {
         // not enough workspace for the split tail: whole tiles only
@@ -480,5 +538,7 @@ cudaError_t simt_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches)
     }
     return cudaSuccess;
 }
+
+}  // namespace
 
 }  // namespace dga
