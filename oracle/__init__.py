@@ -11,9 +11,11 @@ Product" (elainafan.one), section "Dense matrix multiplication", following
 the CPU triple loop of its section "Row-major order".  Beside ``ref`` it
 returns the per-element error bound
 
-    bound = 1e-4 * sum_k |alpha * a_ik * b_kj| + |beta * c_ij| * 2**-22
+    bound = rel * sum_k |alpha * a_ik * b_kj| + |beta * c_ij| * 2**-22
 
-(plus ``ulp_bf16(ref)`` for bf16 output, via :func:`ulp_bf16`).
+with rel = 1e-4, or 2**-9 + 2**-20 + 1e-4 for TF32 inputs (fp32 operands
+whose products the tensor cores form at 10 fraction bits), plus
+``ulp_bf16(ref)`` for bf16 output, via :func:`ulp_bf16`.
 
 Every function is pinned by ``tests/test_oracle.py`` against facts that do not
 come from this code: identity and permutation matrices, alpha/beta semantics,
@@ -29,7 +31,7 @@ import threading
 
 import numpy as np
 
-F32, BF16, F16, I8, I32 = 0, 1, 2, 3, 4
+F32, BF16, F16, I8, I32, TF32 = 0, 1, 2, 3, 4, 5
 ROW_MAJOR, COL_MAJOR = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -63,7 +65,7 @@ def build_variant(src_path: str, out_path: str, defines=()) -> "Oracle":
     return Oracle(out_path)
 
 
-_FP_NP = {F32: np.float32, BF16: np.uint16, F16: np.uint16}
+_FP_NP = {F32: np.float32, BF16: np.uint16, F16: np.uint16, TF32: np.float32}
 
 
 def _buf(arr, dtype, name):

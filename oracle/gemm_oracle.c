@@ -38,8 +38,20 @@
  * the OpenMP thread count.
  *
  * Error bound returned beside ref (fp64):
- *   bound(i,j) = 1e-4 * sum_k |alpha*a(i,k)*b(k,j)| + |beta*c(i,j)| * 2^-22
- * The bf16-output ulp term is a separate function (oracle_ulp_bf16).
+ *   bound(i,j) = rel * sum_k |alpha*a(i,k)*b(k,j)| + (|beta*c(i,j)| + |bias(j)|) * 2^-22
+ * with rel = 1e-4.  The bf16-output ulp term is a separate function
+ * (oracle_ulp_bf16).
+ *
+ * TF32 inputs (in_dtype OR_TF32): the operands are stored as fp32 and ref is
+ * the same exact definition as for OR_F32.  "Matrix multiplication:
+ * arithmetic intensity, tiling and Tensor Core" (dilfish.github.io),
+ * sections 5.5 and 5.7, lists TF32 beside FP32 and says it keeps fewer
+ * mantissa bits (10 instead of 23), so it is lossy; it does not say how an
+ * fp32 value is reduced to TF32.  Reading: each operand may be replaced by a
+ * value with 10 fraction bits, by truncation or by rounding, which changes
+ * it by less than 2^-10 of its magnitude (normal numbers); a product then
+ * changes by less than (1 + 2^-10)^2 - 1 = 2^-9 + 2^-20 of its magnitude.
+ * rel is widened by that much: rel = 2^-9 + 2^-20 + 1e-4.
  *
  * Parity pins: every function here is pinned by tests/test_oracle.py
  * (identity, permutation, alpha/beta semantics, exact small integers against
@@ -57,7 +69,7 @@ static int64_t g_mac_count = 0;
 #define COUNT_MAC() ((void)0)
 #endif
 
-enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2, OR_I8 = 3, OR_I32 = 4 };
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2, OR_I8 = 3, OR_I32 = 4, OR_TF32 = 5 };
 enum { OR_ROW_MAJOR = 0, OR_COL_MAJOR = 1 };
 
 /* ---- exact decoding of stored elements ---------------------------------- */
@@ -88,7 +100,8 @@ static double decode_f16(uint16_t h) {
 
 static double load_fp(int dtype, const void* p, int64_t idx) {
     switch (dtype) {
-    case OR_F32: return (double)((const float*)p)[idx];
+    case OR_F32:
+    case OR_TF32: return (double)((const float*)p)[idx];  /* TF32 operands are stored as fp32 */
     case OR_BF16: return decode_bf16(((const uint16_t*)p)[idx]);
     case OR_F16: return decode_f16(((const uint16_t*)p)[idx]);
     default: return NAN;
@@ -122,8 +135,10 @@ static void fp_element(int in_dtype, int out_dtype, int layout_a, int layout_b, 
     double cterm = 0.0;
     if (beta != 0.0) cterm = beta * load_fp(out_dtype, C, i * ldc + j);
     double bterm = bias ? load_fp(out_dtype, bias, j) : 0.0;
+    /* relative term: fp32 accumulation (1e-4), plus TF32 operand reduction */
+    const double rel = in_dtype == OR_TF32 ? ldexp(1.0, -9) + ldexp(1.0, -20) + 1e-4 : 1e-4;
     *ref = alpha * sum + cterm + bterm;
-    *bound = 1e-4 * fabs(alpha) * abs_sum + (fabs(cterm) + fabs(bterm)) * ldexp(1.0, -22);
+    *bound = rel * fabs(alpha) * abs_sum + (fabs(cterm) + fabs(bterm)) * ldexp(1.0, -22);
 }
 
 /* ---- one output element, INT8 x INT8 -> INT32 ---------------------------- */
@@ -159,7 +174,8 @@ int oracle_gemm_fp_ex(int in_dtype, int out_dtype, int layout_a, int layout_b, i
                       int64_t N, int64_t K, double alpha, const void* A, int64_t lda,
                       const void* B, int64_t ldb, double beta, const void* C, int64_t ldc,
                       const void* bias, double* ref, double* bound) {
-    if (in_dtype != OR_F32 && in_dtype != OR_BF16 && in_dtype != OR_F16) return -1;
+    if (in_dtype != OR_F32 && in_dtype != OR_BF16 && in_dtype != OR_F16 && in_dtype != OR_TF32)
+        return -1;
     if (out_dtype != OR_F32 && out_dtype != OR_BF16 && out_dtype != OR_F16) return -1;
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < M; ++i)
@@ -185,7 +201,8 @@ int oracle_gemm_fp_sampled(int in_dtype, int out_dtype, int layout_b, int64_t K,
                            const void* C, int64_t ldc, int64_t n_samples,
                            const int64_t* rows, const int64_t* cols,
                            double* ref, double* bound) {
-    if (in_dtype != OR_F32 && in_dtype != OR_BF16 && in_dtype != OR_F16) return -1;
+    if (in_dtype != OR_F32 && in_dtype != OR_BF16 && in_dtype != OR_F16 && in_dtype != OR_TF32)
+        return -1;
     if (out_dtype != OR_F32 && out_dtype != OR_BF16 && out_dtype != OR_F16) return -1;
 #pragma omp parallel for schedule(dynamic, 64)
     for (int64_t s = 0; s < n_samples; ++s)

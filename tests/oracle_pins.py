@@ -12,7 +12,10 @@ disagrees with what the mathematics or the pages fix:
   summation error bound, and the error-bound formula itself;
 * INT8 against Python integers, including wrap-around mod 2**32;
 * the MAC count M*N*K (2MNK FLOPs) of the instrumented build;
-* bf16 decoding and IEEE round-to-nearest-even encoding.
+* bf16 decoding and IEEE round-to-nearest-even encoding;
+* TF32 inputs: the same exact result as FP32, and a bound that covers the
+  result of operands cut to 10 fraction bits, by truncation or by rounding
+  (computed here from the binary32 encoding, in exact rationals).
 
 The GEMM definition pinned here is BLAS's C <- alpha*A*B + beta*C, "AI
 Programming: Matrix Product" (elainafan.one), section "Dense matrix
@@ -27,7 +30,7 @@ from fractions import Fraction
 import numpy as np
 import torch
 
-F32, BF16, F16, I8, I32 = 0, 1, 2, 3, 4
+F32, BF16, F16, I8, I32, TF32 = 0, 1, 2, 3, 4, 5
 ROW, COL = 0, 1
 
 
@@ -396,6 +399,76 @@ def pin_sum_rows(o):
     assert np.array_equal(got_b, got)
 
 
+# -------------------------------------------------------------------- TF32 --
+#
+# "Matrix multiplication: arithmetic intensity, tiling and Tensor Core",
+# sections 5.5 and 5.7: TF32 keeps the fp32 exponent but only 10 mantissa
+# bits, so it is lossy.  How an fp32 value becomes TF32 is not stated; the
+# two plain readings, truncation and round-to-nearest-even, are both built
+# here from the binary32 encoding (sign, 8-bit exponent, 23-bit fraction).
+
+def _tf32_value(x, mode):
+    """Exact value of the fp32 number x with its fraction cut to 10 bits."""
+    bits = int(np.array([x], np.float32).view(np.uint32)[0])
+    sign = -1 if bits >> 31 else 1
+    e = (bits >> 23) & 0xFF
+    frac = bits & 0x7FFFFF
+    assert 0 < e < 0xFF, "normal numbers only"
+    keep, rem = frac >> 13, frac & 0x1FFF
+    if mode == "nearest" and (rem > 0x1000 or (rem == 0x1000 and keep & 1)):
+        keep += 1   # may carry into the exponent: (1 + 1024/1024) = 2, still exact
+    return sign * (1 + Fraction(keep, 1024)) * Fraction(2) ** (e - 127)
+
+
+def pin_tf32(o):
+    g = _rng(12)
+    # (a) the reference is the exact product of the stored fp32 operands:
+    #     the same as for FP32 inputs, for both layouts, with beta and a bias
+    M, N, K = 9, 7, 21
+    A = _f32((M, K), g)
+    for layout in (ROW, COL):
+        B = _f32((N, K) if layout == COL else (K, N), g)
+        C = _f32((M, N), g)
+        bias = _f32((N,), g)
+        ldb = K if layout == COL else N
+        r32, b32 = o.gemm_fp_ex(F32, F32, ROW, layout, M, N, K, 1.25, A, K, B, ldb, -0.5, C, N,
+                                bias=bias)
+        rtf, btf = o.gemm_fp_ex(TF32, F32, ROW, layout, M, N, K, 1.25, A, K, B, ldb, -0.5, C, N,
+                                bias=bias)
+        assert np.array_equal(r32, rtf), ("tf32 ref", layout)
+        assert (btf > b32).all(), "tf32 bound wider than fp32"
+    # (b) the bound covers both readings of the TF32 reduction
+    rnd = random.Random(13)
+    for trial in range(40):
+        M, N, K = rnd.randint(1, 6), rnd.randint(1, 6), rnd.randint(1, 9)
+        def val():
+            return np.float32(rnd.uniform(0.5, 1.0) * rnd.choice((-1, 1)) * 2.0 ** rnd.randint(-30, 30))
+        A = np.array([[val() for _ in range(K)] for _ in range(M)], np.float32)
+        B = np.array([[val() for _ in range(N)] for _ in range(K)], np.float32)
+        C = np.array([[val() for _ in range(N)] for _ in range(M)], np.float32)
+        alpha = float(np.float32(rnd.uniform(-2, 2)))
+        beta = rnd.choice((0.0, float(np.float32(rnd.uniform(-2, 2)))))
+        ref, bound = o.gemm_fp(TF32, F32, ROW, M, N, K, alpha, A, K, B, N, beta, C, N)
+        for mode in ("trunc", "nearest"):
+            for i in range(M):
+                for j in range(N):
+                    s = sum((_tf32_value(A[i, k], mode) * _tf32_value(B[k, j], mode)
+                             for k in range(K)), Fraction(0))
+                    cterm = Fraction(beta) * Fraction(float(C[i, j])) if beta != 0 else 0
+                    exact = Fraction(alpha) * s + cterm
+                    assert abs(exact - Fraction(float(ref[i, j]))) <= Fraction(float(bound[i, j])), \
+                        (trial, mode, i, j)
+    # (c) the widening is needed, and not much more than needed: with both
+    #     operands just below 1 + 2^-10, truncation loses almost 2^-9 of the
+    #     product
+    a = np.float32(1.0 + 2.0**-10 - 2.0**-23)
+    Ak = np.array([[a]], np.float32)
+    ref, bound = o.gemm_fp(TF32, F32, ROW, 1, 1, 1, 1.0, Ak, 1, Ak, 1, 0.0)
+    lost = Fraction(float(ref[0, 0])) - _tf32_value(a, "trunc") ** 2
+    assert lost > Fraction(2) ** -9 * Fraction(99, 100)
+    assert lost <= Fraction(float(bound[0, 0])) < 2 * lost
+
+
 ALL_PINS = [pin_identity, pin_permutation, pin_alpha_beta, pin_small_integers, pin_int8,
             pin_tiny_rational, pin_bf16_decode, pin_f16_decode, pin_bf16_round, pin_ulp_bf16,
-            pin_transposed_a, pin_bias, pin_sum_rows]
+            pin_transposed_a, pin_bias, pin_sum_rows, pin_tf32]

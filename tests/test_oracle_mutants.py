@@ -30,13 +30,18 @@ MUTANTS = [
     ("bf16_decode_shift", "((uint32_t)h) << 16", "((uint32_t)h) << 15", 0),
     ("round_ties_away", "nearbyint(scaled)", "round(scaled)", 0),
     ("i8_beta_dropped", "if (beta != 0) r +=", "if (0) r +=", 0),
-    ("bound_without_alpha", "1e-4 * fabs(alpha) * abs_sum", "1e-4 * abs_sum", 0),
+    ("bound_without_alpha", "rel * fabs(alpha) * abs_sum", "rel * abs_sum", 0),
     ("ulp_one_bit_off", "ldexp(1.0, exp2 - 7)", "ldexp(1.0, exp2 - 8)", 0),
     ("f16_bias", "e - 25);", "e - 24);", 0),
     ("beta_zero_reads_c", "if (beta != 0.0) cterm", "if (1) cterm", 0),
     ("alpha_zero_reads_ab", "if (alpha != 0.0) {", "if (1) {", 0),
     ("lda_ignored", "a_index(layout_a, i, k, lda)", "a_index(layout_a, i, k, K)", 0),
     ("i8_lda_ignored", "a_index(layout_a, i, k, lda)", "a_index(layout_a, i, k, K)", 1),
+    ("tf32_term_dropped", "in_dtype == OR_TF32 ? ldexp(1.0, -9) + ldexp(1.0, -20) + 1e-4 : 1e-4",
+     "1e-4", 0),
+    ("tf32_read_as_16_bit", "    case OR_F32:\n    case OR_TF32: return (double)((const float*)p)[idx];",
+     "    case OR_F32: return (double)((const float*)p)[idx];\n"
+     "    case OR_TF32: return decode_bf16(((const uint16_t*)p)[idx]);", 0),
 ]
 
 
