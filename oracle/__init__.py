@@ -17,6 +17,11 @@ with rel = 1e-4, or 2**-9 + 2**-20 + 1e-4 for TF32 inputs (fp32 operands
 whose products the tensor cores form at 10 fraction bits), plus
 ``ulp_bf16(ref)`` for bf16 output, via :func:`ulp_bf16`.
 
+It also holds the CSR sparse matrix-vector product of the same page
+(sections "CSR" and "SpMV"): ``spmv_csr`` returns ``alpha * A @ x + beta * y``
+row by row in fp64 and the bound ``1e-4 * |alpha| * sum |a_ip x_p| +
+|beta * y_i| * 2**-22``.
+
 Every function is pinned by ``tests/test_oracle.py`` against facts that do not
 come from this code: identity and permutation matrices, alpha/beta semantics,
 exact Python-integer and rational arithmetic on small cases, the MAC count
@@ -120,6 +125,7 @@ class Oracle:
         lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
         lib.oracle_decode_f16.restype = f64
         lib.oracle_mac_count.restype = i64
+        lib.oracle_spmv_csr.argtypes = [i64, i64, vp, vp, vp, f64, vp, f64, vp, vp, vp]
         lib.oracle_round_bf16_array.argtypes = [vp, vp, i64]
         lib.oracle_ulp_bf16_array.argtypes = [vp, vp, i64]
         self.lib = lib
@@ -227,6 +233,28 @@ class Oracle:
                                         _ptr(cols), _ptr(out))
         return out
 
+    def spmv_csr(self, rows, cols, row_offsets, column_indices, values, x, alpha=1.0, beta=0.0,
+                 y=None):
+        """(ref, bound): alpha * A @ x + beta * y for the CSR matrix A
+        (int32 row_offsets of rows + 1 entries, int32 column_indices and fp32
+        values of nnz entries), both (rows,) fp64."""
+        ro = _buf(row_offsets, np.int32, "row_offsets")
+        ci = _buf(column_indices, np.int32, "column_indices")
+        va = _buf(values, np.float32, "values")
+        xx = _buf(x, np.float32, "x")
+        yy = None if y is None else _buf(y, np.float32, "y")
+        if yy is None and beta != 0:
+            raise ValueError("beta != 0 needs y")
+        if ro.size != rows + 1:
+            raise ValueError("row_offsets must have rows + 1 entries")
+        ref = np.empty(rows, np.float64)
+        bound = np.empty(rows, np.float64)
+        rc = self.lib.oracle_spmv_csr(rows, cols, _ptr(ro), _ptr(ci), _ptr(va), float(alpha),
+                                      _ptr(xx), float(beta), _ptr(yy), _ptr(ref), _ptr(bound))
+        if rc != 0:
+            raise ValueError("oracle_spmv_csr: not a CSR matrix of the given shape")
+        return ref, bound
+
     def round_bf16(self, x) -> np.ndarray:
         """Nearest-even bf16 encodings (uint16) of the fp64 values x."""
         flat = np.ascontiguousarray(np.asarray(x, np.float64).ravel())
@@ -296,6 +324,10 @@ def gemm_i8_ex(*args, **kw):
 
 def sum_rows(*args, **kw):
     return default().sum_rows(*args, **kw)
+
+
+def spmv_csr(*args, **kw):
+    return default().spmv_csr(*args, **kw)
 
 
 def round_bf16(x):

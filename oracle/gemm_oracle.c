@@ -53,6 +53,8 @@
  * changes by less than (1 + 2^-10)^2 - 1 = 2^-9 + 2^-20 of its magnitude.
  * rel is widened by that much: rel = 2^-9 + 2^-20 + 1e-4.
  *
+ * CSR sparse matrix-vector product (oracle_spmv_csr): see its comment.
+ *
  * Parity pins: every function here is pinned by tests/test_oracle.py
  * (identity, permutation, alpha/beta semantics, exact small integers against
  * Python integers, tiny shapes against exact rationals, MAC count = M*N*K,
@@ -261,6 +263,47 @@ int oracle_sum_rows(int dtype, int64_t rows, int64_t cols, const void* G, int64_
         }
         out[j] = s;
         bound[j] = 1e-4 * a;
+    }
+    return 0;
+}
+
+/* ---- CSR sparse matrix-vector product ------------------------------------ */
+
+/* y <- alpha * A * x + beta * y for A in CSR form: the SpMV of "AI
+ * Programming: Matrix Product", sections "CSR" and "SpMV".  Row i holds the
+ * nonzeros p in the half-open interval [row_offsets[i], row_offsets[i+1]),
+ * each with its value values[p] in column column_indices[p]; the row's
+ * result is the sum of values[p] * x[column_indices[p]] over those p.  The
+ * page gives y = A x; the scaling by alpha and beta is the same BLAS-style
+ * update as the GEMM above (beta == 0: y is not read; alpha == 0: A and x
+ * are not read).  fp64 accumulation in ascending p.  Beside ref,
+ *   bound[i] = 1e-4 * |alpha| * sum_p |values[p] * x[col]| + |beta * y[i]| * 2^-22.
+ * Returns -1 when the arrays are not a CSR matrix of rows x cols
+ * (row_offsets[0] != 0, decreasing offsets, or a column index outside
+ * [0, cols)), else 0. */
+int oracle_spmv_csr(int64_t rows, int64_t cols, const int32_t* row_offsets,
+                    const int32_t* column_indices, const float* values, double alpha,
+                    const float* x, double beta, const float* y, double* ref, double* bound) {
+    if (rows > 0 && row_offsets[0] != 0) return -1;
+    for (int64_t i = 0; i < rows; ++i) {
+        if (row_offsets[i + 1] < row_offsets[i]) return -1;
+        for (int64_t p = row_offsets[i]; p < row_offsets[i + 1]; ++p)
+            if (column_indices[p] < 0 || column_indices[p] >= cols) return -1;
+    }
+#pragma omp parallel for schedule(dynamic, 256)
+    for (int64_t i = 0; i < rows; ++i) {
+        double sum = 0.0, abs_sum = 0.0;
+        if (alpha != 0.0) {
+            for (int64_t p = row_offsets[i]; p < row_offsets[i + 1]; ++p) {
+                double prod = (double)values[p] * (double)x[column_indices[p]];  /* exact */
+                sum += prod;
+                abs_sum += fabs(prod);
+                COUNT_MAC();
+            }
+        }
+        double yterm = beta != 0.0 ? beta * (double)y[i] : 0.0;
+        ref[i] = alpha * sum + yterm;
+        bound[i] = 1e-4 * fabs(alpha) * abs_sum + fabs(yterm) * ldexp(1.0, -22);
     }
     return 0;
 }

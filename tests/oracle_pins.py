@@ -13,6 +13,10 @@ disagrees with what the mathematics or the pages fix:
 * INT8 against Python integers, including wrap-around mod 2**32;
 * the MAC count M*N*K (2MNK FLOPs) of the instrumented build;
 * bf16 decoding and IEEE round-to-nearest-even encoding;
+* CSR SpMV: the page's worked 3 x 4 example, dense products of COO
+  triplets in Python integers and exact rationals (empty rows, a long row,
+  repeated columns), identity and permutation matrices, alpha/beta
+  semantics, and rejection of arrays that are not a CSR matrix;
 * TF32 inputs: the same exact result as FP32, and a bound that covers the
   result of operands cut to 10 fraction bits, by truncation or by rounding
   (computed here from the binary32 encoding, in exact rationals).
@@ -24,6 +28,8 @@ order".
 """
 from __future__ import annotations
 
+import json
+import os
 import random
 from fractions import Fraction
 
@@ -265,6 +271,12 @@ def pin_mac_count(o_counting):
     o_counting.gemm_fp(F32, F32, ROW, 4, 4, 4, 0.0, np.zeros((4, 4), np.float32), 4,
                        np.zeros((4, 4), np.float32), 4, 0.0)
     assert o_counting.mac_count() == 0, "alpha=0 must not multiply"
+    # CSR SpMV: one multiply per stored nonzero (empty rows cost nothing)
+    offs = np.array([0, 3, 3, 7, 8], np.int32)
+    cols = np.array([0, 1, 2, 0, 0, 3, 1, 2], np.int32)
+    o_counting.reset_mac_count()
+    o_counting.spmv_csr(4, 4, offs, cols, np.ones(8, np.float32), np.ones(4, np.float32))
+    assert o_counting.mac_count() == 8, "SpMV MACs = nnz"
 
 
 # ------------------------------------------------------------------- bf16 --
@@ -469,6 +481,143 @@ def pin_tf32(o):
     assert lost <= Fraction(float(bound[0, 0])) < 2 * lost
 
 
+# --------------------------------------------------------------- CSR SpMV --
+#
+# "AI Programming: Matrix Product", sections "COO", "CSR" and "SpMV": a CSR
+# matrix keeps values and column indices of the nonzeros row after row, and
+# row_offsets[i] .. row_offsets[i+1] is row i's half-open range; SpMV
+# multiplies every nonzero by the vector element of its column and sums the
+# products of each row.  The checks build the same matrix independently, as
+# COO triplets (row, column, value), and compute the dense product from them.
+
+def _csr_from_triplets(n_rows, triplets):
+    """CSR arrays from (row, col, value) triplets by the page's recipe: a
+    histogram of row indices, a prefix sum into row_offsets, then a scatter
+    (keeping the triplets' order within a row)."""
+    counts = [0] * n_rows
+    for r, _, _ in triplets:
+        counts[r] += 1
+    offs = [0]
+    for c in counts:
+        offs.append(offs[-1] + c)
+    fill = offs[:-1].copy()
+    cols = [0] * len(triplets)
+    vals = [0.0] * len(triplets)
+    for r, c, v in triplets:
+        cols[fill[r]] = c
+        vals[fill[r]] = v
+        fill[r] += 1
+    return (np.array(offs, np.int32), np.array(cols, np.int32), np.array(vals, np.float32))
+
+
+def _dense_spmv(n_rows, triplets, x, alpha, beta, y):
+    """alpha * A x + beta * y, exactly, with A summed from the triplets."""
+    out = []
+    for i in range(n_rows):
+        s = sum((Fraction(float(np.float32(v))) * Fraction(float(x[c]))
+                 for r, c, v in triplets if r == i), Fraction(0))
+        t = Fraction(alpha) * s
+        if beta != 0:
+            t += Fraction(beta) * Fraction(float(y[i]))
+        out.append(t)
+    return out
+
+
+def pin_spmv(o):
+    # (a) the page's example, its COO and CSR forms taken from the golden file
+    here = os.path.dirname(os.path.abspath(__file__))
+    with open(os.path.join(here, "golden", "csr_example.json")) as f:
+        ex = json.load(f)
+    m, n = ex["shape"]
+    coo = ex["coo"]
+    trip = list(zip(coo["rows"], coo["cols"], coo["values"]))
+    csr = ex["csr"]
+    for x in ([1, 2, 3, 4], [-1, 0.5, 2, -3]):
+        xs = np.array(x, np.float32)
+        ref, _ = o.spmv_csr(m, n, np.array(csr["row_offsets"], np.int32),
+                            np.array(csr["column_indices"], np.int32),
+                            np.array(csr["values"], np.float32), xs)
+        assert [Fraction(float(v)) for v in ref] == _dense_spmv(m, trip, xs, 1, 0, None), x
+    # (b) integer values: exact, with empty rows, one long row and a column
+    #     repeated within a row (the repeats add up, as in the dense matrix)
+    rnd = random.Random(14)
+    for trial in range(6):
+        n_rows, n_cols = rnd.randint(1, 40), rnd.randint(1, 30)
+        trip = []
+        for i in range(n_rows):
+            length = rnd.choice((0, 0, 1, 2, 3, 5, 8))
+            if i == n_rows // 2:
+                length = 300
+            for _ in range(length):
+                trip.append((i, rnd.randrange(n_cols), float(rnd.randint(-9, 9))))
+        if trip:
+            r, c, _ = trip[0]
+            trip.append((r, c, 4.0))          # a repeated (row, column) pair
+        trip.sort(key=lambda t: t[0])
+        offs, cols, vals = _csr_from_triplets(n_rows, trip)
+        x = np.array([rnd.randint(-7, 7) for _ in range(n_cols)], np.float32)
+        y = np.array([rnd.randint(-5, 5) for _ in range(n_rows)], np.float32)
+        for alpha, beta in ((1.0, 0.0), (3.0, -2.0), (0.0, 1.5)):
+            ref, _ = o.spmv_csr(n_rows, n_cols, offs, cols, vals, x, alpha, beta, y)
+            want = _dense_spmv(n_rows, trip, x, alpha, beta, y)
+            assert [Fraction(float(v)) for v in ref] == want, (trial, alpha, beta)
+    # (c) fp32 values with spread exponents: within the fp64 summation bound,
+    #     and the returned bound is the documented one
+    u = Fraction(1, 2**53)
+    for trial in range(10):
+        n_rows, n_cols = rnd.randint(1, 12), rnd.randint(1, 12)
+        trip = [(rnd.randrange(n_rows), rnd.randrange(n_cols),
+                 float(np.float32(rnd.uniform(-1, 1) * 2.0 ** rnd.randint(-20, 20))))
+                for _ in range(rnd.randint(0, 40))]
+        trip.sort(key=lambda t: t[0])
+        offs, cols, vals = _csr_from_triplets(n_rows, trip)
+        x = np.array([rnd.uniform(-1, 1) * 2.0 ** rnd.randint(-10, 10) for _ in range(n_cols)],
+                     np.float32)
+        y = np.array([rnd.uniform(-1, 1) for _ in range(n_rows)], np.float32)
+        ref, bound = o.spmv_csr(n_rows, n_cols, offs, cols, vals, x, 0.75, 0.5, y)
+        want = _dense_spmv(n_rows, trip, x, 0.75, 0.5, y)
+        for i in range(n_rows):
+            terms = [Fraction(float(np.float32(v))) * Fraction(float(x[c])) for r, c, v in trip if r == i]
+            mag = Fraction(3, 4) * sum((abs(t) for t in terms), Fraction(0)) + \
+                abs(Fraction(1, 2) * Fraction(float(y[i])))
+            k = len(terms) + 2
+            assert abs(Fraction(float(ref[i])) - want[i]) <= k * u / (1 - k * u) * mag + \
+                Fraction(2) ** -1074, (trial, i)
+            want_bound = Fraction(1, 10**4) * Fraction(3, 4) * sum((abs(t) for t in terms), Fraction(0)) + \
+                abs(Fraction(1, 2) * Fraction(float(y[i]))) * Fraction(1, 2**22)
+            assert abs(Fraction(float(bound[i])) - want_bound) <= 8 * u * want_bound + Fraction(2) ** -1074
+    # (d) identity and permutation matrices: exact copies of x
+    n_ = 17
+    x = np.array([rnd.uniform(-1, 1) for _ in range(n_)], np.float32)
+    offs, cols, vals = _csr_from_triplets(n_, [(i, i, 1.0) for i in range(n_)])
+    ref, _ = o.spmv_csr(n_, n_, offs, cols, vals, x)
+    assert np.array_equal(ref, x.astype(np.float64)), "identity"
+    perm = list(range(n_))
+    rnd.shuffle(perm)
+    offs, cols, vals = _csr_from_triplets(n_, [(i, perm[i], 1.0) for i in range(n_)])
+    ref, _ = o.spmv_csr(n_, n_, offs, cols, vals, x)
+    assert np.array_equal(ref, x[perm].astype(np.float64)), "permutation"
+    # (e) BLAS semantics: beta == 0 never reads y, alpha == 0 never reads A or x
+    offs, cols, vals = _csr_from_triplets(3, [(0, 1, 2.0), (2, 0, -1.0)])
+    ynan = np.full(3, np.nan, np.float32)
+    ref, bound = o.spmv_csr(3, 2, offs, cols, vals, np.array([1, 2], np.float32), 1.0, 0.0, ynan)
+    assert np.isfinite(ref).all() and np.isfinite(bound).all(), "beta=0 read y"
+    y = np.array([1, -2, 4], np.float32)
+    ref, _ = o.spmv_csr(3, 2, offs, cols, np.full(2, np.nan, np.float32),
+                        np.full(2, np.nan, np.float32), 0.0, -0.5, y)
+    assert np.array_equal(ref, -0.5 * y.astype(np.float64)), "alpha=0 read A/x"
+    # (f) arrays that are not a CSR matrix of the shape are rejected
+    bad = [(np.array([0, 2, 1, 2], np.int32), np.array([0, 1], np.int32)),   # decreasing
+           (np.array([1, 1, 2, 2], np.int32), np.array([0, 1], np.int32)),   # first offset != 0
+           (np.array([0, 1, 2, 2], np.int32), np.array([0, 2], np.int32))]   # column 2 of 2
+    for offs, cols in bad:
+        try:
+            o.spmv_csr(3, 2, offs, cols, np.ones(2, np.float32), np.ones(2, np.float32))
+        except ValueError:
+            continue
+        raise AssertionError(("accepted", offs.tolist(), cols.tolist()))
+
+
 ALL_PINS = [pin_identity, pin_permutation, pin_alpha_beta, pin_small_integers, pin_int8,
             pin_tiny_rational, pin_bf16_decode, pin_f16_decode, pin_bf16_round, pin_ulp_bf16,
-            pin_transposed_a, pin_bias, pin_sum_rows, pin_tf32]
+            pin_transposed_a, pin_bias, pin_sum_rows, pin_tf32, pin_spmv]

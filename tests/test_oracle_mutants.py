@@ -37,6 +37,15 @@ MUTANTS = [
     ("alpha_zero_reads_ab", "if (alpha != 0.0) {", "if (1) {", 0),
     ("lda_ignored", "a_index(layout_a, i, k, lda)", "a_index(layout_a, i, k, K)", 0),
     ("i8_lda_ignored", "a_index(layout_a, i, k, lda)", "a_index(layout_a, i, k, K)", 1),
+    ("spmv_x_by_position", "(double)x[column_indices[p]];  /* exact */", "(double)x[p % cols];", 0),
+    ("spmv_row_end_inclusive", "p < row_offsets[i + 1]; ++p) {\n                double prod",
+     "p <= row_offsets[i + 1] && p < row_offsets[rows]; ++p) {\n                double prod", 0),
+    ("spmv_skips_first", "p = row_offsets[i]; p < row_offsets[i + 1]; ++p) {\n                double prod",
+     "p = row_offsets[i] + 1; p < row_offsets[i + 1]; ++p) {\n                double prod", 0),
+    ("spmv_beta_dropped", "double yterm = beta != 0.0 ? beta * (double)y[i] : 0.0;", "double yterm = 0.0;", 0),
+    ("spmv_alpha_on_y", "ref[i] = alpha * sum + yterm;", "ref[i] = alpha * (sum + yterm);", 0),
+    ("spmv_beta_zero_reads_y", "double yterm = beta != 0.0 ?", "double yterm = 1 ?", 0),
+    ("spmv_no_column_check", "column_indices[p] >= cols) return -1;", "column_indices[p] > cols) return -1;", 0),
     ("tf32_term_dropped", "in_dtype == OR_TF32 ? ldexp(1.0, -9) + ldexp(1.0, -20) + 1e-4 : 1e-4",
      "1e-4", 0),
     ("tf32_read_as_16_bit", "    case OR_F32:\n    case OR_TF32: return (double)((const float*)p)[idx];",
