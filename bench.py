@@ -10,7 +10,8 @@ than 2x the 129 MB L2).  Rank 0 prints ONE JSON line.
 
 Extra keys beside the contract's: `per_dtype` (the other hot-path workloads
 -- BF16 8192^3 on tcgen05, skinny M in {1, 8, 16}, INT8 4093x4099x4096, FP16
-8192^3, BF16 8192^3 with a row-major B, and one fully-connected layer step
+8192^3, BF16 8192^3 with a row-major B, FP32 8192^3 multiplied as TF32 (the
+opt-in lossy tensor-core path), and one fully-connected layer step
 (forward, both gradient GEMMs and the bias gradient) in bf16 at 8192 and in
 fp32 at 4096 -- each timed the same way, with its roofline fraction) and
 `peaks` (where every denominator came from).
@@ -46,7 +47,7 @@ L2_BYTES = 129 * 1024 * 1024
 # A and B read, C written, and C read as well when beta != 0 (section 5.1's
 # "minimum bytes" column).  Intensity I = FLOPs / bytes (section 5.1).
 
-DTYPE_BYTES = {0: 4, 1: 2, 2: 2, 3: 1, 4: 4}
+DTYPE_BYTES = {0: 4, 1: 2, 2: 2, 3: 1, 4: 4, 5: 4}  # 5: TF32 (fp32 storage)
 
 
 def gemm_flops(M, N, K):
@@ -82,7 +83,19 @@ def fc_accounting(w):
     return fl, by
 
 
-def workload_accounting(w):
+def spmv_accounting(w, nnz):
+    """CSR SpMV y = alpha A x + beta y ("AI Programming: Matrix Product",
+    section "SpMV"): one multiply and one add per stored entry; bytes read
+    once each: row offsets (rows + 1 int32), column indices and values (nnz
+    int32 + nnz fp32), x (cols fp32), y written (and read when beta != 0)."""
+    fl = 2 * nnz
+    by = 4 * (w.M + 1) + 8 * nnz + 4 * w.N + 4 * w.M * (2 if w.beta != 0 else 1)
+    return fl, by
+
+
+def workload_accounting(w, nnz=None):
+    if w.kind == "spmv":
+        return spmv_accounting(w, nnz)
     if w.kind == "fc":
         return fc_accounting(w)
     fl = gemm_flops(w.M, w.N, w.K)
@@ -110,7 +123,11 @@ def load_peaks(sm_count):
         hbm, bf16, bf16_sus, sm_max = 6800.0, 1900.0, 1700.0, 2070.0
     # 128 FP32 lanes per SM, one FFMA (2 FLOP) per lane per clock
     fp32 = sm_count * 128 * 2 * sm_max * 1e6 / 1e12
-    return {"source": src, "hbm_gbs": hbm, "bf16_tflops": bf16,
+    # TF32 has no measured figure: the measured bf16 peak times the nominal
+    # dense ratio (1.1 PFLOP/s TF32 against 2.25 PFLOP/s BF16 per GPU)
+    tf32 = bf16 * 1.1 / 2.25
+    return {"source": src, "hbm_gbs": hbm, "bf16_tflops": bf16, "tf32_tflops": tf32,
+            "tf32_basis": "measured bf16 x nominal 1.1/2.25",
             "bf16_tflops_sustained": bf16_sus, "fp32_ffma_tflops": fp32,
             "fp32_ffma_basis": f"{sm_count} SMs x 128 lanes x 2 FLOP x {sm_max:.0f} MHz",
             "sm_max_mhz": sm_max}
@@ -304,13 +321,56 @@ class FcRunner:
         return launches + 1
 
 
+class SpmvRunner:
+    """Device-resident synthetic CSR matrices (the power-law structure of
+    inputs.csr_powerlaw, drawn with torch's CUDA generator) and the
+    dga_spmv_csr call on them."""
+
+    def __init__(self, w, device, sets, seed=0):
+        import torch
+
+        import dense_gemm_accelerator_gb300 as dga
+        from dense_gemm_accelerator_gb300 import inputs as gen
+        self.w, self.dga = w, dga
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.sets = []
+        for _ in range(sets):
+            offs, cols, vals = gen.csr_powerlaw(w.M, w.N, g, device, **gen.CSR_STRUCTURE)
+            x = torch.rand(w.N, generator=g, device=device) * 2 - 1
+            self.sets.append((offs, cols, vals, x))
+        self.nnz = [st[2].numel() for st in self.sets]
+        self.mean_nnz = sum(self.nnz) / len(self.nnz)
+        self.y = torch.empty(w.M, dtype=torch.float32, device=device)
+        self.ws_bytes = max(dga.dga_spmv_csr_workspace_size(w.M, n) for n in self.nnz)
+        self.ws = torch.empty(max(self.ws_bytes, 1), dtype=torch.uint8, device=device)
+        self.alpha = dga.scalar(w.alpha, gen.F32)
+        self.beta = dga.scalar(w.beta, gen.F32)
+        self.paths = ["spmv"]
+
+    def call(self, i, stream):
+        import ctypes
+        offs, cols, vals, x = self.sets[i % len(self.sets)]
+        w, dga = self.w, self.dga
+        st = dga.dga_spmv_csr(w.M, w.N, vals.numel(), offs.data_ptr(), cols.data_ptr(),
+                              vals.data_ptr(), ctypes.byref(self.alpha), x.data_ptr(),
+                              ctypes.byref(self.beta), self.y.data_ptr(), self.ws.data_ptr(),
+                              self.ws_bytes, stream)
+        if st != dga.OK:
+            raise dga.DgaError(st, f"dga_spmv_csr ({w.name})")
+        return dga.dga_last_launch_count()
+
+
 def runner_for(w, device, sets, seed=0):
-    return (FcRunner if w.kind == "fc" else Runner)(w, device, sets, seed)
+    return {"fc": FcRunner, "spmv": SpmvRunner}.get(w.kind, Runner)(w, device, sets, seed)
 
 
 def sets_for(w, min_sets=2):
     """Enough input sets that one rotation spans > 2x L2."""
     from dense_gemm_accelerator_gb300 import inputs as gen
+    if w.kind == "spmv":  # mean row length ~23: values + column indices ~184 bytes per row
+        per = 8 * 23 * w.M
+        return int(max(min_sets, -(-2 * L2_BYTES // per) + 1))
     if w.kind == "fc":  # X, W, G (the outputs are shared by all sets)
         per = DTYPE_BYTES[w.in_dtype] * (w.M * w.K + w.N * w.K + w.M * w.N)
     else:
@@ -340,10 +400,10 @@ def time_kernel(runner, steps, warmup):
     return e0.elapsed_time(e1) / steps, launches
 
 
-def roofline_for(w, ms_mean, peaks, sustained=False):
-    fl, by = workload_accounting(w)
+def roofline_for(w, ms_mean, peaks, sustained=False, nnz=None):
+    fl, by = workload_accounting(w, nnz)
     from dense_gemm_accelerator_gb300 import inputs as gen
-    if w.name.startswith("skinny"):
+    if w.name.startswith("skinny") or w.kind == "spmv":
         ach = by / (ms_mean * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / peaks["hbm_gbs"], "algorithmic_bytes": by}
@@ -353,10 +413,14 @@ def roofline_for(w, ms_mean, peaks, sustained=False):
                 "unit": "TFLOP/s", "frac": ach / peaks["fp32_ffma_tflops"],
                 "algorithmic_flops": fl}
     pk = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    if w.in_dtype == gen.TF32:
+        pk = peaks["tf32_tflops"] * (peaks["bf16_tflops_sustained"] / peaks["bf16_tflops"]
+                                     if sustained else 1.0)
     return {"bound": "tensor", "achieved": ach, "peak": pk, "unit": "TFLOP/s" if w.in_dtype != gen.I8 else "TOP/s",
             "frac": ach / pk, "algorithmic_flops": fl,
             "peak_kind": {gen.I8: "bf16 tensor (INT8 runs as exact bf16 products)",
-                          gen.F16: "bf16 tensor (fp16 has the same nominal rate)"}.get(
+                          gen.F16: "bf16 tensor (fp16 has the same nominal rate)",
+                          gen.TF32: "tf32 tensor (measured bf16 x nominal 1.1/2.25)"}.get(
                               w.in_dtype, "bf16 tensor")}
 
 
@@ -383,10 +447,12 @@ def traffic_record(kernel_src, workload):
 
 
 KERNEL_SOURCE = {"fp32": "sgemm_simt.cu", "bf16": "gemm_tcgen05.cu", "skinny": "gemv_skinny.cu",
-                 "int8": "gemm_tcgen05.cu"}
+                 "int8": "gemm_tcgen05.cu", "spmv": "spmv_csr.cu"}
 
 
 def source_of(w):
+    if w.kind == "spmv":
+        return KERNEL_SOURCE["spmv"]
     if w.name.startswith("skinny"):
         return KERNEL_SOURCE["skinny"]
     if w.name.startswith("fp32"):
@@ -417,7 +483,8 @@ def e2e_leg(w, steps, warmup, device):
         dB.copy_(hB, non_blocking=True)
         if hC is not None:
             dC.copy_(hC, non_blocking=True)
-        dga.gemm(dA, dB.t() if w.layout_b == gen.COL_MAJOR else dB, dC, w.alpha, w.beta)
+        dga.gemm(dA, dB.t() if w.layout_b == gen.COL_MAJOR else dB, dC, w.alpha, w.beta,
+                 tf32=w.in_dtype == gen.TF32)
         out.copy_(dC, non_blocking=True)
 
     for _ in range(warmup):
@@ -609,13 +676,14 @@ def main():
     # (the paths measured here launch one kernel per call; when a call
     # launches more, their sum is attributed to the call)
     kmean = g0.elapsed_time(g1) / args.steps
-    fl, by = workload_accounting(w)
-    if w.name.startswith("skinny"):
+    nnz = getattr(runner, "mean_nnz", None)
+    fl, by = workload_accounting(w, nnz)
+    if w.name.startswith("skinny") or w.kind == "spmv":
         value, unit = job_throughput(by, world, args.steps, total_ms, 1e9), "GB/s"
     else:
         value = job_throughput(fl, world, args.steps, total_ms, 1e12)
         unit = "TOPS" if w.in_dtype == gen.I8 else "TFLOPS"
-    roof = roofline_for(w, kmean, peaks)
+    roof = roofline_for(w, kmean, peaks, nnz=nnz)
     roof["traffic"] = traffic_record(source_of(w), w.name)
     roof["kernel_ms_mean"] = kmean
     roof["launches_per_step"] = launches / args.steps
@@ -623,11 +691,12 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
-            "dtype": {gen.F32: "f32", gen.BF16: "bf16", gen.F16: "f16", gen.I8: "int8"}[w.in_dtype],
+            "dtype": {gen.F32: "f32", gen.BF16: "bf16", gen.F16: "f16", gen.I8: "int8",
+                      gen.TF32: "tf32"}[w.in_dtype],
             "data": "synthetic",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
                        "beta": w.beta, "layout_b": "col" if w.layout_b else "row",
-                       "path": (",".join(runner.paths) if w.kind == "fc"
+                       "path": (",".join(runner.paths) if w.kind in ("fc", "spmv")
                                 else dga.PATH_NAMES[dga.dga_last_path()]),
                        "l2": f"inputs rotated over {len(runner.sets)} resident sets (> 2x L2 per rotation)",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -642,7 +711,8 @@ def main():
         line["e2e"] = e2e_leg(w, max(3, args.steps // 3), 2, device)
         per = {}
         for name in ("bf16_8192", "skinny_m1", "skinny_m8", "skinny_m16", "int8_ragged",
-                     "f16_8192", "bf16_8192_rowb", "fc_bf16_8192", "fc_f32_4096"):
+                     "f16_8192", "bf16_8192_rowb", "tf32_8192", "spmv_powerlaw", "fc_bf16_8192",
+                     "fc_f32_4096"):
             if name == w.name:
                 continue
             ow = gen.WORKLOADS[name]
@@ -655,11 +725,15 @@ def main():
             ms, nl = time_kernel(r, iters, 5 if ow.kind != "fc" else 2)
             t1 = time.time()
             leg_clocks.stop()
-            rf = roofline_for(ow, ms, peaks)
-            rf["traffic"] = traffic_record(source_of(ow), name) if ow.kind == "gemm" else None
+            rf = roofline_for(ow, ms, peaks, nnz=getattr(r, "mean_nnz", None))
+            rf["traffic"] = traffic_record(source_of(ow), name) if ow.kind != "fc" else None
             rf["ms_mean"] = ms
             rf["launches_per_call"] = nl / iters
             rf["clocks"] = leg_clocks.summary(t0 - 0.05, t1 + 0.05)
+            if ow.kind == "spmv":
+                rf["nnz"] = r.mean_nnz
+                rf["structure"] = ("Pareto(1.5) row lengths, min 8, max 16384, 5% empty rows; "
+                                   "columns within +-4096 of the diagonal; x stays in L2")
             if ow.kind == "fc":
                 rf["paths"] = r.paths
                 rf["algorithmic_bytes"] = workload_accounting(ow)[1]

@@ -15,7 +15,7 @@ import ctypes
 import os
 import threading
 
-from .inputs import BF16, COL_MAJOR, F16, F32, I8, I32, ROW_MAJOR  # noqa: F401  (codes)
+from .inputs import BF16, COL_MAJOR, F16, F32, I8, I32, ROW_MAJOR, TF32  # noqa: F401  (codes)
 
 PATH_AUTO, PATH_GENERIC, PATH_SIMT, PATH_TCGEN05, PATH_SKINNY = 0, 1, 2, 3, 4
 PATH_NAMES = {PATH_AUTO: "auto", PATH_GENERIC: "generic", PATH_SIMT: "simt",
@@ -24,6 +24,7 @@ PATH_NAMES = {PATH_AUTO: "auto", PATH_GENERIC: "generic", PATH_SIMT: "simt",
 OK = 0
 ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT, ERR_PATH, ERR_WORKSPACE, ERR_OVERLAP, ERR_DEVICE = \
     1, 2, 3, 4, 5, 6, 7
+ERR_BAD_INDEX = 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libdga.so")
@@ -51,6 +52,8 @@ SIGNATURES = {
     "dga_sum_rows": (_CI, [_CI, _I64, _I64, _VP, _I64, _VP, _VP]),
     "dga_gemm_i8_noalloc": (_CI, [_CI, _I64, _I64, _I64, _VP, _VP, _I64, _VP, _I64, _VP, _VP,
                                   _I64, _VP]),
+    "dga_spmv_csr": (_CI, [_I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
+    "dga_spmv_csr_workspace_size": (_SZ, [_I64, _I64]),
 }
 
 _lock = threading.Lock()
@@ -160,6 +163,16 @@ def dga_gemm_i8_noalloc(layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, 
                                      stream)
 
 
+def dga_spmv_csr(rows, cols, nnz, row_offsets, column_indices, values, alpha, x, beta, y,
+                 workspace, workspace_bytes, stream):
+    return lib().dga_spmv_csr(rows, cols, nnz, row_offsets, column_indices, values, alpha, x,
+                              beta, y, workspace, workspace_bytes, stream)
+
+
+def dga_spmv_csr_workspace_size(rows, nnz):
+    return lib().dga_spmv_csr_workspace_size(rows, nnz)
+
+
 # ---- tensor convenience layer ----------------------------------------------
 
 def _dtype_code(t):
@@ -204,7 +217,7 @@ def operand_layout(A, B, C):
 
 
 def gemm(A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, path=PATH_AUTO, workspace=None,
-         stream=None, bias=None):
+         stream=None, bias=None, tf32=False):
     """C <- alpha * A @ B + beta * C (+ bias) on the GPU; returns C.
 
     A: (M, K) and B: (K, N) CUDA tensors, each row- or column-major (a
@@ -212,11 +225,17 @@ def gemm(A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, path=PATH_AUTO, work
     row-major, allocated when None (then beta must be 0).  bias: optional (N,)
     tensor of C's dtype added to every row.  The workspace, when the chosen
     path needs one, is allocated from PyTorch's caching allocator unless given.
+    tf32=True (fp32 A and B only) asks for the lossy TF32 tensor-core product
+    (DGA_TF32); fp32 inputs are otherwise multiplied exactly in fp32.
     """
     import torch
     in_dtype = _dtype_code(A)
     if _dtype_code(B) != in_dtype:
         raise TypeError("A and B must have the same dtype")
+    if tf32:
+        if in_dtype != F32:
+            raise TypeError("tf32=True needs fp32 A and B")
+        in_dtype = TF32
     if A.dim() != 2 or B.dim() != 2:
         raise ValueError("A and B must be 2-D")
     M, K = A.shape
@@ -227,7 +246,7 @@ def gemm(A, B, C=None, alpha=1.0, beta=0.0, out_dtype=None, path=PATH_AUTO, work
         if beta != 0:
             raise ValueError("beta != 0 needs C")
         if out_dtype is None:
-            out_dtype = I32 if in_dtype == I8 else (in_dtype if in_dtype != F32 else F32)
+            out_dtype = I32 if in_dtype == I8 else (F32 if in_dtype == TF32 else in_dtype)
         C = torch.empty((M, N), dtype={F32: torch.float32, BF16: torch.bfloat16,
                                        F16: torch.float16, I32: torch.int32}[out_dtype],
                         device=A.device)
@@ -275,6 +294,46 @@ def sum_rows(G, out=None, stream=None):
     if st != OK:
         raise DgaError(st, "dga_sum_rows")
     return out
+
+
+def spmv_csr(row_offsets, column_indices, values, x, y=None, alpha=1.0, beta=0.0, cols=None,
+             workspace=None, stream=None):
+    """y <- alpha * A @ x + beta * y for the CSR matrix A given by int32
+    row_offsets (rows + 1), int32 column_indices and fp32 values (nnz each),
+    all CUDA tensors; x has cols = x.numel() entries unless `cols` is given.
+    Returns y (allocated when None; then beta must be 0)."""
+    import ctypes as ct
+
+    import torch
+    rows = row_offsets.numel() - 1
+    nnz = values.numel()
+    cols = x.numel() if cols is None else cols
+    for t, name, dt in ((row_offsets, "row_offsets", torch.int32),
+                        (column_indices, "column_indices", torch.int32),
+                        (values, "values", torch.float32), (x, "x", torch.float32)):
+        if t.dtype != dt or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous {dt} tensor")
+    if column_indices.numel() != nnz:
+        raise ValueError("column_indices and values must have the same length")
+    if y is None:
+        if beta != 0:
+            raise ValueError("beta != 0 needs y")
+        y = torch.empty(rows, dtype=torch.float32, device=values.device)
+    if y.dtype != torch.float32 or not y.is_contiguous() or y.numel() != rows:
+        raise ValueError(f"y must be a contiguous float32 tensor of {rows} entries")
+    if stream is None:
+        stream = torch.cuda.current_stream(values.device).cuda_stream
+    ws_bytes = dga_spmv_csr_workspace_size(rows, nnz)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=values.device)
+    a, b = ct.c_float(float(alpha)), ct.c_float(float(beta))
+    st = dga_spmv_csr(rows, cols, nnz, row_offsets.data_ptr(), column_indices.data_ptr(),
+                      values.data_ptr(), ct.byref(a), x.data_ptr(), ct.byref(b), y.data_ptr(),
+                      workspace.data_ptr() if workspace is not None else None,
+                      workspace.numel() if workspace is not None else 0, stream)
+    if st != OK:
+        raise DgaError(st, "dga_spmv_csr")
+    return y
 
 
 def linear_forward(X, W, bias=None, Y=None):

@@ -28,12 +28,13 @@ cudaError_t g_dev_err[kMaxDevices];
 
 bool pair_supported(int in, int out) {
     return (in == DGA_F32 && out == DGA_F32) || (in == DGA_BF16 && (out == DGA_F32 || out == DGA_BF16)) ||
-           (in == DGA_F16 && (out == DGA_F32 || out == DGA_F16)) || (in == DGA_I8 && out == DGA_I32);
+           (in == DGA_F16 && (out == DGA_F32 || out == DGA_F16)) || (in == DGA_I8 && out == DGA_I32) ||
+           (in == DGA_TF32 && out == DGA_F32);
 }
 
 size_t elem_size(int dt) {
     switch (dt) {
-    case DGA_F32: case DGA_I32: return 4;
+    case DGA_F32: case DGA_I32: case DGA_TF32: return 4;
     case DGA_BF16: case DGA_F16: return 2;
     case DGA_I8: return 1;
     default: return 0;
@@ -65,7 +66,7 @@ int check_args(const ArgPos& pos, dga_dtype in_dtype, dga_dtype out_dtype, dga_l
                const void* A, int64_t lda, const void* B, int64_t ldb, const void* beta, void* C,
                int64_t ldc, const void* bias, void* ws, size_t ws_bytes, GemmArgs* g,
                bool with_pointers = true) {
-    if (in_dtype < DGA_F32 || in_dtype > DGA_I32 || out_dtype < DGA_F32 || out_dtype > DGA_I32)
+    if (in_dtype < DGA_F32 || in_dtype > DGA_TF32 || out_dtype < DGA_F32 || out_dtype > DGA_TF32)
         return DGA_ERR_UNSUPPORTED;
     if (layout_a != DGA_ROW_MAJOR && layout_a != DGA_COL_MAJOR) return DGA_ERR_UNSUPPORTED;
     if (layout_b != DGA_ROW_MAJOR && layout_b != DGA_COL_MAJOR) return DGA_ERR_UNSUPPORTED;
@@ -141,7 +142,8 @@ int choose_path(const GemmArgs& g) {
         if (tc_supports(g)) return DGA_PATH_TCGEN05;
         return DGA_PATH_GENERIC;
     }
-    if (g.in_dtype == DGA_I8) return tc_supports(g) ? DGA_PATH_TCGEN05 : DGA_PATH_GENERIC;
+    if (g.in_dtype == DGA_I8 || g.in_dtype == DGA_TF32)
+        return tc_supports(g) ? DGA_PATH_TCGEN05 : DGA_PATH_GENERIC;
     return DGA_PATH_GENERIC;
 }
 
@@ -341,6 +343,54 @@ int dga_select_path(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b
     return choose_path(g);
 }
 
+size_t dga_spmv_csr_workspace_size(int64_t rows, int64_t nnz) {
+    if (rows <= 0 || nnz < 0) return 0;
+    return spmv_workspace_size(rows, nnz, sm_count_or_default());
+}
+
+int dga_spmv_csr(int64_t rows, int64_t cols, int64_t nnz, const int32_t* row_offsets,
+                 const int32_t* column_indices, const float* values, const float* alpha,
+                 const float* x, const float* beta, float* y, void* workspace,
+                 size_t workspace_bytes, dga_stream_t stream) {
+    if (rows < 0 || rows >= (int64_t(1) << 31) - 1) return -1;
+    if (cols < 0 || cols >= (int64_t(1) << 31)) return -2;
+    if (nnz < 0 || nnz >= (int64_t(1) << 31)) return -3;
+    if (!alpha) return -7;
+    if (!beta) return -9;
+    t_last_path = DGA_PATH_AUTO;
+    t_last_launches = 0;
+    if (rows == 0) return DGA_OK;
+    if (!row_offsets) return -4;
+    const float a = *alpha, b = *beta;
+    const bool reads_a = a != 0.0f && nnz > 0;
+    if (reads_a && !column_indices) return -5;
+    if (reads_a && !values) return -6;
+    if (reads_a && !x) return -8;
+    if (!y) return -10;
+    if (workspace_bytes > 0 && !workspace) return -11;
+    // y must not overlap the arrays it is computed from
+    const uintptr_t y0 = reinterpret_cast<uintptr_t>(y), y1 = y0 + static_cast<uintptr_t>(rows) * 4;
+    auto hits = [&](const void* q, int64_t bytes) {
+        const uintptr_t q0 = reinterpret_cast<uintptr_t>(q);
+        return q && bytes > 0 && overlaps(y0, y1, q0, q0 + static_cast<uintptr_t>(bytes));
+    };
+    if (hits(row_offsets, (rows + 1) * 4) || (reads_a && (hits(column_indices, nnz * 4) ||
+                                                          hits(values, nnz * 4) || hits(x, cols * 4))))
+        return DGA_ERR_OVERLAP;
+    DeviceInfo dev;
+    cudaError_t e = current_device_info(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev.major != 10 || dev.minor != 3) return DGA_ERR_DEVICE;
+    if (reads_a && workspace_bytes < spmv_workspace_size(rows, nnz, dev.sm_count))
+        return DGA_ERR_WORKSPACE;
+    int launches = 0;
+    e = spmv_launch(rows, cols, nnz, row_offsets, column_indices, values, a, x, b, y, workspace,
+                    workspace_bytes, dev, reinterpret_cast<cudaStream_t>(stream), &launches);
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_launches = launches;
+    return DGA_OK;
+}
+
 int dga_last_path(void) { return t_last_path; }
 
 int dga_last_launch_count(void) { return t_last_launches; }
@@ -348,10 +398,13 @@ int dga_last_launch_count(void) { return t_last_launches; }
 int dga_sync_status(dga_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e);
-    int st = 0;
+    int st = 0, st_skinny = 0, st_spmv = 0;
     e = tc_status_take(&st);
+    if (e == cudaSuccess) e = skinny_status_take(&st_skinny);
+    if (e == cudaSuccess) e = spmv_status_take(&st_spmv);
     if (e != cudaSuccess) return fail_cuda(e);
-    return st != 0 ? DGA_ERR_DEVICE_TIMEOUT : DGA_OK;
+    if (st != 0 || st_skinny != 0) return DGA_ERR_DEVICE_TIMEOUT;
+    return st_spmv != 0 ? DGA_ERR_BAD_INDEX : DGA_OK;
 }
 
 int dga_last_cuda_error(void) { return t_last_cuda_error; }
@@ -374,6 +427,7 @@ const char* dga_status_string(int status) {
     case DGA_ERR_WORKSPACE: return "workspace smaller than dga_gemm_workspace_size()";
     case DGA_ERR_OVERLAP: return "C overlaps A or B";
     case DGA_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    case DGA_ERR_BAD_INDEX: return "a CSR index or row offset was out of range (reported by dga_sync_status)";
     default: return "unknown status";
     }
 }

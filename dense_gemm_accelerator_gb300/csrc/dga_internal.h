@@ -68,6 +68,17 @@ cudaError_t simt_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches)
 
 bool skinny_supports(const GemmArgs& a);
 cudaError_t skinny_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);
+// Reads and clears this device's skinny-path status word.
+cudaError_t skinny_status_take(int* status);
+
+// CSR sparse matrix-vector product (validated arguments; alpha, beta by value).
+size_t spmv_workspace_size(int64_t rows, int64_t nnz, int sm_count);
+cudaError_t spmv_launch(int64_t rows, int64_t cols, int64_t nnz, const int32_t* row_offsets,
+                        const int32_t* column_indices, const float* values, float alpha,
+                        const float* x, float beta, float* y, void* ws, size_t ws_bytes,
+                        const DeviceInfo& dev, cudaStream_t stream, int* launches);
+// Reads and clears this device's SpMV status word (non-zero: malformed CSR arrays).
+cudaError_t spmv_status_take(int* status);
 
 bool tc_supports(const GemmArgs& a);
 size_t tc_workspace_size(const GemmArgs& a);

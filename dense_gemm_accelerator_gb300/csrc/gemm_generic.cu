@@ -158,7 +158,10 @@ cudaError_t generic_launch(const GemmArgs& a, int* launches) {
     Params p{a.M, a.N, a.K, a.A, a.lda, a.B, a.ldb, a.C, a.ldc, a.bias, a.layout_a, a.layout_b,
              a.alpha_f, a.beta_f, a.alpha_i, a.beta_i, (a.K == 0 || alpha_is_zero(a)) ? 1 : 0};
     cudaError_t e = cudaErrorInvalidValue;
-    if (a.in_dtype == DGA_F32 && a.out_dtype == DGA_F32) e = launch_typed<float, float>(p, a.stream);
+    // TF32 inputs are fp32 in memory; this family multiplies them exactly in
+    // fp32, which is within the TF32 error bound
+    if ((a.in_dtype == DGA_F32 || a.in_dtype == DGA_TF32) && a.out_dtype == DGA_F32)
+        e = launch_typed<float, float>(p, a.stream);
     else if (a.in_dtype == DGA_BF16 && a.out_dtype == DGA_F32) e = launch_typed<__nv_bfloat16, float>(p, a.stream);
     else if (a.in_dtype == DGA_BF16 && a.out_dtype == DGA_BF16) e = launch_typed<__nv_bfloat16, __nv_bfloat16>(p, a.stream);
     else if (a.in_dtype == DGA_F16 && a.out_dtype == DGA_F32) e = launch_typed<__half, float>(p, a.stream);

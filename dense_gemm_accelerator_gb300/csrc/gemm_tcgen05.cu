@@ -4,7 +4,8 @@
 // fp32 accumulation and fp32 / bf16 / fp16 output -- the Tensor Core
 // precision rows (BF16 / FP16 inputs, FP32 accumulate) of "Matrix
 // multiplication: arithmetic intensity, tiling and Tensor Core", section
-// 5.5.  The pages' own tensor-core kernels are WMMA 16x16x16 warp tiles on
+// 5.5 -- and, on request only, fp32 inputs multiplied as TF32 (the TF32 row
+// of the same table; 10 mantissa bits, so lossy, as section 5.7 warns).  The pages' own tensor-core kernels are WMMA 16x16x16 warp tiles on
 // A100/H100; this one is built for Blackwell instead:
 //
 //   * One persistent CTA per SM walks output tiles of 128 x 256 in a grouped
@@ -27,6 +28,13 @@
 //     per-device status word, tells the other roles to stop, and the CTA
 //     drains its outstanding copies and MMAs and frees its TMEM before
 //     returning (read with dga_sync_status()).
+//
+// TF32 uses the same kernels with kind::tf32: a K block is still one
+// 128-byte swizzle row (32 fp32 elements instead of 64 16-bit ones) and every
+// MMA still consumes 32 bytes of it (K = 8 instead of 16), so the shared
+// memory layout, descriptors and pipeline are the same.  TF32 operands are
+// always read K-major: a column-major A or row-major B is first transposed
+// into the workspace by pack_transposed_f32_kernel.
 //
 // Operands reach the tensor cores in their own layout: K-major (A row-major,
 // B column-major) as 64 x rows boxes, or MN-major (A column-major, B
@@ -68,8 +76,10 @@ __device__ int g_tc_status;  // non-zero: a bounded wait expired (role code)
 namespace {
 
 constexpr int BM = 128;  // tile rows (UMMA M)
-constexpr int BK = 64;   // K per stage: 64 x 2 bytes = one 128-byte swizzle row
-constexpr int UK = 16;   // K per tcgen05.mma (kind::f16)
+constexpr int BK = 64;   // 16-bit K elements per stage: 64 x 2 bytes = one 128-byte swizzle row
+constexpr int UK = 16;   // 16-bit K elements per tcgen05.mma (32 bytes; kind::f16)
+// K elements per stage for an operand format: 32 fp32 elements for TF32.
+__host__ __device__ constexpr int k_per_stage(uint32_t fmt) { return fmt == kFmtTF32 ? BK / 2 : BK; }
 constexpr int kStages = 4;
 constexpr int kI8ChunkBlocks = 16;  // INT8: K blocks per exact fp32 chunk (16 x 64 = 1024)
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s
@@ -190,7 +200,7 @@ __device__ __forceinline__ void store_block_staged_i32(const TcParams& p, uint32
 // kI8: INT8 mode (bf16-encoded operands, chunked exact accumulation, int32 out).
 // BN: tile columns.  Epilogue warps: 4 (float) or 8 (INT8: two column halves).
 
-template <bool kBf16, bool kI8, int BN, typename TOut>
+template <uint32_t kFmt, bool kI8, int BN, typename TOut>
 __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    TcParams p) {
@@ -198,7 +208,8 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
     static_assert(BN % kMnAtom == 0, "MN-major B boxes tile the block columns");
     using S = Smem<BN, kI8 ? 8 : 4>;
     constexpr uint32_t kTmemCols = 2 * BN;  // two accumulators
-    constexpr uint32_t kIdesc = idesc_f16(kBf16, BM, BN);
+    constexpr uint32_t kIdesc = idesc_mma(kFmt, BM, BN);
+    constexpr int kKElems = k_per_stage(kFmt);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -257,7 +268,7 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                     uint8_t* a_dst = smem + stage * S::kStageBytes;
                     uint8_t* b_dst = a_dst + S::kABytes;
                     mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
-                    const int32_t k0 = static_cast<int32_t>(kb * BK);
+                    const int32_t k0 = static_cast<int32_t>(kb * kKElems);
                     if (p.a_mn) {
                         for (uint32_t j = 0; j < BM / kMnAtom; ++j)
                             tma_load_2d(a_dst + j * kMnBoxBytes, &tmA, &full[stage],
@@ -319,7 +330,7 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                                    : smem_desc_kmajor_sw128(a_addr + S::kABytes);
 #pragma unroll
                         for (int k = 0; k < BK / UK; ++k) {
-                            tc_mma_f16(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc,
+                            tc_mma<kFmt>(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc,
                                        (kb > kb_begin || k > 0) ? 1u : 0u);
                         }
                         tc_commit(&empty[stage]);
@@ -460,13 +471,14 @@ struct PairSmem {
     static constexpr uint32_t kLaunchBytes = kTotal + 1024;
 };
 
-template <bool kBf16, typename TOut>
+template <uint32_t kFmt, typename TOut>
 __global__ void __launch_bounds__(192, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, TcParams p) {
     using S = PairSmem;
     constexpr uint32_t kTmemCols = 2 * kPairBN;  // two accumulators
-    constexpr uint32_t kIdesc = idesc_f16(kBf16, 256, kPairBN);
+    constexpr uint32_t kIdesc = idesc_mma(kFmt, 256, kPairBN);
+    constexpr int kKElems = k_per_stage(kFmt);
     constexpr uint16_t kBothCtas = 0x3;
 
     extern __shared__ uint8_t smem_raw[];
@@ -532,7 +544,7 @@ __global__ void __launch_bounds__(192, 1)
                     uint8_t* b_dst = a_dst + S::kABytes;
                     if (leader) mbar_arrive_expect_tx(&full[stage], 2 * S::kStageBytes);
                     const uint32_t bar = map_to_cta(smem_u32(&full[stage]), 0);
-                    const int32_t k0 = static_cast<int32_t>(kb * BK);
+                    const int32_t k0 = static_cast<int32_t>(kb * kKElems);
                     if (p.a_mn) {
                         for (uint32_t j = 0; j < BM / kMnAtom; ++j)
                             tma_load_2d_pair(a_dst + j * kMnBoxBytes, &tmA, bar,
@@ -583,7 +595,7 @@ __global__ void __launch_bounds__(192, 1)
                                : smem_desc_kmajor_sw128(a_addr + S::kABytes);
 #pragma unroll
                     for (int k = 0; k < BK / UK; ++k)
-                        tc_mma_f16_pair(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc,
+                        tc_mma_pair<kFmt>(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     tc_commit_pair_multicast(&empty[stage], kBothCtas);
                     if (++stage == kPairStages) { stage = 0; phase ^= 1; }
@@ -745,6 +757,54 @@ __global__ void __launch_bounds__(256) pack_transposed_kernel(const TSrc* __rest
     }
 }
 
+// fp32 operands of the TF32 path, same contract with 4-byte elements:
+// dst[r][k] = src(r, k) for k < K, zero for K <= k < ld_dst (ld_dst % 4 == 0,
+// so every thread writes whole 16-byte vectors).
+__global__ void __launch_bounds__(256) pack_rows_f32_kernel(const float* __restrict__ src,
+                                                            int64_t ld_src, int64_t rows, int64_t K,
+                                                            float* __restrict__ dst, int64_t ld_dst) {
+    const int64_t groups = ld_dst / 4;
+    const int64_t total = rows * groups;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / groups, k = (i % groups) * 4;
+        const float* s = src + r * ld_src + k;
+        float4 v;
+        v.x = k < K ? s[0] : 0.0f;
+        v.y = k + 1 < K ? s[1] : 0.0f;
+        v.z = k + 2 < K ? s[2] : 0.0f;
+        v.w = k + 3 < K ? s[3] : 0.0f;
+        *reinterpret_cast<float4*>(dst + r * ld_dst + k) = v;
+    }
+}
+
+// Transposed fp32 source, src(r, k) = src[k*ld_src + r]: a 64 (k) x 64 (r)
+// tile per block through shared memory; reads walk r, writes walk k.
+__global__ void __launch_bounds__(256) pack_transposed_f32_kernel(const float* __restrict__ src,
+                                                                  int64_t ld_src, int64_t rows,
+                                                                  int64_t K, float* __restrict__ dst,
+                                                                  int64_t ld_dst) {
+    __shared__ float tile[64][64 + 1];  // tile[k][r]
+    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 64;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;
+    const int t = threadIdx.x;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+        const int idx = i * 256 + t, kk = idx >> 6, rr = idx & 63;
+        const int64_t k = k0 + kk, r = r0 + rr;
+        tile[kk][rr] = (k < K && r < rows) ? src[k * ld_src + r] : 0.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = i * 256 + t, rr = idx >> 4, kq = (idx & 15) * 4;
+        const int64_t r = r0 + rr, k = k0 + kq;
+        if (r < rows && k < ld_dst)
+            *reinterpret_cast<float4*>(dst + r * ld_dst + k) =
+                make_float4(tile[kq][rr], tile[kq + 1][rr], tile[kq + 2][rr], tile[kq + 3][rr]);
+    }
+}
+
 // ---- host side -------------------------------------------------------------------
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -766,16 +826,25 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// K-major operand: rows x K elements of 2 bytes, row stride ld elements.
+// Tensor-map element type and size of an operand format.
+CUtensorMapDataType map_dtype(uint32_t fmt) {
+    return fmt == kFmtTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                           : (fmt == kFmtBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+}
+int64_t elem_bytes(uint32_t fmt) { return fmt == kFmtTF32 ? 4 : 2; }
+
+// K-major operand: rows x K elements, row stride ld elements; boxes of one
+// 128-byte row of K (64 16-bit or 32 fp32 elements) x box_rows.
 cudaError_t make_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
-                            int64_t ld, uint32_t box_rows, bool bf16) {
+                            int64_t ld, uint32_t box_rows, uint32_t fmt) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * elem_bytes(fmt))};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(k_per_stage(fmt)), box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    CUresult r = fn(map, map_dtype(fmt), 2,
                     const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -785,14 +854,14 @@ cudaError_t make_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, in
 // MN-major operand: MN x K elements of 2 bytes with MN contiguous, k-row
 // stride ld elements; boxes of 64 MN-elements x 64 k.
 cudaError_t make_mnmajor_map(CUtensorMap* map, const void* base, int64_t mn, int64_t K,
-                             int64_t ld, bool bf16) {
+                             int64_t ld, uint32_t fmt) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return cudaErrorNotSupported;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(mn), static_cast<cuuint64_t>(K)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
     cuuint32_t box[2] = {kMnAtom, static_cast<cuuint32_t>(BK)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+    CUresult r = fn(map, map_dtype(fmt), 2,
                     const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -815,8 +884,19 @@ struct PackPlan {
 
 PackPlan plan_for(const GemmArgs& a) {
     PackPlan pl{};
-    pl.kp = round_up(a.K, 8);
     const bool i8 = a.in_dtype == DGA_I8;
+    if (a.in_dtype == DGA_TF32) {
+        // fp32 rows (4 elements = 16 bytes); TF32 operands are always K-major,
+        // so a column-major A or row-major B is transposed into the workspace
+        pl.kp = round_up(a.K, 4);
+        pl.pack_a = a.layout_a == DGA_COL_MAJOR || a.lda % 4 != 0 || !aligned(a.A, 16);
+        pl.pack_b = a.layout_b == DGA_ROW_MAJOR || a.ldb % 4 != 0 || !aligned(a.B, 16);
+        pl.a_mn = pl.b_mn = false;
+        pl.a_bytes = pl.pack_a ? round_up(a.M * pl.kp * 4, kWsAlign) : 0;
+        pl.b_bytes = pl.pack_b ? round_up(a.N * pl.kp * 4, kWsAlign) : 0;
+        return pl;
+    }
+    pl.kp = round_up(a.K, 8);
     // TMA needs 16-byte row strides and a 16-byte aligned base; INT8 is
     // always re-encoded (as bf16, K-major).
     pl.pack_a = i8 || a.lda % 8 != 0 || !aligned(a.A, 16);
@@ -850,10 +930,10 @@ uint32_t raster_group_rows(int64_t K, uint32_t tiles_m, int tile_rows) {
     return std::min(g, tiles_m);
 }
 
-template <bool kBf16, bool kI8, int BN, typename TOut>
+template <uint32_t kFmt, bool kI8, int BN, typename TOut>
 cudaError_t launch_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
                           const DeviceInfo& dev, cudaStream_t s) {
-    auto kern = tc_gemm_kernel<kBf16, kI8, BN, TOut>;
+    auto kern = tc_gemm_kernel<kFmt, kI8, BN, TOut>;
     const int smem = static_cast<int>(Smem<BN, kI8 ? 8 : 4>::kLaunchBytes);
     if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -890,10 +970,10 @@ int max_pair_clusters(Kern kern, int smem, const DeviceInfo& dev) {
     return n;
 }
 
-template <bool kBf16, typename TOut>
+template <uint32_t kFmt, typename TOut>
 cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
                                const DeviceInfo& dev, cudaStream_t s) {
-    auto kern = tc_gemm_pair_kernel<kBf16, TOut>;
+    auto kern = tc_gemm_pair_kernel<kFmt, TOut>;
     const int smem = static_cast<int>(PairSmem::kLaunchBytes);
     if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -933,11 +1013,28 @@ cudaError_t launch_pack(const void* src, int64_t ld_src, bool transposed, int64_
     return cudaGetLastError();
 }
 
+cudaError_t launch_pack_f32(const void* src, int64_t ld_src, bool transposed, int64_t rows,
+                            int64_t K, void* dst, int64_t ld_dst, int sm_count, cudaStream_t s) {
+    if (transposed) {
+        dim3 grid(static_cast<unsigned>((ld_dst + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
+        if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+        pack_transposed_f32_kernel<<<grid, 256, 0, s>>>(static_cast<const float*>(src), ld_src, rows,
+                                                        K, static_cast<float*>(dst), ld_dst);
+    } else {
+        const int64_t work = rows * (ld_dst / 4);
+        const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sm_count) * 16);
+        pack_rows_f32_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
+            static_cast<const float*>(src), ld_src, rows, K, static_cast<float*>(dst), ld_dst);
+    }
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool tc_supports(const GemmArgs& a) {
     const bool fp = (a.in_dtype == DGA_BF16 && (a.out_dtype == DGA_F32 || a.out_dtype == DGA_BF16)) ||
-                    (a.in_dtype == DGA_F16 && (a.out_dtype == DGA_F32 || a.out_dtype == DGA_F16));
+                    (a.in_dtype == DGA_F16 && (a.out_dtype == DGA_F32 || a.out_dtype == DGA_F16)) ||
+                    (a.in_dtype == DGA_TF32 && a.out_dtype == DGA_F32);
     const bool i8 = a.in_dtype == DGA_I8 && a.out_dtype == DGA_I32;
     if (!fp && !i8) return false;
     if (a.K < 1 || a.M < 1 || a.N < 1) return false;
@@ -953,7 +1050,9 @@ size_t tc_workspace_size(const GemmArgs& a) {
 
 cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     const bool i8 = a.in_dtype == DGA_I8;
+    const bool tf32 = a.in_dtype == DGA_TF32;
     const bool bf16 = i8 || a.in_dtype == DGA_BF16;
+    const uint32_t fmt = tf32 ? kFmtTF32 : (bf16 ? kFmtBF16 : kFmtF16);
     PackPlan pl = plan_for(a);
     if (a.ws_bytes < pl.a_bytes + pl.b_bytes) return cudaErrorInvalidValue;
     const void* A = a.A;
@@ -965,7 +1064,8 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     if (pl.pack_a) {
         void* dst = ws;
         const bool tr = a.layout_a == DGA_COL_MAJOR;  // A(i, k) = A[k*lda + i]: transpose to M x K
-        if (i8) e = launch_pack<int8_t>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        if (tf32) e = launch_pack_f32(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        else if (i8) e = launch_pack<int8_t>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
         else if (bf16) e = launch_pack<__nv_bfloat16>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
         else e = launch_pack<__half>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
         if (e != cudaSuccess) return e;
@@ -976,7 +1076,8 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     if (pl.pack_b) {
         void* dst = ws + pl.a_bytes;
         const bool tr = a.layout_b == DGA_ROW_MAJOR;  // B(k, j) = B[k*ldb + j]: transpose to N x K
-        if (i8) e = launch_pack<int8_t>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        if (tf32) e = launch_pack_f32(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
+        else if (i8) e = launch_pack<int8_t>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
         else if (bf16) e = launch_pack<__nv_bfloat16>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
         else e = launch_pack<__half>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
         if (e != cudaSuccess) return e;
@@ -989,11 +1090,11 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     const bool pair = !i8 && a.M > BM;
     const int BN = i8 ? kBnI8 : (pair ? kPairBN : kBnFloat);
     CUtensorMap ma, mb;
-    e = pl.a_mn ? make_mnmajor_map(&ma, A, a.M, a.K, lda, bf16)
-                : make_kmajor_map(&ma, A, a.M, a.K, lda, BM, bf16);
+    e = pl.a_mn ? make_mnmajor_map(&ma, A, a.M, a.K, lda, fmt)
+                : make_kmajor_map(&ma, A, a.M, a.K, lda, BM, fmt);
     if (e != cudaSuccess) return e;
-    e = pl.b_mn ? make_mnmajor_map(&mb, B, a.N, a.K, ldb, bf16)
-                : make_kmajor_map(&mb, B, a.N, a.K, ldb, pair ? kPairBN / 2 : BN, bf16);
+    e = pl.b_mn ? make_mnmajor_map(&mb, B, a.N, a.K, ldb, fmt)
+                : make_kmajor_map(&mb, B, a.N, a.K, ldb, pair ? kPairBN / 2 : BN, fmt);
     if (e != cudaSuccess) return e;
 
     TcParams p{};
@@ -1013,18 +1114,20 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     p.tiles_m = static_cast<uint32_t>((a.M + tile_m - 1) / tile_m);
     p.tiles_n = static_cast<uint32_t>((a.N + BN - 1) / BN);
     p.num_tiles = p.tiles_m * p.tiles_n;
-    p.num_kb = static_cast<uint32_t>((a.K + BK - 1) / BK);
+    p.num_kb = static_cast<uint32_t>((a.K + k_per_stage(fmt) - 1) / k_per_stage(fmt));
     p.group_m = raster_group_rows(a.K, p.tiles_m, tile_m);
 
-    if (i8) e = launch_kernel<true, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream);
-    else if (pair && bf16 && a.out_dtype == DGA_F32) e = launch_pair_kernel<true, float>(ma, mb, p, dev, a.stream);
-    else if (pair && bf16) e = launch_pair_kernel<true, __nv_bfloat16>(ma, mb, p, dev, a.stream);
-    else if (pair && a.out_dtype == DGA_F32) e = launch_pair_kernel<false, float>(ma, mb, p, dev, a.stream);
-    else if (pair) e = launch_pair_kernel<false, __half>(ma, mb, p, dev, a.stream);
-    else if (bf16 && a.out_dtype == DGA_F32) e = launch_kernel<true, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
-    else if (bf16) e = launch_kernel<true, false, kBnFloat, __nv_bfloat16>(ma, mb, p, dev, a.stream);
-    else if (a.out_dtype == DGA_F32) e = launch_kernel<false, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
-    else e = launch_kernel<false, false, kBnFloat, __half>(ma, mb, p, dev, a.stream);
+    if (i8) e = launch_kernel<kFmtBF16, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream);
+    else if (tf32 && pair) e = launch_pair_kernel<kFmtTF32, float>(ma, mb, p, dev, a.stream);
+    else if (tf32) e = launch_kernel<kFmtTF32, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
+    else if (pair && bf16 && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtBF16, float>(ma, mb, p, dev, a.stream);
+    else if (pair && bf16) e = launch_pair_kernel<kFmtBF16, __nv_bfloat16>(ma, mb, p, dev, a.stream);
+    else if (pair && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtF16, float>(ma, mb, p, dev, a.stream);
+    else if (pair) e = launch_pair_kernel<kFmtF16, __half>(ma, mb, p, dev, a.stream);
+    else if (bf16 && a.out_dtype == DGA_F32) e = launch_kernel<kFmtBF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
+    else if (bf16) e = launch_kernel<kFmtBF16, false, kBnFloat, __nv_bfloat16>(ma, mb, p, dev, a.stream);
+    else if (a.out_dtype == DGA_F32) e = launch_kernel<kFmtF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
+    else e = launch_kernel<kFmtF16, false, kBnFloat, __half>(ma, mb, p, dev, a.stream);
     if (e == cudaSuccess) ++*launches;
     return e;
 }

@@ -133,15 +133,31 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem], kind::f16 (bf16 or fp16 inputs), one CTA.
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                           uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+// Operand formats of the instruction descriptor (A and B alike): kind::f16
+// takes fp16 or bf16, kind::tf32 takes fp32 storage read as TF32.
+enum : uint32_t { kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2 };
+
+// D[tmem] (+)= A[smem] * B[smem], one CTA: kind::f16 for 16-bit operands,
+// kind::tf32 for fp32 operands (each K step is 32 bytes of a row either way:
+// 16 elements of 2 bytes or 8 of 4).
+template <uint32_t kFmt>
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    if constexpr (kFmt == kFmtTF32) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
 }
 
 // Arrive (once) on `bar` when every tcgen05 operation this thread issued so
@@ -209,13 +225,12 @@ __device__ __forceinline__ uint64_t smem_desc_mnmajor_sw128(uint32_t saddr, uint
     return d;
 }
 
-// Instruction descriptor for kind::f16:
+// Instruction descriptor for kind::f16 and kind::tf32:
 //   bits 4-5 D format (1 = f32), bits 7-9 A format, bits 10-12 B format
-//   (0 = f16, 1 = bf16), bit 15/16 A/B major (0 = K-major),
-//   bits 17-22 N >> 3, bits 24-28 M >> 4.
-__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, uint32_t m, uint32_t n) {
-    return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-           ((n >> 3) << 17) | ((m >> 4) << 24);
+//   (kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2), bit 15/16 A/B major
+//   (0 = K-major), bits 17-22 N >> 3, bits 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t idesc_mma(uint32_t fmt, uint32_t m, uint32_t n) {
+    return (1u << 4) | (fmt << 7) | (fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 // The same with A and/or B MN-major (bits 15 and 16 set).
 __host__ __device__ constexpr uint32_t idesc_major(uint32_t idesc, uint32_t a_mn, uint32_t b_mn) {
@@ -287,14 +302,24 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
 }
 
 // Pair MMA (M = 256 across the two CTAs), issued by the even-ranked CTA.
-__device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                                uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+template <uint32_t kFmt>
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    if constexpr (kFmt == kFmtTF32) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    }
 }
 
 // Arrive once on the mbarrier at this shared-memory offset in every CTA of

@@ -11,6 +11,12 @@ drawing A, then B, then C):
 * N(0, sigma) as bf16:   ``(torch.randn(shape) * sigma).to(torch.bfloat16)``
   (float32 draw, round-to-nearest-even to bf16)
 * int8 uniform [-128, 127]: ``torch.randint(-128, 128, shape, dtype=int8)``
+* CSR sparse matrices (:func:`csr_powerlaw`): row lengths from a Pareto law
+  (a few rows thousands of entries long, most a few dozen, some empty),
+  column indices near the row's diagonal position, values uniform[-1, 1);
+  x uniform[-1, 1).  The sparse-matrix sections of "AI Programming: Matrix
+  Product" give no sizes; the structure follows their remark that row lengths
+  can differ a lot.
 
 The workloads are the synthetic square and skinny shapes that the pages
 measure ("Matrix multiplication: arithmetic intensity, tiling and Tensor
@@ -23,12 +29,13 @@ from dataclasses import dataclass, field
 
 import torch
 
-# dtype / layout codes shared with the C ABI (values fixed by include/dga.h)
-F32, BF16, F16, I8, I32 = 0, 1, 2, 3, 4
+# dtype / layout codes shared with the C ABI (values fixed by include/dga.h);
+# TF32 operands are fp32 in memory
+F32, BF16, F16, I8, I32, TF32 = 0, 1, 2, 3, 4, 5
 ROW_MAJOR, COL_MAJOR = 0, 1
 
 TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16, F16: torch.float16,
-               I8: torch.int8, I32: torch.int32}
+               I8: torch.int8, I32: torch.int32, TF32: torch.float32}
 
 
 @dataclass(frozen=True)
@@ -47,7 +54,8 @@ class Workload:
     dist_c: tuple = ("uniform",)
     seed: int = 0
     note: str = field(default="", compare=False)
-    # "gemm": one C <- alpha*A*B + beta*C.  "fc": one fully-connected layer
+    # "gemm": one C <- alpha*A*B + beta*C.  "spmv": y <- alpha*A*x + beta*y
+    # for a CSR matrix of M rows and N columns (csr_powerlaw).  "fc": one fully-connected layer
     # step with batch M, N outputs and K inputs -- forward Y = X W^T + b and
     # backward dX = G W, dW = G^T X, db = sum over the batch of G; dist_a
     # draws X, dist_b W and b, dist_c the output gradient G.
@@ -80,6 +88,16 @@ WORKLOADS = {
     "bf16_8192_rowb": Workload("bf16_8192_rowb", BF16, F32, ROW_MAJOR, 8192, 8192, 8192, 1.0,
                                0.0, ("normal", 1.0), ("normal", 1.0),
                                note="BF16 in, FP32 out, M=N=K=8192, B row-major"),
+    "tf32_8192": Workload("tf32_8192", TF32, F32, COL_MAJOR, 8192, 8192, 8192, 1.0, 0.0,
+                          note="FP32 in memory multiplied as TF32 on the tensor cores, FP32 out, "
+                               "M=N=K=8192, B column-major, A and B uniform[-1,1)"),
+    "spmv_powerlaw": Workload("spmv_powerlaw", F32, F32, ROW_MAJOR, 4194304, 4194304, 0, 1.0, 0.0,
+                              kind="spmv",
+                              note="CSR SpMV y = A x, 4194304 x 4194304, Pareto(1.5) row lengths "
+                                   "(min 8, max 16384, 5% empty rows, mean ~23), columns within "
+                                   "+-4096 of the diagonal"),
+    "spmv_small": Workload("spmv_small", F32, F32, ROW_MAJOR, 20000, 30000, 0, 1.0, 0.0,
+                           kind="spmv", note="CSR SpMV, 20000 x 30000, same structure"),
     "fc_bf16_8192": Workload("fc_bf16_8192", BF16, BF16, COL_MAJOR, 8192, 8192, 8192, 1.0, 0.0,
                              ("normal", 1.0), ("normal", 0.02), ("normal", 1.0), kind="fc",
                              note="fully-connected layer step, bf16, batch 8192, 8192 -> 8192"),
@@ -129,3 +147,46 @@ def small_int_matrix(shape, dtype_code, gen, lo=-4, hi=4):
     """Integer-valued entries in [lo, hi], stored in ``dtype_code``."""
     t = torch.randint(lo, hi + 1, shape, generator=gen, dtype=torch.int32)
     return t.to(TORCH_DTYPE[dtype_code])
+
+
+# Structure of the synthetic CSR matrices.
+CSR_STRUCTURE = dict(pareto_alpha=1.5, min_len=8, max_len=16384, empty_frac=0.05, window=4096)
+
+
+def csr_powerlaw(rows, cols, gen, device="cpu", pareto_alpha=1.5, min_len=8, max_len=16384,
+                 empty_frac=0.05, window=4096):
+    """A seeded synthetic CSR matrix: (row_offsets int32 [rows + 1],
+    column_indices int32 [nnz], values float32 [nnz]).
+
+    Row lengths: floor(min_len * u^(-1/pareto_alpha)) capped at max_len, u
+    uniform in (0, 1] (a Pareto law: mean about 3 * min_len for alpha 1.5),
+    and a fraction empty_frac of rows set empty.  Columns: row i's entries
+    sit at (i * cols // rows + offset) mod cols, offset uniform in
+    [-window, window] (unsorted, repeats possible).  Values uniform[-1, 1).
+    Draw order: lengths, empty flags, column offsets, values."""
+    u = 1.0 - torch.rand(rows, generator=gen, device=device, dtype=torch.float64)
+    lengths = torch.floor(min_len * u.pow(-1.0 / pareto_alpha)).clamp_(max=max_len).to(torch.int64)
+    empty = torch.rand(rows, generator=gen, device=device) < empty_frac
+    lengths[empty] = 0
+    offsets = torch.zeros(rows + 1, dtype=torch.int64, device=device)
+    offsets[1:] = torch.cumsum(lengths, 0)
+    nnz = int(offsets[-1])
+    if nnz >= 2 ** 31:
+        raise ValueError("too many entries for int32 offsets")
+    row_of = torch.repeat_interleave(torch.arange(rows, device=device), lengths)
+    off = torch.randint(-window, window + 1, (nnz,), generator=gen, device=device)
+    cols_idx = torch.remainder(row_of * cols // rows + off, cols).to(torch.int32)
+    del row_of, off
+    values = torch.rand(nnz, generator=gen, device=device) * 2 - 1
+    return offsets.to(torch.int32), cols_idx, values
+
+
+def make_csr_inputs(w: Workload, seed: int | None = None, device="cpu"):
+    """(row_offsets, column_indices, values, x, y) for an "spmv" workload;
+    y is drawn only when beta != 0."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed if seed is None else seed)
+    offs, cols, vals = csr_powerlaw(w.M, w.N, gen, device, **CSR_STRUCTURE)
+    x = torch.rand(w.N, generator=gen, device=device) * 2 - 1
+    y = torch.rand(w.M, generator=gen, device=device) * 2 - 1 if w.beta != 0 else None
+    return offs, cols, vals, x, y

@@ -45,8 +45,16 @@ typedef struct CUstream_st* dga_stream_t;
  *   (DGA_F16, DGA_F32)    fp16 inputs, fp32 accumulate, fp32 output
  *   (DGA_F16, DGA_F16)    fp16 inputs, fp32 accumulate, fp16 output (nearest-even)
  *   (DGA_I8, DGA_I32)     int8 inputs, exact integer products and sums, int32
- *                         output; alpha*sum + beta*c is reduced mod 2^32.      */
-typedef enum { DGA_F32 = 0, DGA_BF16 = 1, DGA_F16 = 2, DGA_I8 = 3, DGA_I32 = 4 } dga_dtype;
+ *                         output; alpha*sum + beta*c is reduced mod 2^32.
+ *   (DGA_TF32, DGA_F32)   opt-in, lossy: A and B are fp32 in memory, but the
+ *                         tensor cores form each product from operands kept
+ *                         to 10 fraction bits (TF32, "Matrix multiplication:
+ *                         arithmetic intensity, tiling and Tensor Core",
+ *                         sections 5.5 and 5.7), accumulating in fp32; each
+ *                         product may be off by up to 2^-9 of its magnitude.
+ *                         Never chosen for DGA_F32 inputs.  alpha, beta, C
+ *                         and the bias are fp32 as for DGA_F32.            */
+typedef enum { DGA_F32 = 0, DGA_BF16 = 1, DGA_F16 = 2, DGA_I8 = 3, DGA_I32 = 4, DGA_TF32 = 5 } dga_dtype;
 
 /* Layout of B only; A and C are always row-major.
  *   DGA_ROW_MAJOR: B(k, j) = B[k*ldb + j], ldb >= max(1, N)
@@ -59,7 +67,8 @@ typedef enum { DGA_ROW_MAJOR = 0, DGA_COL_MAJOR = 1 } dga_layout;
  *   GENERIC  any dtype pair, any layout, alignment or leading dimension
  *   SIMT     FP32 register-tiled FFMA kernel (F32 -> F32)
  *   TCGEN05  5th-generation tensor cores, TMA + mbarrier pipeline, TMEM
- *            accumulators (BF16/F16 inputs; INT8 through exact bf16 encoding)
+ *            accumulators (BF16/F16 inputs, TF32 inputs; INT8 through exact
+ *            bf16 encoding)
  *   SKINNY   bandwidth-bound kernel for M <= 16 with column-major B
  *            (decode-shaped X * W^T; BF16/F16 inputs)                          */
 typedef enum {
@@ -84,6 +93,7 @@ typedef enum {
 #define DGA_ERR_WORKSPACE 5       /* workspace_bytes < dga_gemm_workspace_size(...)     */
 #define DGA_ERR_OVERLAP 6         /* C overlaps A or B                                  */
 #define DGA_ERR_DEVICE 7          /* current device is not sm_103 (GB300)               */
+#define DGA_ERR_BAD_INDEX 8       /* a CSR index was out of range (dga_sync_status only) */
 
 /*
  * dga_gemm -- C <- alpha*A*B + beta*C on `stream`, path chosen automatically.
@@ -92,7 +102,7 @@ typedef enum {
  *   layout_b             DGA_ROW_MAJOR or DGA_COL_MAJOR (B only)
  *   M, N, K              sizes, >= 0
  *   alpha, beta          HOST pointers to the scalars: float for floating
- *                        point inputs, int32_t for DGA_I8 inputs.  beta == 0:
+ *                        point inputs (TF32 included), int32_t for DGA_I8 inputs.  beta == 0:
  *                        C is not read (NaN or Inf there does not propagate).
  *                        alpha == 0 or K == 0: A and B are not read.
  *   A, lda               device pointer, A(i, k) = A[i*lda + k], lda >= max(1, K)
@@ -101,8 +111,8 @@ typedef enum {
  *   workspace            device scratch of at least workspace_bytes, or NULL
  *   workspace_bytes      bytes at `workspace`.  The tensor-core path needs
  *                        dga_gemm_workspace_size() bytes when it repacks
- *                        operands (INT8 inputs, row-major B, leading
- *                        dimensions TMA cannot express) and fails with
+ *                        operands (INT8 inputs; TF32 inputs with a row-major
+ *                        B; leading dimensions TMA cannot express) and fails with
  *                        DGA_ERR_WORKSPACE without them.  The FP32 SIMT path
  *                        uses workspace only if given enough: then the tiles
  *                        of its last, partial wave are split along K (faster
@@ -199,8 +209,9 @@ int dga_last_path(void);
 int dga_last_launch_count(void);
 
 /* Synchronises `stream`, then reads and clears the device status words the
- * kernels write when one of their bounded waits expires.  Returns DGA_OK,
- * DGA_ERR_DEVICE_TIMEOUT, or DGA_ERR_CUDA when the synchronisation failed. */
+ * kernels write when one of their bounded waits expires or (SpMV) when the
+ * CSR arrays were malformed.  Returns DGA_OK, DGA_ERR_DEVICE_TIMEOUT,
+ * DGA_ERR_BAD_INDEX, or DGA_ERR_CUDA when the synchronisation failed. */
 int dga_sync_status(dga_stream_t stream);
 
 /* Failure-detection self-test.  Enqueues one small kernel that waits on an
@@ -250,6 +261,47 @@ int dga_gemm_i8_noalloc(dga_layout layout_b, int64_t M, int64_t N, int64_t K,
                         const int32_t* alpha, const int8_t* A, int64_t lda,
                         const int8_t* B, int64_t ldb, const int32_t* beta,
                         int32_t* C, int64_t ldc, dga_stream_t stream);
+
+/*
+ * dga_spmv_csr -- y <- alpha * A * x + beta * y for a sparse rows x cols
+ * matrix A in CSR form: the SpMV of "AI Programming: Matrix Product",
+ * sections "CSR" and "SpMV".  Row i holds the entries p in the half-open
+ * interval [row_offsets[i], row_offsets[i+1]), entry p being values[p] in
+ * column column_indices[p]; y[i] gets the sum over those p of
+ * values[p] * x[column_indices[p]] (fp32 products and sums, any order within
+ * the tolerance 1e-4 * sum |a x| of the result; the order is fixed, so
+ * results repeat bit for bit).  Entries may be unsorted within a row and may
+ * repeat a column (they add up); rows may be empty.
+ *
+ *   rows, cols       >= 0 and < 2^31 - 1 (argument errors -1, -2)
+ *   nnz              number of entries, 0 <= nnz < 2^31 (-3); must equal
+ *                    row_offsets[rows]
+ *   row_offsets      device, rows + 1 int32, row_offsets[0] = 0, nondecreasing (-4)
+ *   column_indices   device, nnz int32 in [0, cols) (-5)
+ *   values           device, nnz float (-6)
+ *   alpha, beta      HOST pointers to float (-7, -9).  beta == 0: y is not
+ *                    read.  alpha == 0 or nnz == 0: A and x are not read.
+ *   x                device, cols float (-8)
+ *   y                device, rows float, in/out (-10); must not overlap the
+ *                    other arrays (DGA_ERR_OVERLAP)
+ *   workspace        device scratch of dga_spmv_csr_workspace_size(rows, nnz)
+ *                    bytes (-11 if NULL with workspace_bytes > 0,
+ *                    DGA_ERR_WORKSPACE if smaller): one row index and one
+ *                    partial sum per CTA, for rows that cross CTAs
+ * Work is split evenly over rows + nnz whatever the row lengths.  Malformed
+ * arrays never cause an access outside them: out-of-range column indices and
+ * offsets are skipped or clamped and the next dga_sync_status() returns
+ * DGA_ERR_BAD_INDEX.  Enqueued on `stream`; 2 kernel launches (1 when no
+ * entry is read).
+ */
+int dga_spmv_csr(int64_t rows, int64_t cols, int64_t nnz, const int32_t* row_offsets,
+                 const int32_t* column_indices, const float* values, const float* alpha,
+                 const float* x, const float* beta, float* y, void* workspace,
+                 size_t workspace_bytes, dga_stream_t stream);
+
+/* Bytes of workspace dga_spmv_csr needs for rows and nnz on the current device
+ * (152 SMs assumed when no device can be queried); 0 for rows <= 0. */
+size_t dga_spmv_csr_workspace_size(int64_t rows, int64_t nnz);
 
 /* Library version: major*10000 + minor*100 + patch. */
 int dga_version(void);

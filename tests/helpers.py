@@ -51,8 +51,9 @@ def run_gpu(path, in_dtype, out_dtype, layout_b, A, B, C, alpha, beta, lda=None,
     ws_bytes = dga.dga_gemm_workspace_size(in_dtype, out_dtype, layout_b, M, N, K, lda, ldb, ldc,
                                            path)
     # the size query assumes aligned pointers; packing never needs more than
-    # one M x K and one N x K bf16 copy (plus alignment)
-    ws_bytes = max(ws_bytes, 2 * (M + N) * ((K + 7) // 8 * 8) + 1024)
+    # one M x K and one N x K copy of 16-bit (or, for TF32, 32-bit) elements,
+    # plus alignment
+    ws_bytes = max(ws_bytes, 4 * (M + N) * ((K + 7) // 8 * 8) + 1024)
     if not workspace:
         ws_bytes = 0
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)

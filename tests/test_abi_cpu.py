@@ -61,6 +61,9 @@ def _call(**over):
     (dict(workspace=None, workspace_bytes=16), -15), (dict(path=9), -17),
     (dict(in_dtype=gen.F32, out_dtype=gen.BF16), dga.ERR_UNSUPPORTED),
     (dict(in_dtype=gen.I8, out_dtype=gen.F32), dga.ERR_UNSUPPORTED),
+    (dict(in_dtype=gen.TF32, out_dtype=gen.BF16), dga.ERR_UNSUPPORTED),
+    (dict(in_dtype=gen.F32, out_dtype=gen.TF32), dga.ERR_UNSUPPORTED),
+    (dict(in_dtype=6, out_dtype=gen.F32), dga.ERR_UNSUPPORTED),
     (dict(layout_b=5), dga.ERR_UNSUPPORTED),
     (dict(C=0x1004), dga.ERR_OVERLAP),
 ])
@@ -102,6 +105,15 @@ def test_workspace_size_query(lib):
                                        513, 512, dga.PATH_TCGEN05) >= 512 * 104 * 2
     assert dga.dga_gemm_workspace_size(gen.F32, gen.F32, gen.ROW_MAJOR, 64, 64, 64, 64, 64, 64,
                                        dga.PATH_SIMT) == 0
+    # TF32 reads K-major only: column-major B in place, a row-major B is
+    # transposed into the workspace as fp32 (4 bytes x N x K4)
+    w = W["tf32_8192"]
+    assert dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
+                                       w.K, w.N, dga.PATH_AUTO) == 0
+    assert dga.dga_gemm_workspace_size(gen.TF32, gen.F32, gen.ROW_MAJOR, 256, 512, 100, 100,
+                                       512, 512, dga.PATH_TCGEN05) >= 512 * 100 * 4
+    assert dga.dga_gemm_workspace_size(gen.TF32, gen.F32, gen.COL_MAJOR, 256, 512, 100, 102,
+                                       100, 512, dga.PATH_TCGEN05) >= 256 * 100 * 4
 
 
 def test_binding_layout_from_strides():
@@ -189,3 +201,39 @@ def test_binding_general_layouts():
     assert dga._layout_of(torch.empty(10, 14)[:, :6], "W") == (gen.ROW_MAJOR, 14)
     with pytest.raises(ValueError):
         dga._layout_of(torch.empty(10, 14)[::2, ::2], "W")
+
+
+def _spmv(**over):
+    import ctypes
+    one = ctypes.c_float(1.0)
+    args = dict(rows=4, cols=4, nnz=8, row_offsets=0x1000, column_indices=0x2000, values=0x3000,
+                alpha=ctypes.byref(one), x=0x4000, beta=ctypes.byref(one), y=0x5000,
+                workspace=0x6000, workspace_bytes=1 << 20, stream=None)
+    args.update(over)
+    return dga.dga_spmv_csr(*args.values())
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(rows=-1), -1), (dict(cols=-1), -2), (dict(nnz=-1), -3), (dict(nnz=1 << 31), -3),
+    (dict(alpha=None), -7), (dict(beta=None), -9), (dict(row_offsets=None), -4),
+    (dict(column_indices=None), -5), (dict(values=None), -6), (dict(x=None), -8),
+    (dict(y=None), -10), (dict(workspace=None), -11),
+    (dict(y=0x4008), dga.ERR_OVERLAP), (dict(y=0x0ffc), dga.ERR_OVERLAP),
+])
+def test_spmv_argument_errors(lib, over, code):
+    assert _spmv(**over) == code
+
+
+def test_spmv_quick_returns_and_workspace(lib):
+    import ctypes
+    zero = ctypes.c_float(0.0)
+    # no rows: nothing to do, nothing touched
+    assert _spmv(rows=0, row_offsets=None, y=None) == dga.OK
+    # alpha == 0 reads neither A nor x: their pointers may be NULL (the call
+    # then needs the device, absent here, so it stops at the device check)
+    st = _spmv(alpha=ctypes.byref(zero), column_indices=None, values=None, x=None)
+    assert st in (dga.ERR_CUDA, dga.ERR_DEVICE)
+    # one row index and one float per CTA, at most 8 CTAs per SM
+    ws = dga.dga_spmv_csr_workspace_size(1 << 22, 1 << 26)
+    assert 8 * 152 * 8 <= ws <= 8 * 152 * 8 + 512
+    assert dga.dga_spmv_csr_workspace_size(0, 10) == 0

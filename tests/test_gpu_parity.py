@@ -172,11 +172,51 @@ def test_tc_int8_extreme_magnitudes():
     assert_exact(got, ref, gen.I32, "alternating")
 
 
+# ------------------------------------------------------------------- TF32 --
+#
+# fp32 operands multiplied as TF32 on the tensor cores (opt-in, lossy): the
+# oracle's reference is the exact fp32 product and its bound is widened for
+# operands kept to 10 fraction bits.
+
+TF32_SHAPES = [(128, 256, 32), (1, 1, 1), (129, 257, 65), (300, 520, 1000), (256, 512, 4096),
+               (1000, 300, 136), (128, 16, 4), (77, 91, 600)]
+
+
+@pytest.mark.parametrize("M,N,K", TF32_SHAPES)
+def test_tc_tf32(M, N, K):
+    check(T, gen.TF32, gen.F32, gen.COL_MAJOR, M, N, K, 1.0, 0.0, seed=M * 3 + K)
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 300, 264), (64, 1000, 520)])
+def test_tc_tf32_row_major_b_beta(M, N, K):
+    # a row-major B is transposed into the workspace (TF32 reads K-major only)
+    check(T, gen.TF32, gen.F32, gen.ROW_MAJOR, M, N, K, 1.5, 0.5, seed=N)
+
+
+def test_tc_tf32_unaligned():
+    check(T, gen.TF32, gen.F32, gen.COL_MAJOR, 150, 270, 99, 1.0, 0.0, lda=101, ldb=99)
+    check(T, gen.TF32, gen.F32, gen.COL_MAJOR, 150, 270, 128, 1.0, 0.0, offsets=(1, 3, 1))
+
+
+def test_tf32_is_opt_in():
+    # fp32 inputs never take the TF32 path; TF32 inputs go to the tensor cores
+    A, B, C = _mats(gen.F32, gen.F32, gen.COL_MAJOR, 256, 256, 256, 4)
+    run_gpu(dga.PATH_AUTO, gen.F32, gen.F32, gen.COL_MAJOR, A, B, C, 1, 0)
+    assert dga.dga_last_path() == S
+    run_gpu(dga.PATH_AUTO, gen.TF32, gen.F32, gen.COL_MAJOR, A, B, C, 1, 0)
+    assert dga.dga_last_path() == T
+    # the generic family accepts TF32 too (it multiplies exactly, within the bound)
+    check(GEN, gen.TF32, gen.F32, gen.ROW_MAJOR, 45, 71, 37, 1.25, -0.5, offsets=(1, 1, 1))
+
+
 # ----------------------------------------------------------------- skinny --
 
 @pytest.mark.parametrize("M,N,K", [(1, 8192, 8192), (8, 1000, 1024), (16, 96, 256), (3, 33, 72),
-                                   (9, 64, 8), (16, 40, 4104)])
+                                   (9, 64, 8), (16, 40, 4104), (5, 15000, 200),
+                                   (16, 20000, 136), (2, 152, 520), (16, 2432, 64)])
 def test_skinny(M, N, K):
+    # (5, 15000): 98-99 rows per CTA; (16, 20000): two waves of CTAs;
+    # (2, 152): one 16-row group per CTA on 9 CTAs; K % 256 != 0 tails
     check(K_, gen.BF16, gen.BF16, gen.COL_MAJOR, M, N, K, 1.0, 0.0, seed=M + N)
 
 
@@ -200,8 +240,12 @@ def test_generic_all_pairs(pair, layout):
 @pytest.mark.parametrize("path,in_dtype,out_dtype,layout", [
     (S, gen.F32, gen.F32, gen.ROW_MAJOR), (T, gen.BF16, gen.F32, gen.COL_MAJOR),
     (T, gen.BF16, gen.BF16, gen.ROW_MAJOR), (K_, gen.BF16, gen.BF16, gen.COL_MAJOR),
-    (GEN, gen.F32, gen.F32, gen.COL_MAJOR), (T, gen.F16, gen.F32, gen.COL_MAJOR)])
+    (GEN, gen.F32, gen.F32, gen.COL_MAJOR), (T, gen.F16, gen.F32, gen.COL_MAJOR),
+    (T, gen.TF32, gen.F32, gen.COL_MAJOR), (T, gen.TF32, gen.F32, gen.ROW_MAJOR),
+    (K_, gen.F16, gen.F32, gen.COL_MAJOR)])
 def test_small_integers_bit_exact(path, in_dtype, out_dtype, layout):
+    # small integers are exact in every input format (TF32 included: 10
+    # fraction bits) and every partial sum stays below 2^24
     M = 16 if path == K_ else 150
     N, K = 270, 520
     g = torch.Generator().manual_seed(11)
@@ -215,7 +259,8 @@ def test_small_integers_bit_exact(path, in_dtype, out_dtype, layout):
 
 @pytest.mark.parametrize("path,in_dtype,layout", [
     (S, gen.F32, gen.ROW_MAJOR), (T, gen.BF16, gen.COL_MAJOR), (T, gen.BF16, gen.ROW_MAJOR),
-    (GEN, gen.BF16, gen.COL_MAJOR), (K_, gen.BF16, gen.COL_MAJOR)])
+    (GEN, gen.BF16, gen.COL_MAJOR), (K_, gen.BF16, gen.COL_MAJOR), (T, gen.TF32, gen.COL_MAJOR),
+    (T, gen.TF32, gen.ROW_MAJOR)])
 def test_permutation_detects_transpose(path, in_dtype, layout):
     # A = P (a row selection), so C = B[rows]: exact, and any transposition of B fails
     M = 16 if path == K_ else 140
@@ -228,7 +273,14 @@ def test_permutation_detects_transpose(path, in_dtype, layout):
     out_dtype = gen.F32
     C = torch.zeros(M, N)
     got = run_gpu(path, in_dtype, out_dtype, layout, A, B, C, 1.0, 0.0)
-    assert torch.equal(got, Bkn[rows].float())
+    want = Bkn[rows].float()
+    if in_dtype == gen.TF32:
+        # one nonzero product per output: B's value as the tensor core keeps
+        # it, within 2^-10 of its magnitude (truncated or rounded)
+        assert (torch.abs(got - want) <= torch.abs(want) * 2.0 ** -10).all()
+        assert torch.equal(got == 0, want == 0)
+    else:
+        assert torch.equal(got, want)
 
 
 @pytest.mark.parametrize("path", [S, T, K_, GEN])
@@ -315,7 +367,8 @@ def _sample(M, N, n, seed):
 
 
 @pytest.mark.parametrize("name", ["fp32_4096", "bf16_8192", "skinny_m1", "skinny_m8",
-                                  "skinny_m16", "int8_ragged", "f16_8192", "bf16_8192_rowb"])
+                                  "skinny_m16", "int8_ragged", "f16_8192", "bf16_8192_rowb",
+                                  "tf32_8192"])
 def test_full_size_workload(name):
     import oracle
     w = gen.WORKLOADS[name]
@@ -323,7 +376,7 @@ def test_full_size_workload(name):
     dev = torch.device("cuda")
     Ad, Bd, Cd = A.to(dev), B.to(dev), C0.to(dev)
     Bview = Bd.t() if w.layout_b == gen.COL_MAJOR else Bd
-    dga.gemm(Ad, Bview, Cd, w.alpha, w.beta)
+    dga.gemm(Ad, Bview, Cd, w.alpha, w.beta, tf32=w.in_dtype == gen.TF32)
     torch.cuda.synchronize()
     got = Cd.cpu()
     ldb = w.K if w.layout_b == gen.COL_MAJOR else w.N
