@@ -737,6 +737,8 @@ def main():
             if ow.kind == "fc":
                 rf["paths"] = r.paths
                 rf["algorithmic_bytes"] = workload_accounting(ow)[1]
+            elif ow.kind == "spmv":
+                rf["path"] = "spmv"
             else:
                 rf["path"] = dga.PATH_NAMES[dga.dga_last_path()]
             if rf["bound"] == "tensor":

@@ -233,7 +233,7 @@ def test_spmv_quick_returns_and_workspace(lib):
     # then needs the device, absent here, so it stops at the device check)
     st = _spmv(alpha=ctypes.byref(zero), column_indices=None, values=None, x=None)
     assert st in (dga.ERR_CUDA, dga.ERR_DEVICE)
-    # one row index and one float per CTA, at most 8 CTAs per SM
+    # one row index and one float per warp: at most 8 CTAs of 8 warps per SM
     ws = dga.dga_spmv_csr_workspace_size(1 << 22, 1 << 26)
-    assert 8 * 152 * 8 <= ws <= 8 * 152 * 8 + 512
+    assert 8 * 8 * 152 * 8 <= ws <= 8 * 8 * 152 * 8 + 512
     assert dga.dga_spmv_csr_workspace_size(0, 10) == 0
