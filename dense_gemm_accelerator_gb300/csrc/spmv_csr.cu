@@ -71,6 +71,7 @@ struct SpParams {
     float alpha, beta;
     int64_t items;         // rows + nnz
     int64_t ctas;
+    int64_t sms;           // SMs of the device (for the block-to-share mapping)
     int32_t* carry_row;    // workspace: per CTA, the row its last partial sum belongs to
     float* carry_val;      //            and that partial sum
 };
@@ -78,6 +79,19 @@ struct SpParams {
 __device__ __forceinline__ void flag_bad() { atomicExch(&g_spmv_status, 1); }
 
 __device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Streamed arrays (values, column indices) are read once: keep them out of L1
+// so that L1 holds the x elements the gathers reuse.
+__device__ __forceinline__ int32_t ld_stream(const int32_t* q) {
+    int32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.b32 %0, [%1];" : "=r"(v) : "l"(q));
+    return v;
+}
+__device__ __forceinline__ float ld_stream(const float* q) {
+    float v;
+    asm volatile("ld.global.nc.L1::no_allocate.f32 %0, [%1];" : "=f"(v) : "l"(q));
+    return v;
+}
 
 // Loads the row ends of rows r + k (k = k0 + lane < k_end) into the warp's
 // window as offsets from the chunk's first nonzero z, clamped to [0, nz_max];
@@ -145,12 +159,20 @@ struct WarpSmem {
     int owned[32];                         // row ends among each lane's items
 };
 
-__global__ void __launch_bounds__(kThreads, 6) spmv_merge_kernel(SpParams p) {
+__global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
     __shared__ WarpSmem s_all[kThreads / 32];
     const int lane = threadIdx.x & 31;
     WarpSmem& sm = s_all[threadIdx.x >> 5];
     const int64_t warps = p.ctas * (kThreads / 32);
-    const int64_t w = static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5);
+    // Blocks b, b + sms, b + 2 sms, ... usually share an SM (one wave, placed
+    // round-robin): give them adjacent shares of the merge, so that the x
+    // elements their gathers touch overlap in that SM's L1.  Any mapping is
+    // correct (a permutation of the shares); this one is only faster.
+    // (b = q * sms + s maps to s * per_sm + q: a bijection when sms divides ctas)
+    const int64_t b = blockIdx.x;
+    const int64_t per_sm = p.ctas / p.sms;
+    const int64_t logical = p.ctas % p.sms == 0 ? (b % p.sms) * per_sm + b / p.sms : b;
+    const int64_t w = logical * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t d_end = (w + 1) * p.items / warps;
     int64_t r = warp_merge_search(p, w * p.items / warps);
     int64_t z = w * p.items / warps - r;
@@ -174,8 +196,8 @@ __global__ void __launch_bounds__(kThreads, 6) spmv_merge_kernel(SpParams p) {
             col[u] = -1;
             val[u] = 0.0f;
             if (k < nz_max) {
-                col[u] = __ldg(p.cidx + z + k);
-                val[u] = __ldg(p.vals + z + k);
+                col[u] = ld_stream(p.cidx + z + k);
+                val[u] = ld_stream(p.vals + z + k);
             }
         }
         // row end k sits at merge position k + (its end - z) of the chunk;
@@ -360,6 +382,7 @@ cudaError_t spmv_launch(int64_t rows, int64_t cols, int64_t nnz, const int32_t* 
     p.beta = beta;
     p.items = rows + nnz;
     p.ctas = spmv_ctas(p.items, dev.sm_count, merge_ctas_per_sm(dev));
+    p.sms = std::max(1, dev.sm_count);
     if (ws_bytes < spmv_workspace_size(rows, nnz, dev.sm_count)) return cudaErrorInvalidValue;
     uint8_t* w = static_cast<uint8_t*>(ws);
     p.carry_row = reinterpret_cast<int32_t*>(w);
