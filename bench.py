@@ -464,7 +464,13 @@ def source_of(w):
 
 def e2e_leg(w, steps, warmup, device):
     """Same metric through the public API with host buffers: every step copies
-    the inputs from pinned host memory, runs the GEMM and reads C back."""
+    its inputs from pinned host memory, runs the GEMM and reads C back to
+    pinned host memory.  The copies are pipelined the way a host-fed caller
+    would: device inputs are double-buffered, a copy-in stream moves step
+    i+1's A, B (and C) while the GEMM of step i runs on the compute stream, and
+    a copy-out stream returns step i's C; events keep every buffer's copy-in,
+    GEMM and copy-out in order.  The timed region starts before the first
+    copy-in and ends after the last copy-out."""
     import torch
 
     import dense_gemm_accelerator_gb300 as dga
@@ -472,42 +478,68 @@ def e2e_leg(w, steps, warmup, device):
     A, B, C = gen.make_inputs(w, with_c=w.beta != 0)
     hA, hB = A.pin_memory(), B.pin_memory()
     hC = C.pin_memory() if C is not None else None
-    out = torch.empty((w.M, w.N), dtype=gen.TORCH_DTYPE[w.out_dtype]).pin_memory()
-    dA = torch.empty_like(hA, device=device)
-    dB = torch.empty_like(hB, device=device)
-    dC = torch.empty((w.M, w.N), dtype=gen.TORCH_DTYPE[w.out_dtype], device=device)
-    stream = torch.cuda.current_stream()
+    odt = gen.TORCH_DTYPE[w.out_dtype]
+    out = [torch.empty((w.M, w.N), dtype=odt).pin_memory() for _ in range(2)]
+    dA = [torch.empty_like(hA, device=device) for _ in range(2)]
+    dB = [torch.empty_like(hB, device=device) for _ in range(2)]
+    dC = [torch.empty((w.M, w.N), dtype=odt, device=device) for _ in range(2)]
+    compute = torch.cuda.current_stream()
+    copy_in = torch.cuda.Stream(device=device)
+    copy_out = torch.cuda.Stream(device=device)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    gemm_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
-    def step():
-        dA.copy_(hA, non_blocking=True)
-        dB.copy_(hB, non_blocking=True)
-        if hC is not None:
-            dC.copy_(hC, non_blocking=True)
-        dga.gemm(dA, dB.t() if w.layout_b == gen.COL_MAJOR else dB, dC, w.alpha, w.beta,
-                 tf32=w.in_dtype == gen.TF32)
-        out.copy_(dC, non_blocking=True)
+    def step(i):
+        b = i % 2
+        with torch.cuda.stream(copy_in):
+            if used[b]:
+                copy_in.wait_event(out_done[b])  # step i-2 is done with buffer b
+            dA[b].copy_(hA, non_blocking=True)
+            dB[b].copy_(hB, non_blocking=True)
+            if hC is not None:
+                dC[b].copy_(hC, non_blocking=True)
+            in_ready[b].record(copy_in)
+        compute.wait_event(in_ready[b])
+        dga.gemm(dA[b], dB[b].t() if w.layout_b == gen.COL_MAJOR else dB[b], dC[b], w.alpha,
+                 w.beta, tf32=w.in_dtype == gen.TF32, stream=compute.cuda_stream)
+        gemm_done[b].record(compute)
+        with torch.cuda.stream(copy_out):
+            copy_out.wait_event(gemm_done[b])
+            out[b].copy_(dC[b], non_blocking=True)
+            out_done[b].record(copy_out)
+        used[b] = True
 
-    for _ in range(warmup):
-        step()
+    def run(n, first):
+        for i in range(n):
+            step(first + i)
+        for b in range(2):
+            if used[b]:
+                compute.wait_event(out_done[b])  # the region ends after the last copy-out
+
+    run(warmup, 0)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(steps):
-        step()
-    t1.record(stream)
+    t0.record(compute)
+    copy_in.wait_event(t0)  # no copy of the timed steps starts before t0
+    run(steps, warmup)
+    t1.record(compute)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
     fl, by = workload_accounting(w)
     h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size() + \
         (hC.numel() * hC.element_size() if hC is not None else 0)
-    d2h = out.numel() * out.element_size()
+    d2h = out[0].numel() * out[0].element_size()
     if w.name.startswith("skinny"):
         val, unit = by / (ms * 1e-3) / 1e9, "GB/s"
     else:
         val, unit = fl / (ms * 1e-3) / 1e12, ("TOPS" if w.in_dtype == gen.I8 else "TFLOPS")
     return {"value": val, "unit": unit, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h,
+            "pipeline": "double-buffered: copy-in of step i+1 and copy-out of step i overlap "
+                        "the GEMM of step i (separate copy streams, event-ordered)"}
 
 
 # ------------------------------------------------------- CPU oracle timing --
