@@ -457,6 +457,9 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
 constexpr int kPairStages = 6;
 constexpr int kPairBN = 256;
 
+// kSquares: epilogue staging squares, 4 for floating point (one per epilogue
+// warp), 8 for INT8 (16 epilogue warps store in two rounds).
+template <int kSquares>
 struct PairSmem {
     static constexpr uint32_t kABytes = 128 * BK * 2;
     static constexpr uint32_t kBBytes = (kPairBN / 2) * BK * 2;
@@ -467,15 +470,16 @@ struct PairSmem {
     static constexpr uint32_t kBarBytes = (2 * kPairStages + 5) * 8 + 16;
     static constexpr uint32_t kEpiOffset = (kBarOffset + kBarBytes + 127) / 128 * 128;
     static constexpr uint32_t kEpiWarpBytes = 32 * 33 * 4;
-    static constexpr uint32_t kTotal = kEpiOffset + 4 * kEpiWarpBytes;
+    static constexpr uint32_t kTotal = kEpiOffset + kSquares * kEpiWarpBytes;
     static constexpr uint32_t kLaunchBytes = kTotal + 1024;
 };
 
-template <uint32_t kFmt, typename TOut>
-__global__ void __launch_bounds__(192, 1)
+template <uint32_t kFmt, bool kI8, typename TOut>
+__global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
     tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, TcParams p) {
-    using S = PairSmem;
+    constexpr int kEpiWarps = kI8 ? 16 : 4;
+    using S = PairSmem<kI8 ? 8 : 4>;
     constexpr uint32_t kTmemCols = 2 * kPairBN;  // two accumulators
     constexpr uint32_t kIdesc = idesc_mma(kFmt, 256, kPairBN);
     constexpr int kKElems = k_per_stage(kFmt);
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 2 * 4);  // one lane of each epilogue warp of both CTAs
+            mbar_init(&acc_empty[b], 2 * kEpiWarps);  // one lane of each epilogue warp of both CTAs
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -572,37 +576,46 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t a_step = p.a_mn ? kStepMnMajor : kStepKMajor;
             const uint32_t b_step = p.b_mn ? kStepMnMajor : kStepKMajor;
             bool ok = true;
+            // INT8: the K loop of a tile is cut into exact 1024-deep chunks, each
+            // in its own accumulator (see the single-CTA kernel); otherwise one
+            // chunk spans the whole K loop
+            const uint32_t n_chunks = kI8 ? (p.num_kb + kI8ChunkBlocks - 1) / kI8ChunkBlocks : 1;
             for (uint32_t t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
-                if (!mbar_wait_bounded<true>(&acc_empty[acc], acc_phase ^ 1, abort_flag,
-                                             kWaitLimitNs)) {
-                    record_failure(kRoleMma, abort_flag);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * kPairBN;
-                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
-                    if (!mbar_wait_bounded<true>(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                for (uint32_t ch = 0; ok && ch < n_chunks; ++ch) {
+                    if (!mbar_wait_bounded<true>(&acc_empty[acc], acc_phase ^ 1, abort_flag,
+                                                 kWaitLimitNs)) {
                         record_failure(kRoleMma, abort_flag);
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + stage * S::kStageBytes);
-                    const uint64_t a_desc = p.a_mn ? smem_desc_mnmajor_sw128(a_addr, kMnBoxBytes)
-                                                   : smem_desc_kmajor_sw128(a_addr);
-                    const uint64_t b_desc =
-                        p.b_mn ? smem_desc_mnmajor_sw128(a_addr + S::kABytes, kMnBoxBytes)
-                               : smem_desc_kmajor_sw128(a_addr + S::kABytes);
+                    const uint32_t d_tmem = tmem_base + acc * kPairBN;
+                    const uint32_t kb_begin = kI8 ? ch * kI8ChunkBlocks : 0;
+                    const uint32_t kb_end = kI8 ? min(p.num_kb, kb_begin + kI8ChunkBlocks) : p.num_kb;
+                    for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
+                        if (!mbar_wait_bounded<true>(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                            record_failure(kRoleMma, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(smem + stage * S::kStageBytes);
+                        const uint64_t a_desc = p.a_mn ? smem_desc_mnmajor_sw128(a_addr, kMnBoxBytes)
+                                                       : smem_desc_kmajor_sw128(a_addr);
+                        const uint64_t b_desc =
+                            p.b_mn ? smem_desc_mnmajor_sw128(a_addr + S::kABytes, kMnBoxBytes)
+                                   : smem_desc_kmajor_sw128(a_addr + S::kABytes);
 #pragma unroll
-                    for (int k = 0; k < BK / UK; ++k)
-                        tc_mma_pair<kFmt>(d_tmem, a_desc + a_step * k, b_desc + b_step * k, idesc,
-                                        (kb > 0 || k > 0) ? 1u : 0u);
-                    tc_commit_pair_multicast(&empty[stage], kBothCtas);
-                    if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+                        for (int k = 0; k < BK / UK; ++k)
+                            tc_mma_pair<kFmt>(d_tmem, a_desc + a_step * k, b_desc + b_step * k,
+                                              idesc, (kb > kb_begin || k > 0) ? 1u : 0u);
+                        tc_commit_pair_multicast(&empty[stage], kBothCtas);
+                        if (++stage == kPairStages) { stage = 0; phase ^= 1; }
+                    }
+                    if (!ok) break;
+                    tc_commit_pair_multicast(&acc_full[acc], kBothCtas);
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1; }
                 }
-                if (!ok) break;
-                tc_commit_pair_multicast(&acc_full[acc], kBothCtas);
-                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
             }
             // every pair MMA issued so far must finish before TMEM is freed
             tc_commit_pair_multicast(drain, 0x1);
@@ -614,29 +627,79 @@ __global__ void __launch_bounds__(192, 1)
         const int ew = warp - 2;
         const int quarter = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        uint32_t* stage = reinterpret_cast<uint32_t*>(smem + S::kEpiOffset + ew * S::kEpiWarpBytes);
+        uint32_t* stage =
+            reinterpret_cast<uint32_t*>(smem + S::kEpiOffset + (ew & 7) * S::kEpiWarpBytes);
+        // INT8: four warps per lane quarter, each owning a quarter of the columns
+        const int col_group = kI8 ? (ew >> 2) : 0;
+        constexpr int kColsPerWarp = kI8 ? kPairBN / 4 : kPairBN;
         uint32_t acc = 0, acc_phase = 0;
-        for (uint32_t t = cluster_id; t < p.num_tiles; t += n_clusters) {
+        bool ok = true;
+        for (uint32_t t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
             uint32_t tm, tn;
             tile_coords(t, p, tm, tn);
             const int64_t row_base = static_cast<int64_t>(tm) * 256 + rank * 128 + quarter * 32;
-            const int64_t col0 = static_cast<int64_t>(tn) * kPairBN;
-            if (!mbar_wait_bounded<true>(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
-                record_failure(kRoleEpilogue, abort_flag);
-                break;
-            }
-            tc_fence_after();
+            const int64_t col0 = static_cast<int64_t>(tn) * kPairBN + col_group * kColsPerWarp;
+            if constexpr (!kI8) {
+                if (!mbar_wait_bounded<true>(&acc_full[acc], acc_phase, abort_flag, kWaitLimitNs)) {
+                    record_failure(kRoleEpilogue, abort_flag);
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll 1
-            for (int c = 0; c < kPairBN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + c * 32, r);
-                tmem_ld_wait();
-                store_block_staged<TOut>(p, stage, lane, row_base, col0 + c * 32, r);
+                for (int c = 0; c < kPairBN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + c * 32, r);
+                    tmem_ld_wait();
+                    store_block_staged<TOut>(p, stage, lane, row_base, col0 + c * 32, r);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&acc_empty[acc]), 0));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+            } else {
+                // each chunk's exact fp32 sums become int32 and add up (wrapping)
+                int32_t sum[kColsPerWarp];
+#pragma unroll
+                for (int j = 0; j < kColsPerWarp; ++j) sum[j] = 0;
+                const uint32_t n_chunks = (p.num_kb + kI8ChunkBlocks - 1) / kI8ChunkBlocks;
+                for (uint32_t ch = 0; ch < n_chunks; ++ch) {
+                    if (!mbar_wait_bounded<true>(&acc_full[acc], acc_phase, abort_flag,
+                                                 kWaitLimitNs)) {
+                        record_failure(kRoleEpilogue, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < kColsPerWarp / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN +
+                                               col_group * kColsPerWarp + c * 32, r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            sum[c * 32 + j] = static_cast<int32_t>(
+                                static_cast<uint32_t>(sum[c * 32 + j]) +
+                                static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j]))));
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&acc_empty[acc]), 0));
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+                }
+                if (!ok) break;
+                // 16 warps, 8 staging squares: warps 0-7 store first, then 8-15
+                // (named barrier 1 over this CTA's 512 epilogue threads)
+                for (int round = 0; round < 2; ++round) {
+                    if ((ew >> 3) == round) {
+#pragma unroll
+                        for (int c = 0; c < kColsPerWarp / 32; ++c)
+                            store_block_staged_i32(p, stage, lane, row_base, col0 + c * 32,
+                                                   &sum[c * 32]);
+                    }
+                    asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&acc_empty[acc]), 0));
-            if (++acc == 2) { acc = 0; acc_phase ^= 1; }
         }
     }
 
@@ -945,14 +1008,14 @@ cudaError_t launch_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const Tc
 
 // Clusters of two that fit at once on this device (queried once per kernel).
 template <typename Kern>
-int max_pair_clusters(Kern kern, int smem, const DeviceInfo& dev) {
+int max_pair_clusters(Kern kern, int smem, int threads, const DeviceInfo& dev) {
     static int cached[64] = {};
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     if (dev.ordinal >= 0 && dev.ordinal < 64 && cached[dev.ordinal] > 0) return cached[dev.ordinal];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (dev.sm_count / 2));
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -970,18 +1033,19 @@ int max_pair_clusters(Kern kern, int smem, const DeviceInfo& dev) {
     return n;
 }
 
-template <uint32_t kFmt, typename TOut>
+template <uint32_t kFmt, bool kI8, typename TOut>
 cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
                                const DeviceInfo& dev, cudaStream_t s) {
-    auto kern = tc_gemm_pair_kernel<kFmt, TOut>;
-    const int smem = static_cast<int>(PairSmem::kLaunchBytes);
+    auto kern = tc_gemm_pair_kernel<kFmt, kI8, TOut>;
+    const int smem = static_cast<int>(PairSmem<kI8 ? 8 : 4>::kLaunchBytes);
+    const int threads = kI8 ? 576 : 192;
     if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int clusters = std::min<int64_t>(p.num_tiles, max_pair_clusters(kern, smem, dev));
+    const int clusters = std::min<int64_t>(p.num_tiles, max_pair_clusters(kern, smem, threads, dev));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * std::max(clusters, 1)));
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1087,8 +1151,10 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     }
     // Floating point with more than one 128-row tile: the CTA-pair kernel
     // (256 x 256 tiles, each CTA loading half of B).
-    const bool pair = !i8 && a.M > BM;
-    const int BN = i8 ? kBnI8 : (pair ? kPairBN : kBnFloat);
+    // More than one 128-row tile: the CTA-pair kernel (256 x 256 tiles, each
+    // CTA loading half of B), INT8 included (its chunked exact accumulation).
+    const bool pair = a.M > BM;
+    const int BN = pair ? kPairBN : (i8 ? kBnI8 : kBnFloat);
     CUtensorMap ma, mb;
     e = pl.a_mn ? make_mnmajor_map(&ma, A, a.M, a.K, lda, fmt)
                 : make_kmajor_map(&ma, A, a.M, a.K, lda, BM, fmt);
@@ -1117,13 +1183,14 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     p.num_kb = static_cast<uint32_t>((a.K + k_per_stage(fmt) - 1) / k_per_stage(fmt));
     p.group_m = raster_group_rows(a.K, p.tiles_m, tile_m);
 
-    if (i8) e = launch_kernel<kFmtBF16, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream);
-    else if (tf32 && pair) e = launch_pair_kernel<kFmtTF32, float>(ma, mb, p, dev, a.stream);
+    if (i8 && pair) e = launch_pair_kernel<kFmtBF16, true, int32_t>(ma, mb, p, dev, a.stream);
+    else if (i8) e = launch_kernel<kFmtBF16, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream);
+    else if (tf32 && pair) e = launch_pair_kernel<kFmtTF32, false, float>(ma, mb, p, dev, a.stream);
     else if (tf32) e = launch_kernel<kFmtTF32, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
-    else if (pair && bf16 && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtBF16, float>(ma, mb, p, dev, a.stream);
-    else if (pair && bf16) e = launch_pair_kernel<kFmtBF16, __nv_bfloat16>(ma, mb, p, dev, a.stream);
-    else if (pair && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtF16, float>(ma, mb, p, dev, a.stream);
-    else if (pair) e = launch_pair_kernel<kFmtF16, __half>(ma, mb, p, dev, a.stream);
+    else if (pair && bf16 && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtBF16, false, float>(ma, mb, p, dev, a.stream);
+    else if (pair && bf16) e = launch_pair_kernel<kFmtBF16, false, __nv_bfloat16>(ma, mb, p, dev, a.stream);
+    else if (pair && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtF16, false, float>(ma, mb, p, dev, a.stream);
+    else if (pair) e = launch_pair_kernel<kFmtF16, false, __half>(ma, mb, p, dev, a.stream);
     else if (bf16 && a.out_dtype == DGA_F32) e = launch_kernel<kFmtBF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
     else if (bf16) e = launch_kernel<kFmtBF16, false, kBnFloat, __nv_bfloat16>(ma, mb, p, dev, a.stream);
     else if (a.out_dtype == DGA_F32) e = launch_kernel<kFmtF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
