@@ -507,7 +507,9 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 2 * kEpiWarps);  // one lane of each epilogue warp of both CTAs
+            // floating point: one lane of each epilogue warp of both CTAs;
+            // INT8: one thread per CTA, after its 16 epilogue warps meet
+            mbar_init(&acc_empty[b], kI8 ? 2 : 2 * kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -682,9 +684,12 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                                 static_cast<uint32_t>(sum[c * 32 + j]) +
                                 static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j]))));
                     }
+                    // every epilogue warp of this CTA has read the accumulator: one
+                    // thread tells the leader (a single cluster-scope release per CTA)
                     tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&acc_empty[acc]), 0));
+                    asm volatile("bar.sync 2, %0;" ::"n"(kEpiWarps * 32) : "memory");
+                    if (ew == 0 && lane == 0)
+                        mbar_arrive_cluster(map_to_cta(smem_u32(&acc_empty[acc]), 0));
                     if (++acc == 2) { acc = 0; acc_phase ^= 1; }
                 }
                 if (!ok) break;
@@ -800,7 +805,7 @@ __global__ void __launch_bounds__(256) pack_transposed_kernel(const TSrc* __rest
     const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 64;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;
     const int t = threadIdx.x;
-#pragma unroll 4
+#pragma unroll  // all 16 loads in flight at once (the copy is latency-bound)
     for (int i = 0; i < 16; ++i) {
         const int idx = i * 256 + t, kk = idx >> 6, rr = idx & 63;
         const int64_t k = k0 + kk, r = r0 + rr;
@@ -1069,8 +1074,10 @@ cudaError_t launch_pack(const void* src, int64_t ld_src, bool transposed, int64_
     } else {
         const int vec = (ld_src * static_cast<int64_t>(sizeof(TSrc))) % (8 * sizeof(TSrc)) == 0 &&
                         aligned(src, 8 * sizeof(TSrc));
+        // one 8-element group per thread where the grid allows (no dependent
+        // loads chained through a grid-stride loop)
         const int64_t work = rows * (ld_dst / 8);
-        const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sm_count) * 16);
+        const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sm_count) * 256);
         pack_rows_kernel<TSrc><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
             static_cast<const TSrc*>(src), ld_src, rows, K, static_cast<uint16_t*>(dst), ld_dst, vec);
     }
