@@ -54,6 +54,8 @@ SIGNATURES = {
                                   _I64, _VP]),
     "dga_spmv_csr": (_CI, [_I64, _I64, _I64, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP]),
     "dga_spmv_csr_workspace_size": (_SZ, [_I64, _I64]),
+    "dga_probe_fp32_fma": (_CI, [_CI, _I64, _VP, _I64, _VP, _VP]),
+    "dga_probe_fp32_fma_out_floats": (_I64, []),
 }
 
 _lock = threading.Lock()
@@ -171,6 +173,14 @@ def dga_spmv_csr(rows, cols, nnz, row_offsets, column_indices, values, alpha, x,
 
 def dga_spmv_csr_workspace_size(rows, nnz):
     return lib().dga_spmv_csr_workspace_size(rows, nnz)
+
+
+def dga_probe_fp32_fma(packed, iters, out, out_floats, flops, stream):
+    return lib().dga_probe_fp32_fma(packed, iters, out, out_floats, flops, stream)
+
+
+def dga_probe_fp32_fma_out_floats():
+    return lib().dga_probe_fp32_fma_out_floats()
 
 
 # ---- tensor convenience layer ----------------------------------------------

@@ -416,6 +416,26 @@ int dga_selftest_bounded_wait(int64_t limit_ns, dga_stream_t stream) {
     return e == cudaSuccess ? DGA_OK : fail_cuda(e);
 }
 
+int64_t dga_probe_fp32_fma_out_floats(void) { return fma_probe_out_floats(sm_count_or_default()); }
+
+int dga_probe_fp32_fma(int packed, int64_t iters, float* out, int64_t out_floats, double* flops,
+                       dga_stream_t stream) {
+    if (packed != 0 && packed != 1) return -1;
+    if (iters < 1 || iters > (int64_t{1} << 20)) return -2;
+    if (out == nullptr) return -3;
+    if (flops == nullptr) return -5;
+    DeviceInfo dev;
+    cudaError_t e = current_device_info(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev.major != 10 || dev.minor != 3) return DGA_ERR_DEVICE;
+    if (out_floats < fma_probe_out_floats(dev.sm_count)) return -4;
+    e = fma_probe_launch(packed, iters, out, dev.sm_count, flops,
+                         reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_launches = 1;
+    return DGA_OK;
+}
+
 const char* dga_status_string(int status) {
     if (status < 0) return "invalid argument (the negated value is its 1-based position)";
     switch (status) {

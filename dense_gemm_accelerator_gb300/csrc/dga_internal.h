@@ -80,6 +80,12 @@ cudaError_t spmv_launch(int64_t rows, int64_t cols, int64_t nnz, const int32_t* 
 // Reads and clears this device's SpMV status word (non-zero: malformed CSR arrays).
 cudaError_t spmv_status_take(int* status);
 
+// FP32 FMA-rate probe (measurement only): floats of `out` one launch writes,
+// and the launch itself (*flops receives the FLOPs it performs).
+int64_t fma_probe_out_floats(int sm_count);
+cudaError_t fma_probe_launch(int packed, int64_t iters, float* out, int sm_count, double* flops,
+                             cudaStream_t stream);
+
 bool tc_supports(const GemmArgs& a);
 size_t tc_workspace_size(const GemmArgs& a);
 cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);

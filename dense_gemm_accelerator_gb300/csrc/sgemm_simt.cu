@@ -6,13 +6,15 @@
 //     128 times, so the DRAM-side intensity reaches ~32 FLOP/B (section 5.3:
 //     I_tile = T/4), and the 129 MB L2 serves most re-reads;
 //   * 256 threads, each accumulating an 8 x 8 register tile: per k, 8 A and 8
-//     B values from shared memory feed 64 FFMAs (section 5.4: 4 FMA per
-//     shared read);
+//     B values from shared memory feed 64 FMAs (section 5.4: 4 FMA per
+//     shared read), issued as 32 packed fma.rn.f32x2 -- each half an
+//     ordinary round-to-nearest fp32 FMA, so the results are those of 64
+//     scalar FFMAs in the same order;
 //   * double buffering (section 5.4) at two levels: the next K-slice (8 deep)
 //     is fetched from global memory into registers with 128-bit loads while
 //     the current slice is consumed, then written to the other shared-memory
 //     buffer (one barrier per slice); and inside a slice the fragments of
-//     k+1 are read from shared memory while the FFMAs of k run.  A slice of
+//     k+1 are read from shared memory while the FMAs of k run.  A slice of
 //     8 keeps the staging registers few enough for two CTAs per SM at 128
 //     registers, which measured faster than deeper slices on GB300;
 //   * A is stored k-major in shared memory (transposed on the way in); each
@@ -79,6 +81,23 @@ __device__ __forceinline__ float4 ld_f4(const float* p) {
     return __ldg(reinterpret_cast<const float4*>(p));
 }
 
+// Packed pairs of fp32 values in one 64-bit register: low half first.
+__device__ __forceinline__ uint64_t pair_of(float v) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ void unpair(uint64_t r, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+
+// d.lo += a.lo * b.lo and d.hi += a.hi * b.hi, each one fp32 fused
+// multiply-add rounded to nearest: two FFMAs' results in one instruction.
+__device__ __forceinline__ void fma2(uint64_t& d, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 // Four consecutive elements of a row starting at `col`; zeros outside.
 __device__ __forceinline__ float4 ld_f4_checked(const float* row, int64_t col, int64_t ncols,
                                                 bool row_ok, bool vec) {
@@ -101,8 +120,11 @@ __device__ __forceinline__ float4 ld_f4_checked(const float* row, int64_t col, i
 // recomputing the addresses; measured faster for a column-major B (4096^3:
 // 56.6 against 54.8 TFLOP/s, and 57.1 against 48.5 with a bias row) and no
 // different otherwise, so the interior kernel uses it for column-major B.
+// kColOuter: the order of the 32 packed FMAs of a k-step (see the loop); the
+// interior kernel takes column pairs outer, the general kernel rows outer
+// (the other order needs registers it does not have: it spilled there).
 template <bool kChecked, bool kTransA, bool kTransB, int kReadC = -1, int kBias = -1,
-          bool kRunPtr = false>
+          bool kRunPtr = false, bool kColOuter = false>
 __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t row0, int64_t col0,
                                            int64_t k_begin, int64_t k_end, float* partial) {
     const int tid = threadIdx.x;
@@ -180,11 +202,14 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
     const int am0 = wm * 64 + lm * 4, am1 = am0 + 32;
     const int bn0 = wn * 32 + ln * 4, bn1 = bn0 + 16;
 
-    float acc[8][8];
+    // accumulators as pairs of adjacent columns: acc2[i][q] holds columns
+    // 2q and 2q+1 of row i, updated by one fma.rn.f32x2 (two independent
+    // IEEE fp32 fused multiply-adds: the same results as two fmaf)
+    uint64_t acc2[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int q = 0; q < 4; ++q) acc2[i][q] = 0ull;  // (+0.0f, +0.0f)
 
     const int64_t n_slices = (k_end - k_begin + BK - 1) / BK;
     fetch(k_begin);
@@ -194,33 +219,59 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
         const int buf = static_cast<int>(s & 1);
         const bool more = s + 1 < n_slices;
         // Fragments are double-buffered in registers: the shared-memory loads
-        // for k+1 are issued before the 64 FFMAs of k.  The next slice's global
+        // for k+1 are issued before the 64 FMAs of k.  The next slice's global
         // loads go out after two k-steps (their registers are live for less of
-        // the loop), and the FFMAs walk the 8 x 8 block column by column: both
-        // measured on GB300 (4096^3: 56.0 -> 57.7 TFLOP/s; any fetch point
-        // from k = 1 to 4 gives the same).
-        float a[2][8], b[2][8];
+        // the loop; 4096^3 measured 56.0 -> 57.7 TFLOP/s on GB300, any fetch
+        // point from k = 1 to 4 the same).  The 64 FMAs of a k-step are 32
+        // packed fma.rn.f32x2 on column pairs, each a_i broadcast into both
+        // halves: half the issue slots of scalar FFMAs.  Measured at 4096^3
+        // over the four operand layouts, with beta or a bias row (mean /
+        // lowest of the eight, TFLOP/s): scalar FFMAs 57.1 / 52.4, packed
+        // with rows outer 57.6 / 54.9, packed with column pairs outer (the 8
+        // broadcasts made first) 57.9 / 55.4.  Keeping A as ready-made
+        // (a, a) pairs in shared memory instead measured 50.1 (twice the A
+        // bytes through the shared-memory pipe).
+        float a[2][8];
+        uint64_t b[2][4];  // column pairs (2q, 2q+1) of this thread's 8 B values
         auto frag = [&](int d, int k) {
             *reinterpret_cast<float4*>(&a[d][0]) = *reinterpret_cast<const float4*>(&sm.A[buf][k][am0]);
             *reinterpret_cast<float4*>(&a[d][4]) = *reinterpret_cast<const float4*>(&sm.A[buf][k][am1]);
-            *reinterpret_cast<float4*>(&b[d][0]) = *reinterpret_cast<const float4*>(&sm.B[buf][k][bn0]);
-            *reinterpret_cast<float4*>(&b[d][4]) = *reinterpret_cast<const float4*>(&sm.B[buf][k][bn1]);
+            *reinterpret_cast<ulonglong2*>(&b[d][0]) = *reinterpret_cast<const ulonglong2*>(&sm.B[buf][k][bn0]);
+            *reinterpret_cast<ulonglong2*>(&b[d][2]) = *reinterpret_cast<const ulonglong2*>(&sm.B[buf][k][bn1]);
         };
         frag(0, 0);
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
             if (k == 2 && more) fetch(k_begin + (s + 1) * BK);
             if (k + 1 < BK) frag((k + 1) & 1, k + 1);
+            if constexpr (kColOuter) {
+                uint64_t ap[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
+                for (int i = 0; i < 8; ++i) ap[i] = pair_of(a[k & 1][i]);  // (a_i, a_i)
 #pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i][j] = fmaf(a[k & 1][i], b[k & 1][j], acc[i][j]);
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) fma2(acc2[i][q], ap[i], b[k & 1][q]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint64_t ai = pair_of(a[k & 1][i]);  // (a_i, a_i)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) fma2(acc2[i][q], ai, b[k & 1][q]);
+                }
+            }
         }
         // The other buffer was last read in slice s-1, before the barrier
         // that ended it, so it can be overwritten now.
         if (more) stash(buf ^ 1);
         __syncthreads();
     }
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) unpair(acc2[i][q], acc[i][2 * q], acc[i][2 * q + 1]);
 
     if (partial != nullptr) {
         // a K-range of a tail tile: raw partial sums, reduced by sgemm_tail_reduce
@@ -341,8 +392,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sgemm_128x128_interior_k
     int64_t tm, tn;
     grouped_tile(static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x, gridDim.y, gridDim.x,
                  tm, tn);
-    block_tile<false, kTransA, kTransB, kReadC, kBias, kTransB>(p, sm, tm * BM, tn * BN,
-                                                                            0, p.K, nullptr);
+    block_tile<false, kTransA, kTransB, kReadC, kBias, kTransB, true>(p, sm, tm * BM, tn * BN,
+                                                                      0, p.K, nullptr);
 }
 
 // Sums the K-range partials of each tail tile in part order (so the result

@@ -223,6 +223,32 @@ int dga_sync_status(dga_stream_t stream);
  * The pages have no counterpart (their kernels have no waits). */
 int dga_selftest_bounded_wait(int64_t limit_ns, dga_stream_t stream);
 
+/*
+ * Measurement helper, not part of any GEMM: a probe of the FP32 FMA rate.
+ * The roofline of "Matrix multiplication: arithmetic intensity, tiling and
+ * Tensor Core" (section 5.1) caps a compute-bound kernel at the chip's peak;
+ * for the FP32 SIMT path that peak is derived as SMs x 128 lanes x 2 FLOP x
+ * SM clock, and this probe measures what the FMA pipe sustains so the
+ * derived figure can be checked.
+ *
+ * Enqueues one kernel on `stream`: 4 CTAs of 256 threads per SM, each thread
+ * running 8 independent accumulator chains for `iters` iterations of 64
+ * fused multiply-adds -- scalar fp32 FMAs (packed = 0) or fma.rn.f32x2 pairs
+ * (packed = 1, the form the SIMT GEMM issues).  Time it with events around
+ * the call; *flops (host pointer) receives the FLOPs the launch performs
+ * (2 per FMA).  `out` is caller-owned device memory of at least
+ * dga_probe_fp32_fma_out_floats() floats (one sum per thread, written so the
+ * work cannot be dropped).
+ * Errors: -1 packed not 0 or 1; -2 iters outside [1, 2^20]; -3 out null;
+ * -4 out_floats too small; -5 flops null; DGA_ERR_DEVICE, DGA_ERR_CUDA.
+ */
+int dga_probe_fp32_fma(int packed, int64_t iters, float* out, int64_t out_floats, double* flops,
+                       dga_stream_t stream);
+
+/* Floats of `out` that dga_probe_fp32_fma writes on the current device
+ * (152 SMs assumed when no device can be queried). */
+int64_t dga_probe_fp32_fma_out_floats(void);
+
 /* The cudaError_t value behind the last DGA_ERR_CUDA on this host thread. */
 int dga_last_cuda_error(void);
 

@@ -237,3 +237,19 @@ def test_spmv_quick_returns_and_workspace(lib):
     ws = dga.dga_spmv_csr_workspace_size(1 << 22, 1 << 26)
     assert 8 * 8 * 152 * 8 <= ws <= 8 * 8 * 152 * 8 + 512
     assert dga.dga_spmv_csr_workspace_size(0, 10) == 0
+
+
+def test_fma_probe_argument_errors(lib):
+    import ctypes
+    flops = ctypes.c_double(0.0)
+    out_floats = dga.dga_probe_fp32_fma_out_floats()
+    assert out_floats == 152 * 4 * 256  # no device here: 152 SMs assumed
+    assert dga.dga_probe_fp32_fma(2, 10, 0x1000, out_floats, ctypes.byref(flops), None) == -1
+    assert dga.dga_probe_fp32_fma(0, 0, 0x1000, out_floats, ctypes.byref(flops), None) == -2
+    assert dga.dga_probe_fp32_fma(1, (1 << 20) + 1, 0x1000, out_floats, ctypes.byref(flops),
+                                  None) == -2
+    assert dga.dga_probe_fp32_fma(0, 10, None, out_floats, ctypes.byref(flops), None) == -3
+    assert dga.dga_probe_fp32_fma(0, 10, 0x1000, out_floats, None, None) == -5
+    # valid arguments need the device, absent here
+    assert dga.dga_probe_fp32_fma(0, 10, 0x1000, out_floats, ctypes.byref(flops),
+                                  None) in (dga.ERR_CUDA, dga.ERR_DEVICE)
