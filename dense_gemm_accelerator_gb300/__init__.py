@@ -157,7 +157,7 @@ def dga_selftest_bounded_wait(limit_ns, stream):
     return lib().dga_selftest_bounded_wait(limit_ns, stream)
 
 
-NOALLOC_SCRATCH_BYTES = 64 << 20
+NOALLOC_SCRATCH_BYTES = 72 << 20
 
 
 def dga_gemm_i8_noalloc(layout_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream):

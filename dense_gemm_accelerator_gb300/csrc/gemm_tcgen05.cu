@@ -43,8 +43,8 @@
 // MN-major descriptors (transpose bits of the instruction descriptor).  Only
 // a leading dimension TMA cannot express (not a multiple of 16 bytes, or an
 // unaligned base) and INT8 inputs (encoded exactly as bf16, see below) are
-// first repacked into the caller's workspace by pack_rows_kernel /
-// pack_transposed_kernel.
+// first repacked into the caller's workspace, both operands by one launch of
+// pack_pair_kernel that the GEMM follows as a programmatic dependent.
 //
 // INT8 x INT8 -> INT32 (tcgen05 has no integer MMA on sm_103a: ptxas rejects
 // kind::i8 for this target).  Every int8 value is an exact bf16, every
@@ -247,6 +247,10 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // launched right behind the operand repack (programmatic serialisation):
+    // everything above overlapped its tail; its output is read only from here
+    // on (a no-op when the launch has no such dependency)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer
@@ -527,6 +531,8 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
     cluster_sync();  // barriers of both CTAs initialised before any remote arrive
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // see the single-CTA kernel: the repack's output is read only after this
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t cluster_id = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
 
     if (warp == 0) {
@@ -742,18 +748,15 @@ __global__ void bounded_wait_probe_kernel(uint64_t limit_ns) {
 
 // ---- operand repacking into the workspace ------------------------------------
 //
-// dst[r][k] = src(r, k) converted to 16-bit storage (bf16/fp16; int8 values
-// become exact bf16), for r < rows, k < K, and zero for K <= k < ld_dst.
-// ld_dst is a multiple of 8, so every thread writes whole 16-byte vectors.
-// src(r, k) = src[r*ld_src + k] (k-contiguous) or src[k*ld_src + r]
-// (transposed, e.g. a row-major B that the tensor cores need K-major).
+// 16-bit operands: dst[r][c] = src[r*ld_src + c] converted to 16-bit storage
+// (bf16/fp16; int8 values become exact bf16), for r < rows, c < the row
+// length, and zero up to ld_dst, a multiple of 8 (every thread writes whole
+// 16-byte vectors).  The rows are the source's own: K-long rows of a K-major
+// operand, M- or N-long rows (one per k) of an MN-major one, which the GEMM
+// then reads MN-major.  fp32 operands of the TF32 path (K-major only) are
+// copied, or transposed, by their own kernels.
 
-template <typename TSrc> struct PackIn;
-template <> struct PackIn<int8_t> {
-    __device__ __forceinline__ static uint16_t bits(int8_t v) {  // exact: |v| <= 128
-        return __bfloat16_as_ushort(__float2bfloat16_rn(static_cast<float>(v)));
-    }
-};
+template <typename TSrc> struct PackIn;  // 16-bit sources: their bits
 template <> struct PackIn<__nv_bfloat16> {
     __device__ __forceinline__ static uint16_t bits(__nv_bfloat16 v) { return __bfloat16_as_ushort(v); }
 };
@@ -766,63 +769,121 @@ __device__ __forceinline__ uint4 pack8(const uint16_t (&h)[8]) {
                       h[4] | (uint32_t(h[5]) << 16), h[6] | (uint32_t(h[7]) << 16));
 }
 
-// k-contiguous source: one thread per 8 consecutive k of a row (grid-stride).
+// One operand's repack, as the fused kernel below receives it: dst[r][k] =
+// src[r*ld_src + k] converted, for r < rows, k < K (the row length: K for a
+// K-major operand, M or N for an MN-major one), zero for K <= k < ld_dst.
 template <typename TSrc>
-__global__ void __launch_bounds__(256) pack_rows_kernel(const TSrc* __restrict__ src, int64_t ld_src,
-                                                        int64_t rows, int64_t K,
-                                                        uint16_t* __restrict__ dst, int64_t ld_dst,
-                                                        int vec_src) {
-    const int64_t groups = ld_dst / 8;
-    const int64_t total = rows * groups;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = i / groups, k = (i % groups) * 8;
-        const TSrc* s = src + r * ld_src + k;
-        uint16_t h[8];
-        if (vec_src && k + 8 <= K) {
-            // 8 elements in one load: 8 bytes of int8 or 16 bytes of 16-bit data
-            TSrc v[8];
-            if constexpr (sizeof(TSrc) == 1) *reinterpret_cast<uint2*>(v) = __ldg(reinterpret_cast<const uint2*>(s));
-            else *reinterpret_cast<uint4*>(v) = __ldg(reinterpret_cast<const uint4*>(s));
+struct PackJob {
+    const TSrc* src;
+    const TSrc* src_end;  // one past the last element of the last row
+    int64_t ld_src, rows, K;
+    uint16_t* dst;
+    int64_t ld_dst;
+    int vec_src;      // the source's 8-element groups are aligned
+    int64_t blocks;   // blocks of the launch this job takes
+};
+
+// Eight int8 values (byte q of v is value q) as eight exact bf16, in memory
+// order, without conversion instructions (those issue at a fraction of the
+// integer and FMA rate): for a byte b, u = b ^ 0x80 is v + 128, and the float
+// whose bits are 0x4B000000 | u is exactly 2^23 + u, so subtracting
+// 2^23 + 128 gives v exactly (one FADD); an integer of magnitude <= 128 has at
+// most 8 significant bits, so the top 16 bits of its float encoding are its
+// bf16 encoding, and one byte permute packs two of them.
+__device__ __forceinline__ uint4 int8x8_to_bf16(uint64_t v) {
+    const uint32_t w[2] = {static_cast<uint32_t>(v) ^ 0x80808080u,
+                           static_cast<uint32_t>(v >> 32) ^ 0x80808080u};
+    uint32_t out[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) h[j] = PackIn<TSrc>::bits(v[j]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) h[j] = k + j < K ? PackIn<TSrc>::bits(s[j]) : uint16_t(0);
-        }
-        *reinterpret_cast<uint4*>(dst + r * ld_dst + k) = pack8(h);
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t x = w[q >> 1];
+        const uint32_t b0 = (2 * q) & 3, b1 = (2 * q + 1) & 3;  // byte positions in x
+        // bytes of the result: [x byte b, 0x00, 0x00, 0x4B] (selector digits 4 and 7 pick
+        // bytes 0 and 3 of the constant)
+        const float f0 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u | b0)) - 8388736.0f;
+        const float f1 = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7440u | b1)) - 8388736.0f;
+        out[q] = __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632u);  // top halves
     }
+    return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-// Transposed source: a 64 (k) x 64 (r) tile per block through shared memory;
-// reads walk r (contiguous in the source), writes walk k (16-byte vectors).
+__device__ __forceinline__ uint64_t ldg_u64(uintptr_t a) {
+    return __ldg(reinterpret_cast<const unsigned long long*>(a));
+}
+
+// One thread per 8 consecutive elements of a row (block-stride over
+// `nblocks` blocks, this one being `blk`).
 template <typename TSrc>
-__global__ void __launch_bounds__(256) pack_transposed_kernel(const TSrc* __restrict__ src,
-                                                              int64_t ld_src, int64_t rows,
-                                                              int64_t K, uint16_t* __restrict__ dst,
-                                                              int64_t ld_dst) {
-    __shared__ uint16_t tile[64][64 + 2];  // tile[k][r], already converted
-    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 64;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;
-    const int t = threadIdx.x;
-#pragma unroll  // all 16 loads in flight at once (the copy is latency-bound)
-    for (int i = 0; i < 16; ++i) {
-        const int idx = i * 256 + t, kk = idx >> 6, rr = idx & 63;
-        const int64_t k = k0 + kk, r = r0 + rr;
-        tile[kk][rr] = (k < K && r < rows) ? PackIn<TSrc>::bits(src[k * ld_src + r]) : uint16_t(0);
-    }
-    __syncthreads();
+__device__ __forceinline__ void pack_rows_body(const PackJob<TSrc>& j, int64_t blk, int64_t nblocks) {
+    const TSrc* __restrict__ src = j.src;
+    uint16_t* __restrict__ dst = j.dst;
+    const int64_t ld_src = j.ld_src, K = j.K, ld_dst = j.ld_dst;
+    const int vec_src = j.vec_src;
+    const int64_t groups = ld_dst / 8;
+    const int64_t total = j.rows * groups;
+    for (int64_t i = blk * 256 + threadIdx.x; i < total; i += nblocks * 256) {
+        const int64_t r = i / groups, k = (i % groups) * 8;
+        const TSrc* s = src + r * ld_src + k;
+        if constexpr (sizeof(TSrc) == 1) {
+            // int8: the 8 bytes as one 64-bit word -- one aligned load, or for
+            // a row that is not 8-byte aligned the two aligned words around
+            // them, funnel-shifted (only where both words lie inside the
+            // operand: [src, src_end)); bytewise at the edges
+            uint64_t v = 0;
+            bool have = false;
+            if (k + 8 <= K) {
+                const uintptr_t a = reinterpret_cast<uintptr_t>(s);
+                if (vec_src) {
+                    v = ldg_u64(a);
+                    have = true;
+                } else {
+                    const uintptr_t base = a & ~static_cast<uintptr_t>(7);
+                    if (base >= reinterpret_cast<uintptr_t>(src) &&
+                        base + 16 <= reinterpret_cast<uintptr_t>(j.src_end)) {
+                        const uint64_t w0 = ldg_u64(base), w1 = ldg_u64(base + 8);
+                        const int sh = static_cast<int>(a - base) * 8;
+                        v = sh ? (w0 >> sh) | (w1 << (64 - sh)) : w0;
+                        have = true;
+                    }
+                }
+            }
+            if (!have) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int idx = i * 256 + t, rr = idx >> 3, kq = (idx & 7) * 8;
-        const int64_t r = r0 + rr, k = k0 + kq;
-        if (r < rows && k < ld_dst) {
+                for (int q = 0; q < 8; ++q)
+                    if (k + q < K) v |= static_cast<uint64_t>(static_cast<uint8_t>(s[q])) << (8 * q);
+            }
+            *reinterpret_cast<uint4*>(dst + r * ld_dst + k) = int8x8_to_bf16(v);
+        } else {
+            // 16-bit data is copied bit for bit: 16 bytes in one load where aligned
             uint16_t h[8];
+            if (vec_src && k + 8 <= K) {
+                TSrc v[8];
+                *reinterpret_cast<uint4*>(v) = __ldg(reinterpret_cast<const uint4*>(s));
 #pragma unroll
-            for (int j = 0; j < 8; ++j) h[j] = tile[kq + j][rr];
+                for (int q = 0; q < 8; ++q) h[q] = PackIn<TSrc>::bits(v[q]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) h[q] = k + q < K ? PackIn<TSrc>::bits(s[q]) : uint16_t(0);
+            }
             *reinterpret_cast<uint4*>(dst + r * ld_dst + k) = pack8(h);
         }
     }
+}
+
+// Both operands' 16-bit repacks in one launch: blocks [0, a.blocks) do A's
+// job, the rest B's (a job with 0 blocks is absent).  Every repack copies its
+// source row by row, keeping the layout (an MN-major operand stays MN-major),
+// so none transposes.  One launch lets B's blocks fill the SMs while A's
+// drain, and the GEMM behind it is released (griddepcontrol.launch_dependents)
+// as soon as every block has started: its prologue overlaps the repack's
+// tail, and it reads the output only after griddepcontrol.wait, i.e. after
+// this grid has completed.
+template <typename TSrc>
+__global__ void __launch_bounds__(256) pack_pair_kernel(PackJob<TSrc> a, PackJob<TSrc> b) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t blk = blockIdx.x;
+    if (blk < a.blocks) pack_rows_body(a, blk, a.blocks);
+    else pack_rows_body(b, blk - a.blocks, b.blocks);
 }
 
 // fp32 operands of the TF32 path, same contract with 4-byte elements:
@@ -831,6 +892,7 @@ __global__ void __launch_bounds__(256) pack_transposed_kernel(const TSrc* __rest
 __global__ void __launch_bounds__(256) pack_rows_f32_kernel(const float* __restrict__ src,
                                                             int64_t ld_src, int64_t rows, int64_t K,
                                                             float* __restrict__ dst, int64_t ld_dst) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // see pack_pair_kernel
     const int64_t groups = ld_dst / 4;
     const int64_t total = rows * groups;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -853,6 +915,7 @@ __global__ void __launch_bounds__(256) pack_transposed_f32_kernel(const float* _
                                                                   int64_t K, float* __restrict__ dst,
                                                                   int64_t ld_dst) {
     __shared__ float tile[64][64 + 1];  // tile[k][r]
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // see pack_pair_kernel
     const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 64;
     const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64;
     const int t = threadIdx.x;
@@ -942,11 +1005,14 @@ constexpr size_t kWsAlign = 256;
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-// Which operands need repacking into the workspace.
+// Which operands need repacking into the workspace.  16-bit repacks keep the
+// operand's own layout: a K-major operand becomes rows x kp, an MN-major one
+// (column-major A, row-major B) K rows x ld_mn, both copied row by row.
 struct PackPlan {
     bool pack_a, pack_b;
-    bool a_mn, b_mn;  // read in place MN-major (column-major A / row-major B)
-    int64_t kp;  // padded K of packed operands (multiple of 8 elements = 16 bytes)
+    bool a_mn, b_mn;  // read MN-major (column-major A / row-major B)
+    int64_t kp;  // padded K of K-major repacks (multiple of 8 elements = 16 bytes)
+    int64_t a_ld, b_ld;  // leading dimension of each repacked operand
     size_t a_bytes, b_bytes;
 };
 
@@ -960,19 +1026,23 @@ PackPlan plan_for(const GemmArgs& a) {
         pl.pack_a = a.layout_a == DGA_COL_MAJOR || a.lda % 4 != 0 || !aligned(a.A, 16);
         pl.pack_b = a.layout_b == DGA_ROW_MAJOR || a.ldb % 4 != 0 || !aligned(a.B, 16);
         pl.a_mn = pl.b_mn = false;
+        pl.a_ld = pl.b_ld = pl.kp;
         pl.a_bytes = pl.pack_a ? round_up(a.M * pl.kp * 4, kWsAlign) : 0;
         pl.b_bytes = pl.pack_b ? round_up(a.N * pl.kp * 4, kWsAlign) : 0;
         return pl;
     }
     pl.kp = round_up(a.K, 8);
     // TMA needs 16-byte row strides and a 16-byte aligned base; INT8 is
-    // always re-encoded (as bf16, K-major).
+    // always re-encoded (as bf16).  Either way the copy keeps the layout, so
+    // no repack transposes: MN-major operands are read MN-major from it.
     pl.pack_a = i8 || a.lda % 8 != 0 || !aligned(a.A, 16);
     pl.pack_b = i8 || a.ldb % 8 != 0 || !aligned(a.B, 16);
-    pl.a_mn = !pl.pack_a && a.layout_a == DGA_COL_MAJOR;
-    pl.b_mn = !pl.pack_b && a.layout_b == DGA_ROW_MAJOR;
-    pl.a_bytes = pl.pack_a ? round_up(a.M * pl.kp * 2, kWsAlign) : 0;
-    pl.b_bytes = pl.pack_b ? round_up(a.N * pl.kp * 2, kWsAlign) : 0;
+    pl.a_mn = a.layout_a == DGA_COL_MAJOR;
+    pl.b_mn = a.layout_b == DGA_ROW_MAJOR;
+    pl.a_ld = pl.a_mn ? round_up(a.M, 8) : pl.kp;
+    pl.b_ld = pl.b_mn ? round_up(a.N, 8) : pl.kp;
+    pl.a_bytes = pl.pack_a ? round_up((pl.a_mn ? a.K : a.M) * pl.a_ld * 2, kWsAlign) : 0;
+    pl.b_bytes = pl.pack_b ? round_up((pl.b_mn ? a.K : a.N) * pl.b_ld * 2, kWsAlign) : 0;
     return pl;
 }
 
@@ -998,17 +1068,28 @@ uint32_t raster_group_rows(int64_t K, uint32_t tiles_m, int tile_rows) {
     return std::min(g, tiles_m);
 }
 
+// pdl: the launch follows the operand repack on `s` and may start before it
+// completes (programmatic stream serialisation; the kernel waits for it with
+// griddepcontrol.wait before its first operand load).
 template <uint32_t kFmt, bool kI8, int BN, typename TOut>
 cudaError_t launch_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
-                          const DeviceInfo& dev, cudaStream_t s) {
+                          const DeviceInfo& dev, cudaStream_t s, bool pdl) {
     auto kern = tc_gemm_kernel<kFmt, kI8, BN, TOut>;
     const int smem = static_cast<int>(Smem<BN, kI8 ? 8 : 4>::kLaunchBytes);
     if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>(std::min<uint32_t>(p.num_tiles, dev.sm_count));
-    kern<<<grid, kI8 ? 576 : 192, smem, s>>>(ma, mb, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(std::min<uint32_t>(p.num_tiles, dev.sm_count)));
+    cfg.blockDim = dim3(kI8 ? 576 : 192);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
 }
 
 // Clusters of two that fit at once on this device (queried once per kernel).
@@ -1040,7 +1121,7 @@ int max_pair_clusters(Kern kern, int smem, int threads, const DeviceInfo& dev) {
 
 template <uint32_t kFmt, bool kI8, typename TOut>
 cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
-                               const DeviceInfo& dev, cudaStream_t s) {
+                               const DeviceInfo& dev, cudaStream_t s, bool pdl) {
     auto kern = tc_gemm_pair_kernel<kFmt, kI8, TOut>;
     const int smem = static_cast<int>(PairSmem<kI8 ? 8 : 4>::kLaunchBytes);
     const int threads = kI8 ? 576 : 192;
@@ -1053,34 +1134,48 @@ cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, con
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;  // see launch_kernel
     return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
 }
 
+// One operand's 16-bit repack job: dst (rows x ld_dst) from the source's
+// rows of K elements; `blocks` is what the job takes of the fused launch.
 template <typename TSrc>
-cudaError_t launch_pack(const void* src, int64_t ld_src, bool transposed, int64_t rows,
-                        int64_t K, void* dst, int64_t ld_dst, int sm_count, cudaStream_t s) {
-    if (transposed) {
-        dim3 grid(static_cast<unsigned>((ld_dst + 63) / 64), static_cast<unsigned>((rows + 63) / 64));
-        if (grid.y > 65535) return cudaErrorInvalidConfiguration;
-        pack_transposed_kernel<TSrc><<<grid, 256, 0, s>>>(static_cast<const TSrc*>(src), ld_src,
-                                                          rows, K, static_cast<uint16_t*>(dst), ld_dst);
-    } else {
-        const int vec = (ld_src * static_cast<int64_t>(sizeof(TSrc))) % (8 * sizeof(TSrc)) == 0 &&
-                        aligned(src, 8 * sizeof(TSrc));
-        // one 8-element group per thread where the grid allows (no dependent
-        // loads chained through a grid-stride loop)
-        const int64_t work = rows * (ld_dst / 8);
-        const int64_t blocks = std::min<int64_t>((work + 255) / 256, static_cast<int64_t>(sm_count) * 256);
-        pack_rows_kernel<TSrc><<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, s>>>(
-            static_cast<const TSrc*>(src), ld_src, rows, K, static_cast<uint16_t*>(dst), ld_dst, vec);
-    }
+PackJob<TSrc> pack_job(const void* src, int64_t ld_src, int64_t rows, int64_t K, void* dst,
+                       int64_t ld_dst, int sm_count) {
+    PackJob<TSrc> j{};
+    j.src = static_cast<const TSrc*>(src);
+    j.src_end = j.src + (rows - 1) * ld_src + K;
+    j.ld_src = ld_src;
+    j.rows = rows;
+    j.K = K;
+    j.dst = static_cast<uint16_t*>(dst);
+    j.ld_dst = ld_dst;
+    j.vec_src = (ld_src * static_cast<int64_t>(sizeof(TSrc))) % (8 * sizeof(TSrc)) == 0 &&
+                aligned(src, 8 * sizeof(TSrc));
+    // one 8-element group per thread where the launch allows (no dependent
+    // loads chained through a block-stride loop)
+    const int64_t work = rows * (ld_dst / 8);
+    j.blocks = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256,
+                                                      static_cast<int64_t>(sm_count) * 256));
+    return j;
+}
+
+// Launches the repack jobs (either may be absent: blocks = 0) as one grid.
+template <typename TSrc>
+cudaError_t launch_pack_pair(const PackJob<TSrc>& a, const PackJob<TSrc>& b, cudaStream_t s) {
+    const int64_t blocks = a.blocks + b.blocks;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    pack_pair_kernel<TSrc><<<static_cast<unsigned>(blocks), 256, 0, s>>>(a, b);
     return cudaGetLastError();
 }
 
@@ -1132,30 +1227,51 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     int64_t ldb = a.ldb;
     cudaError_t e;
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
-    if (pl.pack_a) {
-        void* dst = ws;
-        const bool tr = a.layout_a == DGA_COL_MAJOR;  // A(i, k) = A[k*lda + i]: transpose to M x K
-        if (tf32) e = launch_pack_f32(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
-        else if (i8) e = launch_pack<int8_t>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
-        else if (bf16) e = launch_pack<__nv_bfloat16>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
-        else e = launch_pack<__half>(a.A, a.lda, tr, a.M, a.K, dst, pl.kp, dev.sm_count, a.stream);
+    void* dst_a = ws;
+    void* dst_b = ws + pl.a_bytes;
+    // TF32 reads K-major operands only: a column-major A or row-major B is
+    // transposed into the workspace
+    const bool tr_a = a.layout_a == DGA_COL_MAJOR;  // A(i, k) = A[k*lda + i]: to M x K
+    const bool tr_b = a.layout_b == DGA_ROW_MAJOR;  // B(k, j) = B[k*ldb + j]: to N x K
+    if (tf32) {
+        if (pl.pack_a) {
+            e = launch_pack_f32(a.A, a.lda, tr_a, a.M, a.K, dst_a, pl.kp, dev.sm_count, a.stream);
+            if (e != cudaSuccess) return e;
+            ++*launches;
+        }
+        if (pl.pack_b) {
+            e = launch_pack_f32(a.B, a.ldb, tr_b, a.N, a.K, dst_b, pl.kp, dev.sm_count, a.stream);
+            if (e != cudaSuccess) return e;
+            ++*launches;
+        }
+    } else if (pl.pack_a || pl.pack_b) {
+        // both 16-bit repacks in one launch, each copying its source row by
+        // row (an MN-major operand's rows run along M or N, one per k)
+        auto run = [&](auto tag) {
+            using T = decltype(tag);
+            PackJob<T> ja{}, jb{};
+            if (pl.pack_a)
+                ja = pl.a_mn ? pack_job<T>(a.A, a.lda, a.K, a.M, dst_a, pl.a_ld, dev.sm_count)
+                             : pack_job<T>(a.A, a.lda, a.M, a.K, dst_a, pl.a_ld, dev.sm_count);
+            if (pl.pack_b)
+                jb = pl.b_mn ? pack_job<T>(a.B, a.ldb, a.K, a.N, dst_b, pl.b_ld, dev.sm_count)
+                             : pack_job<T>(a.B, a.ldb, a.N, a.K, dst_b, pl.b_ld, dev.sm_count);
+            return launch_pack_pair<T>(ja, jb, a.stream);
+        };
+        e = i8 ? run(int8_t{}) : (bf16 ? run(__nv_bfloat16{}) : run(__half{}));
         if (e != cudaSuccess) return e;
         ++*launches;
-        A = dst;
-        lda = pl.kp;
+    }
+    if (pl.pack_a) {
+        A = dst_a;
+        lda = pl.a_ld;
     }
     if (pl.pack_b) {
-        void* dst = ws + pl.a_bytes;
-        const bool tr = a.layout_b == DGA_ROW_MAJOR;  // B(k, j) = B[k*ldb + j]: transpose to N x K
-        if (tf32) e = launch_pack_f32(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
-        else if (i8) e = launch_pack<int8_t>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
-        else if (bf16) e = launch_pack<__nv_bfloat16>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
-        else e = launch_pack<__half>(a.B, a.ldb, tr, a.N, a.K, dst, pl.kp, dev.sm_count, a.stream);
-        if (e != cudaSuccess) return e;
-        ++*launches;
-        B = dst;
-        ldb = pl.kp;
+        B = dst_b;
+        ldb = pl.b_ld;
     }
+    // the GEMM follows a repack: launch it programmatically behind it
+    const bool pdl = pl.pack_a || pl.pack_b;
     // Floating point with more than one 128-row tile: the CTA-pair kernel
     // (256 x 256 tiles, each CTA loading half of B).
     // More than one 128-row tile: the CTA-pair kernel (256 x 256 tiles, each
@@ -1190,18 +1306,18 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     p.num_kb = static_cast<uint32_t>((a.K + k_per_stage(fmt) - 1) / k_per_stage(fmt));
     p.group_m = raster_group_rows(a.K, p.tiles_m, tile_m);
 
-    if (i8 && pair) e = launch_pair_kernel<kFmtBF16, true, int32_t>(ma, mb, p, dev, a.stream);
-    else if (i8) e = launch_kernel<kFmtBF16, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream);
-    else if (tf32 && pair) e = launch_pair_kernel<kFmtTF32, false, float>(ma, mb, p, dev, a.stream);
-    else if (tf32) e = launch_kernel<kFmtTF32, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
-    else if (pair && bf16 && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtBF16, false, float>(ma, mb, p, dev, a.stream);
-    else if (pair && bf16) e = launch_pair_kernel<kFmtBF16, false, __nv_bfloat16>(ma, mb, p, dev, a.stream);
-    else if (pair && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtF16, false, float>(ma, mb, p, dev, a.stream);
-    else if (pair) e = launch_pair_kernel<kFmtF16, false, __half>(ma, mb, p, dev, a.stream);
-    else if (bf16 && a.out_dtype == DGA_F32) e = launch_kernel<kFmtBF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
-    else if (bf16) e = launch_kernel<kFmtBF16, false, kBnFloat, __nv_bfloat16>(ma, mb, p, dev, a.stream);
-    else if (a.out_dtype == DGA_F32) e = launch_kernel<kFmtF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream);
-    else e = launch_kernel<kFmtF16, false, kBnFloat, __half>(ma, mb, p, dev, a.stream);
+    if (i8 && pair) e = launch_pair_kernel<kFmtBF16, true, int32_t>(ma, mb, p, dev, a.stream, pdl);
+    else if (i8) e = launch_kernel<kFmtBF16, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream, pdl);
+    else if (tf32 && pair) e = launch_pair_kernel<kFmtTF32, false, float>(ma, mb, p, dev, a.stream, pdl);
+    else if (tf32) e = launch_kernel<kFmtTF32, false, kBnFloat, float>(ma, mb, p, dev, a.stream, pdl);
+    else if (pair && bf16 && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtBF16, false, float>(ma, mb, p, dev, a.stream, pdl);
+    else if (pair && bf16) e = launch_pair_kernel<kFmtBF16, false, __nv_bfloat16>(ma, mb, p, dev, a.stream, pdl);
+    else if (pair && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtF16, false, float>(ma, mb, p, dev, a.stream, pdl);
+    else if (pair) e = launch_pair_kernel<kFmtF16, false, __half>(ma, mb, p, dev, a.stream, pdl);
+    else if (bf16 && a.out_dtype == DGA_F32) e = launch_kernel<kFmtBF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream, pdl);
+    else if (bf16) e = launch_kernel<kFmtBF16, false, kBnFloat, __nv_bfloat16>(ma, mb, p, dev, a.stream, pdl);
+    else if (a.out_dtype == DGA_F32) e = launch_kernel<kFmtF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream, pdl);
+    else e = launch_kernel<kFmtF16, false, kBnFloat, __half>(ma, mb, p, dev, a.stream, pdl);
     if (e == cudaSuccess) ++*launches;
     return e;
 }

@@ -11,7 +11,7 @@
 // a fixed scratch area compiled into the library instead.
 //
 // The scratch is a file-scope __device__ array of DGA_NOALLOC_SCRATCH_BYTES
-// (64 MiB).  Every GPU on which this entry point is used holds it until the
+// (72 MiB).  Every GPU on which this entry point is used holds it until the
 // process exits.  All calls share it and it keeps the last call's contents;
 // nothing in it needs to start at zero, because each call rewrites every byte
 // it later reads (the repack writes whole padded rows).  Calls that overlap on
@@ -24,7 +24,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = 64ull << 20;
+constexpr size_t kScratchBytes = 72ull << 20;
 static_assert(kScratchBytes == DGA_NOALLOC_SCRATCH_BYTES, "header and library disagree");
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];

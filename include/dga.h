@@ -271,8 +271,11 @@ const char* dga_status_string(int status);
  * DGA_NOALLOC_SCRATCH_BYTES compiled into the library:
  *   - every GPU on which it is called holds that area until the process exits;
  *   - the call is refused with DGA_ERR_WORKSPACE, before anything is
- *     enqueued, when (M + N) * round_up(K, 8) * 2 bytes (the operands
- *     re-encoded as bf16) exceed it, e.g. M + N = 8192 at K = 4096 fits;
+ *     enqueued, when the operands re-encoded as bf16 exceed it: A takes
+ *     M * round_up(K, 8) * 2 bytes, B N * round_up(K, 8) * 2 bytes when
+ *     column-major and K * round_up(N, 8) * 2 bytes when row-major (each
+ *     rounded up to 256 bytes); e.g. M = 4093, N = 4099, K = 4096 with a
+ *     row-major B (64.04 MiB) fits;
  *   - all calls share the area and it keeps the last call's contents
  *     (nothing in it needs to start at zero: each call rewrites all it reads);
  *     calls that overlap on the GPU -- other streams, other host threads --
@@ -282,7 +285,7 @@ const char* dga_status_string(int status);
  * Argument errors are -(position in this function's argument list); other
  * codes as for dga_gemm_ex.
  */
-#define DGA_NOALLOC_SCRATCH_BYTES (64ull << 20)
+#define DGA_NOALLOC_SCRATCH_BYTES (72ull << 20)
 int dga_gemm_i8_noalloc(dga_layout layout_b, int64_t M, int64_t N, int64_t K,
                         const int32_t* alpha, const int8_t* A, int64_t lda,
                         const int8_t* B, int64_t ldb, const int32_t* beta,

@@ -98,11 +98,14 @@ def test_workspace_size_query(lib):
     assert dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
                                        w.K, w.N, dga.PATH_TCGEN05) == 0
     # row-major B is read in place (MN-major) unless TMA cannot express its
-    # leading dimension; then it is transposed into the workspace
+    # leading dimension; then it is copied row by row (K rows of N, padded to
+    # 8 elements) and still read MN-major
     assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.ROW_MAJOR, 256, 512, 100, 104,
                                        512, 512, dga.PATH_TCGEN05) == 0
     assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.ROW_MAJOR, 256, 512, 100, 104,
-                                       513, 512, dga.PATH_TCGEN05) >= 512 * 104 * 2
+                                       513, 512, dga.PATH_TCGEN05) == 100 * 512 * 2
+    assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.ROW_MAJOR, 256, 510, 100, 104,
+                                       513, 510, dga.PATH_TCGEN05) == 100 * 512 * 2
     assert dga.dga_gemm_workspace_size(gen.F32, gen.F32, gen.ROW_MAJOR, 64, 64, 64, 64, 64, 64,
                                        dga.PATH_SIMT) == 0
     # TF32 reads K-major only: column-major B in place, a row-major B is

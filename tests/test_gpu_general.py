@@ -118,6 +118,18 @@ def test_tc_col_major_a_f16_bf16_out():
                   with_bias=False)
 
 
+@pytest.mark.parametrize("M", [77, 260])
+def test_tc_repack_keeps_mn_major(M):
+    # leading dimensions TMA cannot express (M + 3, N + 3: not multiples of 8)
+    # on a column-major A and a row-major B: each is copied row by row into
+    # the workspace in its own layout and read MN-major (single-CTA and
+    # CTA-pair kernels)
+    check_general(T, gen.BF16, gen.F32, gen.COL_MAJOR, gen.ROW_MAJOR, M, 140, 99, 1.0, 0.5,
+                  with_bias=False, pad=3)
+    check_general(T, gen.F16, gen.F16, gen.COL_MAJOR, gen.ROW_MAJOR, M, 140, 99, 1.0, 0.0,
+                  with_bias=True, pad=3, seed=1)
+
+
 @pytest.mark.parametrize("M,N,K", [(77, 91, 600), (259, 515, 1100)])
 def test_tc_int8_col_major_a(M, N, K):
     check_general(T, gen.I8, gen.I32, gen.COL_MAJOR, gen.ROW_MAJOR, M, N, K, 3, -2,

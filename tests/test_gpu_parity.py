@@ -157,6 +157,18 @@ def test_tc_int8_col_major_alpha_beta():
     check(T, gen.I8, gen.I32, gen.COL_MAJOR, 140, 270, 700, -3, 7, seed=3)
 
 
+def test_tc_int8_one_repack_launch():
+    # both operands are repacked (A by rows, row-major B transposed to K-major)
+    # in one launch, and the GEMM follows it as a programmatic dependent: two
+    # launches, the result still bit-exact (ragged sizes, ldb not a multiple of 16)
+    check(T, gen.I8, gen.I32, gen.ROW_MAJOR, 300, 259, 1030, 1, 0, seed=4, ldb=263)
+    assert dga.dga_last_launch_count() == 2
+    # bf16 with leading dimensions TMA cannot express (lda = 99, ldb = 101):
+    # both repacked, again in one launch
+    check(T, gen.BF16, gen.F32, gen.COL_MAJOR, 260, 140, 99, 1.0, 0.0, seed=5, ldb=101)
+    assert dga.dga_last_launch_count() == 2
+
+
 def test_tc_int8_extreme_magnitudes():
     # all -128: every product is +2^14, the largest partial sums there are
     M, N, K = 130, 260, 2048
