@@ -395,17 +395,20 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                         break;
                     }
                     tc_fence_after();
+                    // 16 columns per load: the 64 running sums and one load's
+                    // registers stay within the 96 registers a thread of this
+                    // 576-thread CTA has (32-column loads spilled)
 #pragma unroll
-                    for (int c = 0; c < kColsPerWarp / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(
-                            tmem_base + lane_base + acc * BN + col_half * kColsPerWarp + c * 32, r);
+                    for (int c = 0; c < kColsPerWarp / 16; ++c) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(
+                            tmem_base + lane_base + acc * BN + col_half * kColsPerWarp + c * 16, r);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
+                        for (int j = 0; j < 16; ++j) {
                             // exact integer in fp32 (|x| <= 2^24) -> int32, wrapping add
-                            sum[c * 32 + j] = static_cast<int32_t>(
-                                static_cast<uint32_t>(sum[c * 32 + j]) +
+                            sum[c * 16 + j] = static_cast<int32_t>(
+                                static_cast<uint32_t>(sum[c * 16 + j]) +
                                 static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j]))));
                         }
                     }
@@ -678,16 +681,17 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                         break;
                     }
                     tc_fence_after();
+                    // 16 columns per load (see the single-CTA kernel: no spills)
 #pragma unroll
-                    for (int c = 0; c < kColsPerWarp / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN +
-                                               col_group * kColsPerWarp + c * 32, r);
+                    for (int c = 0; c < kColsPerWarp / 16; ++c) {
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(tmem_base + lane_base + acc * kPairBN +
+                                               col_group * kColsPerWarp + c * 16, r);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            sum[c * 32 + j] = static_cast<int32_t>(
-                                static_cast<uint32_t>(sum[c * 32 + j]) +
+                        for (int j = 0; j < 16; ++j)
+                            sum[c * 16 + j] = static_cast<int32_t>(
+                                static_cast<uint32_t>(sum[c * 16 + j]) +
                                 static_cast<uint32_t>(__float2int_rn(__uint_as_float(r[j]))));
                     }
                     // every epilogue warp of this CTA has read the accumulator: one
@@ -781,6 +785,14 @@ struct PackJob {
     int64_t ld_dst;
     int vec_src;      // the source's 8-element groups are aligned
     int64_t blocks;   // blocks of the launch this job takes
+    // a thread's unit of work: 8 elements (16-bit sources) or 32 (int8) of a
+    // row; units_per_row = ld_dst / unit, rounded up
+    int64_t units_per_row;
+    // unit index i -> row i / units_per_row as (i * div_m) >> div_s, exact
+    // for i < 2^31 (a precomputed reciprocal: no division in the kernel);
+    // used when fast_div, i.e. when the job has fewer than 2^31 units
+    uint64_t div_m;
+    int div_s, fast_div;
 };
 
 // Eight int8 values (byte q of v is value q) as eight exact bf16, in memory
@@ -811,62 +823,86 @@ __device__ __forceinline__ uint64_t ldg_u64(uintptr_t a) {
     return __ldg(reinterpret_cast<const unsigned long long*>(a));
 }
 
-// One thread per 8 consecutive elements of a row (block-stride over
-// `nblocks` blocks, this one being `blk`).
+// Row r, position i of a job's units (unit_elems elements of a row per unit,
+// units_per_row units per row): r = i / units_per_row through the job's
+// precomputed reciprocal where it is exact.
+template <typename TSrc>
+__device__ __forceinline__ int64_t unit_row(const PackJob<TSrc>& j, int64_t i) {
+    if (j.fast_div) return static_cast<int64_t>((static_cast<uint64_t>(i) * j.div_m) >> j.div_s);
+    return i / j.units_per_row;
+}
+
+// 16-bit sources: one thread per 8 consecutive elements of a row (block-stride
+// over `nblocks` blocks, this one being `blk`), copied bit for bit.
 template <typename TSrc>
 __device__ __forceinline__ void pack_rows_body(const PackJob<TSrc>& j, int64_t blk, int64_t nblocks) {
     const TSrc* __restrict__ src = j.src;
     uint16_t* __restrict__ dst = j.dst;
     const int64_t ld_src = j.ld_src, K = j.K, ld_dst = j.ld_dst;
-    const int vec_src = j.vec_src;
-    const int64_t groups = ld_dst / 8;
-    const int64_t total = j.rows * groups;
+    const int64_t total = j.rows * j.units_per_row;
     for (int64_t i = blk * 256 + threadIdx.x; i < total; i += nblocks * 256) {
-        const int64_t r = i / groups, k = (i % groups) * 8;
+        const int64_t r = unit_row(j, i), k = (i - r * j.units_per_row) * 8;
         const TSrc* s = src + r * ld_src + k;
-        if constexpr (sizeof(TSrc) == 1) {
-            // int8: the 8 bytes as one 64-bit word -- one aligned load, or for
-            // a row that is not 8-byte aligned the two aligned words around
-            // them, funnel-shifted (only where both words lie inside the
-            // operand: [src, src_end)); bytewise at the edges
-            uint64_t v = 0;
-            bool have = false;
-            if (k + 8 <= K) {
-                const uintptr_t a = reinterpret_cast<uintptr_t>(s);
-                if (vec_src) {
-                    v = ldg_u64(a);
+        uint16_t h[8];
+        if (j.vec_src && k + 8 <= K) {
+            TSrc v[8];
+            *reinterpret_cast<uint4*>(v) = __ldg(reinterpret_cast<const uint4*>(s));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) h[q] = PackIn<TSrc>::bits(v[q]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) h[q] = k + q < K ? PackIn<TSrc>::bits(s[q]) : uint16_t(0);
+        }
+        *reinterpret_cast<uint4*>(dst + r * ld_dst + k) = pack8(h);
+    }
+}
+
+// int8 sources: one thread per 32 consecutive elements of a row (four output
+// vectors of 8 bf16).  The 32 bytes are four 64-bit words: four aligned loads
+// for a row that is 8-byte aligned, else the five aligned words around them,
+// funnel-shifted (only where all five lie inside the operand: [src,
+// src_end)); bytewise at the row's end and at the operand's edges.
+template <>
+__device__ __forceinline__ void pack_rows_body<int8_t>(const PackJob<int8_t>& j, int64_t blk,
+                                                       int64_t nblocks) {
+    const int8_t* __restrict__ src = j.src;
+    uint16_t* __restrict__ dst = j.dst;
+    const int64_t ld_src = j.ld_src, K = j.K, ld_dst = j.ld_dst;
+    const int64_t total = j.rows * j.units_per_row;
+    for (int64_t i = blk * 256 + threadIdx.x; i < total; i += nblocks * 256) {
+        const int64_t r = unit_row(j, i), k0 = (i - r * j.units_per_row) * 32;
+        const int8_t* s = src + r * ld_src + k0;
+        uint64_t w[4] = {0, 0, 0, 0};
+        bool have = false;
+        if (k0 + 32 <= K) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(s);
+            if (j.vec_src) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) w[u] = ldg_u64(a + 8 * u);
+                have = true;
+            } else {
+                const uintptr_t base = a & ~static_cast<uintptr_t>(7);
+                if (base >= reinterpret_cast<uintptr_t>(src) &&
+                    base + 40 <= reinterpret_cast<uintptr_t>(j.src_end)) {
+                    uint64_t x[5];
+#pragma unroll
+                    for (int u = 0; u < 5; ++u) x[u] = ldg_u64(base + 8 * u);
+                    const int sh = static_cast<int>(a - base) * 8;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) w[u] = sh ? (x[u] >> sh) | (x[u + 1] << (64 - sh)) : x[u];
                     have = true;
-                } else {
-                    const uintptr_t base = a & ~static_cast<uintptr_t>(7);
-                    if (base >= reinterpret_cast<uintptr_t>(src) &&
-                        base + 16 <= reinterpret_cast<uintptr_t>(j.src_end)) {
-                        const uint64_t w0 = ldg_u64(base), w1 = ldg_u64(base + 8);
-                        const int sh = static_cast<int>(a - base) * 8;
-                        v = sh ? (w0 >> sh) | (w1 << (64 - sh)) : w0;
-                        have = true;
-                    }
                 }
             }
-            if (!have) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    if (k + q < K) v |= static_cast<uint64_t>(static_cast<uint8_t>(s[q])) << (8 * q);
-            }
-            *reinterpret_cast<uint4*>(dst + r * ld_dst + k) = int8x8_to_bf16(v);
-        } else {
-            // 16-bit data is copied bit for bit: 16 bytes in one load where aligned
-            uint16_t h[8];
-            if (vec_src && k + 8 <= K) {
-                TSrc v[8];
-                *reinterpret_cast<uint4*>(v) = __ldg(reinterpret_cast<const uint4*>(s));
-#pragma unroll
-                for (int q = 0; q < 8; ++q) h[q] = PackIn<TSrc>::bits(v[q]);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) h[q] = k + q < K ? PackIn<TSrc>::bits(s[q]) : uint16_t(0);
-            }
-            *reinterpret_cast<uint4*>(dst + r * ld_dst + k) = pack8(h);
         }
+        if (!have) {
+            for (int q = 0; q < 32; ++q)
+                if (k0 + q < K)
+                    w[q >> 3] |= static_cast<uint64_t>(static_cast<uint8_t>(s[q])) << (8 * (q & 7));
+        }
+        uint16_t* d = dst + r * ld_dst + k0;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (k0 + 8 * u < ld_dst) *reinterpret_cast<uint4*>(d + 8 * u) = int8x8_to_bf16(w[u]);
     }
 }
 
@@ -1163,9 +1199,20 @@ PackJob<TSrc> pack_job(const void* src, int64_t ld_src, int64_t rows, int64_t K,
                 aligned(src, 8 * sizeof(TSrc));
     // one 8-element group per thread where the launch allows (no dependent
     // loads chained through a block-stride loop)
-    const int64_t work = rows * (ld_dst / 8);
+    const int64_t unit = sizeof(TSrc) == 1 ? 32 : 8;
+    const int64_t upr = (ld_dst + unit - 1) / unit;
+    j.units_per_row = upr;
+    const int64_t work = rows * upr;
     j.blocks = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256,
                                                       static_cast<int64_t>(sm_count) * 256));
+    // division by an invariant integer as a multiply and a shift (Granlund and
+    // Montgomery): with l = ceil(log2 upr) and m = ceil(2^(31+l) / upr),
+    // floor(i / upr) = (i * m) >> (31 + l) for every 0 <= i < 2^31
+    j.fast_div = work < (int64_t{1} << 31) ? 1 : 0;
+    int l = 0;
+    while ((int64_t{1} << l) < upr) ++l;
+    j.div_s = 31 + l;
+    j.div_m = ((uint64_t{1} << (31 + l)) + static_cast<uint64_t>(upr) - 1) / static_cast<uint64_t>(upr);
     return j;
 }
 
