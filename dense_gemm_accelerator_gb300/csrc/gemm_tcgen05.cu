@@ -857,52 +857,58 @@ __device__ __forceinline__ void pack_rows_body(const PackJob<TSrc>& j, int64_t b
     }
 }
 
-// int8 sources: one thread per 32 consecutive elements of a row (four output
-// vectors of 8 bf16).  The 32 bytes are four 64-bit words: four aligned loads
-// for a row that is 8-byte aligned, else the five aligned words around them,
-// funnel-shifted (only where all five lie inside the operand: [src,
-// src_end)); bytewise at the row's end and at the operand's edges.
+// int8 sources: a warp's unit is 128 consecutive output vectors (8 bf16 each)
+// of one row, lane l taking vectors l, l + 32, l + 64 and l + 96, so every
+// warp-wide load reads 256 contiguous bytes and every warp-wide store writes
+// 512.  A vector's 8 source bytes are one aligned 64-bit word for a row that
+// is 8-byte aligned, else the two aligned words around them, funnel-shifted
+// (only where both lie inside the operand: [src, src_end)); bytewise at the
+// row's end and at the operand's edges.  All four vectors' loads are issued
+// before the first conversion.
 template <>
 __device__ __forceinline__ void pack_rows_body<int8_t>(const PackJob<int8_t>& j, int64_t blk,
                                                        int64_t nblocks) {
-    const int8_t* __restrict__ src = j.src;
-    uint16_t* __restrict__ dst = j.dst;
-    const int64_t ld_src = j.ld_src, K = j.K, ld_dst = j.ld_dst;
-    const int64_t total = j.rows * j.units_per_row;
-    for (int64_t i = blk * 256 + threadIdx.x; i < total; i += nblocks * 256) {
-        const int64_t r = unit_row(j, i), k0 = (i - r * j.units_per_row) * 32;
-        const int8_t* s = src + r * ld_src + k0;
-        uint64_t w[4] = {0, 0, 0, 0};
-        bool have = false;
-        if (k0 + 32 <= K) {
-            const uintptr_t a = reinterpret_cast<uintptr_t>(s);
-            if (j.vec_src) {
+    const int lane = threadIdx.x & 31;
+    const int64_t vec_per_row = j.ld_dst / 8;
+    const int64_t total = j.rows * j.units_per_row;  // warp units
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(j.src), hi = reinterpret_cast<uintptr_t>(j.src_end);
+    for (int64_t wu = blk * 8 + (threadIdx.x >> 5); wu < total; wu += nblocks * 8) {
+        const int64_t r = unit_row(j, wu), seg = wu - r * j.units_per_row;
+        const int8_t* row = j.src + r * j.ld_src;
+        uint64_t w[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) w[u] = ldg_u64(a + 8 * u);
-                have = true;
-            } else {
-                const uintptr_t base = a & ~static_cast<uintptr_t>(7);
-                if (base >= reinterpret_cast<uintptr_t>(src) &&
-                    base + 40 <= reinterpret_cast<uintptr_t>(j.src_end)) {
-                    uint64_t x[5];
-#pragma unroll
-                    for (int u = 0; u < 5; ++u) x[u] = ldg_u64(base + 8 * u);
-                    const int sh = static_cast<int>(a - base) * 8;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) w[u] = sh ? (x[u] >> sh) | (x[u + 1] << (64 - sh)) : x[u];
+        for (int q = 0; q < 4; ++q) {
+            const int64_t v = seg * 128 + lane + 32 * q;
+            const int64_t k = 8 * v;
+            w[q] = 0;
+            if (v >= vec_per_row) continue;
+            const uintptr_t a = reinterpret_cast<uintptr_t>(row + k);
+            bool have = false;
+            if (k + 8 <= j.K) {
+                if (j.vec_src) {
+                    w[q] = ldg_u64(a);
                     have = true;
+                } else {
+                    const uintptr_t base = a & ~static_cast<uintptr_t>(7);
+                    if (base >= lo && base + 16 <= hi) {
+                        const uint64_t x0 = ldg_u64(base), x1 = ldg_u64(base + 8);
+                        const int sh = static_cast<int>(a - base) * 8;
+                        w[q] = sh ? (x0 >> sh) | (x1 << (64 - sh)) : x0;
+                        have = true;
+                    }
                 }
             }
+            if (!have) {
+                for (int b = 0; b < 8; ++b)
+                    if (k + b < j.K) w[q] |= static_cast<uint64_t>(static_cast<uint8_t>(row[k + b])) << (8 * b);
+            }
         }
-        if (!have) {
-            for (int q = 0; q < 32; ++q)
-                if (k0 + q < K)
-                    w[q >> 3] |= static_cast<uint64_t>(static_cast<uint8_t>(s[q])) << (8 * (q & 7));
-        }
-        uint16_t* d = dst + r * ld_dst + k0;
+        uint16_t* d = j.dst + r * j.ld_dst;
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (k0 + 8 * u < ld_dst) *reinterpret_cast<uint4*>(d + 8 * u) = int8x8_to_bf16(w[u]);
+        for (int q = 0; q < 4; ++q) {
+            const int64_t v = seg * 128 + lane + 32 * q;
+            if (v < vec_per_row) *reinterpret_cast<uint4*>(d + 8 * v) = int8x8_to_bf16(w[q]);
+        }
     }
 }
 
@@ -1199,11 +1205,13 @@ PackJob<TSrc> pack_job(const void* src, int64_t ld_src, int64_t rows, int64_t K,
                 aligned(src, 8 * sizeof(TSrc));
     // one 8-element group per thread where the launch allows (no dependent
     // loads chained through a block-stride loop)
-    const int64_t unit = sizeof(TSrc) == 1 ? 32 : 8;
-    const int64_t upr = (ld_dst + unit - 1) / unit;
+    // a unit is 8 elements of a row per thread (16-bit sources) or 1024
+    // elements of a row per warp (int8, see pack_rows_body<int8_t>)
+    const int64_t upr = sizeof(TSrc) == 1 ? (ld_dst / 8 + 127) / 128 : ld_dst / 8;
     j.units_per_row = upr;
     const int64_t work = rows * upr;
-    j.blocks = std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256,
+    const int64_t per_block = sizeof(TSrc) == 1 ? 8 : 256;  // units a block takes at once
+    j.blocks = std::max<int64_t>(1, std::min<int64_t>((work + per_block - 1) / per_block,
                                                       static_cast<int64_t>(sm_count) * 256));
     // division by an invariant integer as a multiply and a shift (Granlund and
     // Montgomery): with l = ceil(log2 upr) and m = ceil(2^(31+l) / upr),
