@@ -478,9 +478,21 @@ def roofline_for(w, ms_mean, peaks, sustained=False, nnz=None):
                               w.in_dtype, "bf16 tensor")}
 
 
+def code_digest(path):
+    """First 16 hex digits of the SHA-256 of a CUDA source with its comments
+    and blank lines removed: a traffic record stays valid across edits that
+    change no code."""
+    import re
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def traffic_record(kernel_src, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current source of the kernel; else None."""
+    the current code of the kernel's source (comments aside); else None."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
@@ -492,10 +504,10 @@ def traffic_record(kernel_src, workload):
         return None
     src = os.path.join(ROOT, "dense_gemm_accelerator_gb300", "csrc", kernel_src)
     try:
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        digest = code_digest(src)
     except OSError:
         return None
-    if entry.get("source_sha256_16") != digest:
+    if entry.get("code_sha256_16") != digest:
         return None
     return entry.get("bytes_per_launch")
 

@@ -785,8 +785,9 @@ struct PackJob {
     int64_t ld_dst;
     int vec_src;      // the source's 8-element groups are aligned
     int64_t blocks;   // blocks of the launch this job takes
-    // a thread's unit of work: 8 elements (16-bit sources) or 32 (int8) of a
-    // row; units_per_row = ld_dst / unit, rounded up
+    // the unit of work: 8 elements of a row per thread (16-bit sources) or
+    // 1024 elements of a row per warp (int8); units_per_row = ld_dst / unit,
+    // rounded up
     int64_t units_per_row;
     // unit index i -> row i / units_per_row as (i * div_m) >> div_s, exact
     // for i < 2^31 (a precomputed reciprocal: no division in the kernel);
@@ -823,9 +824,8 @@ __device__ __forceinline__ uint64_t ldg_u64(uintptr_t a) {
     return __ldg(reinterpret_cast<const unsigned long long*>(a));
 }
 
-// Row r, position i of a job's units (unit_elems elements of a row per unit,
-// units_per_row units per row): r = i / units_per_row through the job's
-// precomputed reciprocal where it is exact.
+// The row of a job's unit i (units_per_row units per row): i / units_per_row
+// through the job's precomputed reciprocal where it is exact.
 template <typename TSrc>
 __device__ __forceinline__ int64_t unit_row(const PackJob<TSrc>& j, int64_t i) {
     if (j.fast_div) return static_cast<int64_t>((static_cast<uint64_t>(i) * j.div_m) >> j.div_s);

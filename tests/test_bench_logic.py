@@ -100,3 +100,16 @@ def test_reference_arm_rank0_only_under_torchrun():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_code_digest_ignores_comments_only(tmp_path):
+    # a traffic record stays valid across comment edits and is dropped when code changes
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("// header\nint f(int x) {\n    return x + 1;  // add one\n}\n")
+    b = tmp_path / "b.cu"
+    b.write_text("/* another\n   header */\nint f(int x) {\n\n    return x + 1;\n}\n")
+    c = tmp_path / "c.cu"
+    c.write_text("int f(int x) {\n    return x + 2;\n}\n")
+    assert bench.code_digest(str(a)) == bench.code_digest(str(b))
+    assert bench.code_digest(str(a)) != bench.code_digest(str(c))
