@@ -610,6 +610,30 @@ def e2e_leg(w, steps, warmup, device):
 
 # ------------------------------------------------------- CPU oracle timing --
 
+def cpu_model():
+    """The host CPU's model name from /proc/cpuinfo; on Arm hosts, which list
+    no model name, the machine type with the first core's implementer and
+    part codes."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" not in line:
+                    continue
+                key, val = (x.strip() for x in line.split(":", 1))
+                fields.setdefault(key.lower(), val)
+    except OSError:
+        pass
+    for key in ("model name", "cpu model"):
+        if key in fields:
+            return fields[key]
+    if "cpu part" in fields:
+        return (f"{platform.machine()} (implementer {fields.get('cpu implementer', '?')}, "
+                f"part {fields['cpu part']})")
+    return platform.machine()
+
+
 class OracleSample:
     """Times the CPU oracle, as it stands, on the first `rows` output rows of
     the workload (all N columns, full K), on this host's cores."""
@@ -697,6 +721,7 @@ def reference_arm(args, w):
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha,
                        "beta": w.beta},
             "cpu_baseline": {"value": val, "unit": unit, "cores": sampler.threads, "kind": "oracle",
+                             "cpu": cpu_model(),
                              "sample": f"first {rows} of {w.M} output rows, all {w.N} columns, "
                                        f"full K={w.K}, per step"},
             "e2e": {"value": val, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -861,6 +886,7 @@ def main():
         dt = sampler.run(rows)
         rate = gemm_flops(rows, w.N, w.K) / dt
         line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOPS", "cores": sampler.threads,
+                                "cpu": cpu_model(),
                                 "kind": "oracle",
                                 "sample": f"first {rows} of {w.M} output rows (all {w.N} columns, "
                                           f"K={w.K}) in {dt:.1f} s"}
