@@ -93,23 +93,25 @@ __device__ __forceinline__ float ld_stream(const float* q) {
     return v;
 }
 
-// Loads the row ends of rows r + k (k = k0 + lane < k_end) into the warp's
-// window as offsets from the chunk's first nonzero z, clamped to [0, nz_max];
-// checks each against the offset before it (row offsets must not decrease);
-// returns whether this lane's row end falls inside the chunk's n_items.
-__device__ __forceinline__ bool load_row_ends(const SpParams& p, int32_t* endl, int64_t r, int64_t z,
+// Loads the row ends of rows r + k (k = k0 + lane < k_end; offs_r = the
+// row offsets from row r on) into the warp's window as offsets from the
+// chunk's first nonzero z, clamped to [0, nz_max]; checks each against the
+// offset before it (row offsets must not decrease); returns whether this
+// lane's row end falls inside the chunk's n_items.  32-bit throughout: rows
+// and nonzeros are below 2^31.
+__device__ __forceinline__ bool load_row_ends(const int32_t* offs_r, int nnz, int32_t* endl, int z,
                                               int k0, int k_end, int nz_max, int n_items) {
     const int lane = threadIdx.x & 31;
     const int k = k0 + lane;
-    int64_t raw = 0;
-    if (k < k_end) raw = p.offs[r + k + 1];
+    int raw = 0;
+    if (k < k_end) raw = offs_r[k + 1];
     // the offset before: the previous lane's, or for lane 0 the row start
-    int64_t before = __shfl_up_sync(0xffffffffu, raw, 1);
-    if (lane == 0 && k < k_end) before = p.offs[r + k];
+    int before = __shfl_up_sync(0xffffffffu, raw, 1);
+    if (lane == 0 && k < k_end) before = offs_r[k];
     if (k < k_end && raw < before) flag_bad();
     if (k >= k_end) return false;
-    if (raw < 0 || raw > p.nnz) flag_bad();
-    const int e = static_cast<int>(lmin(lmin(raw < 0 ? 0 : raw, p.nnz) - z, nz_max));
+    if (raw < 0 || raw > nnz) flag_bad();
+    const int e = min(min(max(raw, 0), nnz) - z, nz_max);
     endl[k] = e < 0 ? 0 : e;
     return k + endl[k] < n_items;
 }
@@ -173,18 +175,26 @@ __global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
     const int64_t per_sm = p.ctas / p.sms;
     const int64_t logical = p.ctas % p.sms == 0 ? (b % p.sms) * per_sm + b / p.sms : b;
     const int64_t w = logical * (kThreads / 32) + (threadIdx.x >> 5);
-    const int64_t d_end = (w + 1) * p.items / warps;
-    int64_t r = warp_merge_search(p, w * p.items / warps);
-    int64_t z = w * p.items / warps - r;
+    const int64_t d_begin = w * p.items / warps;
+    const int64_t r0 = warp_merge_search(p, d_begin);
     if (w == 0 && lane == 0 && p.rows > 0 &&
         (p.offs[0] != 0 || static_cast<int64_t>(p.offs[p.rows]) != p.nnz))
         flag_bad();
+    // rows and nonzeros are below 2^31 (the entry point checks), and a share
+    // holds at most items / 8 < 2^29 merge items: 32-bit counters from here
+    const int rows = static_cast<int>(p.rows), nnz = static_cast<int>(p.nnz);
+    int r = static_cast<int>(r0), z = static_cast<int>(d_begin - r0);
+    int left = static_cast<int>((w + 1) * p.items / warps - d_begin);  // merge items still to do
     float carry = 0.0f;  // partial sum of row r carried from earlier chunks of this warp
 
-    while (r + z < d_end) {
-        const int n_items = static_cast<int>(lmin(kWarpChunk, d_end - (r + z)));
-        const int rows_max = static_cast<int>(lmin(n_items, p.rows - r));  // row ends it may hold
-        const int nz_max = static_cast<int>(lmin(n_items, p.nnz - z));     // nonzeros it may hold
+    while (left > 0) {
+        const int n_items = min(kWarpChunk, left);
+        const int rows_max = min(n_items, rows - r);  // row ends it may hold
+        const int nz_max = min(n_items, nnz - z);     // nonzeros it may hold
+        const int32_t* cidx_z = p.cidx + z;
+        const float* vals_z = p.vals + z;
+        const int32_t* offs_r = p.offs + r;
+        float* y_r = p.y + r;
         // values and column indices of every nonzero the chunk may hold (those
         // past its split are read again, from L1/L2, by the next chunk), and
         // the first 32 row ends, in one round trip
@@ -196,20 +206,20 @@ __global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
             col[u] = -1;
             val[u] = 0.0f;
             if (k < nz_max) {
-                col[u] = ld_stream(p.cidx + z + k);
-                val[u] = ld_stream(p.vals + z + k);
+                col[u] = ld_stream(cidx_z + k);
+                val[u] = ld_stream(vals_z + k);
             }
         }
         // row end k sits at merge position k + (its end - z) of the chunk;
         // those inside the chunk are a prefix of the rows
         int win = min(32, rows_max);
         int c_rows = __popc(__ballot_sync(
-            0xffffffffu, load_row_ends(p, sm.endl, r, z, 0, win, nz_max, n_items)));
+            0xffffffffu, load_row_ends(offs_r, nnz, sm.endl, z, 0, win, nz_max, n_items)));
         while (c_rows == win && win < rows_max) {  // every row of the window closes: widen it
             const int k0 = win;
             win = min(win + 32, rows_max);
             c_rows += __popc(__ballot_sync(
-                0xffffffffu, load_row_ends(p, sm.endl, r, z, k0, win, nz_max, n_items)));
+                0xffffffffu, load_row_ends(offs_r, nnz, sm.endl, z, k0, win, nz_max, n_items)));
         }
         int c_nz = n_items - c_rows;
         if (c_nz > nz_max) {  // only for malformed offsets: keep every index in range
@@ -256,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
             if (k == rs) {
                 head = run;  // closes a row that may have begun in earlier lanes
             } else {
-                float* dst = p.y + (r + k);  // the whole row lies in this lane's items
+                float* dst = y_r + k;  // the whole row lies in this lane's items
                 const float old = p.beta != 0.0f ? *dst : 0.0f;
                 *dst = fmaf(p.beta, old, p.alpha * run);
             }
@@ -283,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
         const int lane_f = __shfl_up_sync(0xffffffffu, f, 1);
         const float carry_in = lane == 0 ? carry : (lane_f ? lane_v : carry + lane_v);
         if (has_end) {
-            float* dst = p.y + (r + rs);
+            float* dst = y_r + rs;
             const float old = p.beta != 0.0f ? *dst : 0.0f;
             *dst = fmaf(p.beta, old, p.alpha * (carry_in + head));
         }
@@ -293,11 +303,12 @@ __global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
         carry = tot_f ? tot_v : carry + tot_v;
         r += c_rows;
         z += c_nz;
+        left -= c_rows + c_nz;
         __syncwarp();  // the warp's shared arrays are reused by the next chunk
     }
     if (lane == 0) {
         // row r has not closed in this warp: its partial sum goes to the next one
-        p.carry_row[w] = static_cast<int32_t>(lmin(r, 0x7fffffff));
+        p.carry_row[w] = r;
         p.carry_val[w] = carry;
     }
 }
