@@ -13,7 +13,7 @@
 // lengths, and inside a chunk every lane takes 8 consecutive items.
 //
 //  * Warps are independent workers: no block-wide barrier anywhere, so while
-//    one warp waits on its loads the SM runs the others (48 warps per SM).
+//    one warp waits on its loads the SM runs the others (32 warps per SM).
 //  * Start: a warp finds where its share begins (how many row ends and
 //    nonzeros precede it) with a search over row_offsets in which each lane
 //    probes one of 32 positions per round: 5 dependent rounds for 4M rows.
@@ -24,6 +24,10 @@
 //    (row end k sits at k + its end offset within the chunk) counts how many
 //    of them fall inside the chunk (more row ends are loaded, 32 at a time,
 //    when all do); then it gathers x and keeps the products in shared memory.
+//    A chunk's own loads are issued one chunk ahead, as soon as the previous
+//    chunk has counted its row ends (which fixes where the next one starts),
+//    so they travel while that chunk gathers and sums: a chunk then waits on
+//    one round trip, its gathers, instead of two.
 //  * Lane ownership: a shared-memory count of the row ends falling in each
 //    lane's 8 items and a warp prefix sum tell every lane which row ends it
 //    closes; it sums the products between them (a tight loop over shared
@@ -116,6 +120,34 @@ __device__ __forceinline__ bool load_row_ends(const int32_t* offs_r, int nnz, in
     return k + endl[k] < n_items;
 }
 
+// The same in two halves, so that a chunk's first window of row ends can be
+// loaded while the previous chunk is still being processed: the loads
+// (this lane's row end and, for lane 0, the offset before the window) ...
+__device__ __forceinline__ void row_ends_issue(const int32_t* offs_r, int k_end, int& raw,
+                                               int& before0) {
+    const int lane = threadIdx.x & 31;
+    raw = 0;
+    before0 = 0;
+    if (lane < k_end) {
+        raw = offs_r[lane + 1];
+        if (lane == 0) before0 = offs_r[0];
+    }
+}
+
+// ... and the rest, once the chunk's first nonzero z is known.
+__device__ __forceinline__ bool row_ends_consume(int raw, int before0, int nnz, int32_t* endl, int z,
+                                                 int k_end, int nz_max, int n_items) {
+    const int lane = threadIdx.x & 31;
+    int before = __shfl_up_sync(0xffffffffu, raw, 1);
+    if (lane == 0) before = before0;
+    if (lane < k_end && raw < before) flag_bad();
+    if (lane >= k_end) return false;
+    if (raw < 0 || raw > nnz) flag_bad();
+    const int e = min(min(max(raw, 0), nnz) - z, nz_max);
+    endl[lane] = e < 0 ? 0 : e;
+    return lane + endl[lane] < n_items;
+}
+
 // Row end i (i < rows) as a position in the nonzero list, clamped to [0, nnz].
 __device__ __forceinline__ int64_t row_end(const SpParams& p, int64_t i) {
     int64_t v = p.offs[i + 1];
@@ -161,7 +193,7 @@ struct WarpSmem {
     int owned[32];                         // row ends among each lane's items
 };
 
-__global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
+__global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
     __shared__ WarpSmem s_all[kThreads / 32];
     const int lane = threadIdx.x & 31;
     WarpSmem& sm = s_all[threadIdx.x >> 5];
@@ -187,34 +219,40 @@ __global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
     int left = static_cast<int>((w + 1) * p.items / warps - d_begin);  // merge items still to do
     float carry = 0.0f;  // partial sum of row r carried from earlier chunks of this warp
 
-    while (left > 0) {
-        const int n_items = min(kWarpChunk, left);
-        const int rows_max = min(n_items, rows - r);  // row ends it may hold
-        const int nz_max = min(n_items, nnz - z);     // nonzeros it may hold
-        const int32_t* cidx_z = p.cidx + z;
-        const float* vals_z = p.vals + z;
-        const int32_t* offs_r = p.offs + r;
-        float* y_r = p.y + r;
-        // values and column indices of every nonzero the chunk may hold (those
-        // past its split are read again, from L1/L2, by the next chunk), and
-        // the first 32 row ends, in one round trip
-        int32_t col[kIpt];
-        float val[kIpt];
+    // A chunk's loads: the values and column indices of every nonzero it may
+    // hold (those past its split are read again, from L1/L2, by the next
+    // chunk) and its first 32 row ends.  They are issued one chunk ahead --
+    // while the previous chunk gathers x and sums -- so that a chunk waits on
+    // one round trip (its gathers) instead of two.
+    int32_t col[kIpt];
+    float val[kIpt];
+    int raw0 = 0, before0 = 0;
+    auto issue = [&](int zz, int rr, int nzm, int win0) {
 #pragma unroll
         for (int u = 0; u < kIpt; ++u) {
             const int k = u * 32 + lane;
             col[u] = -1;
             val[u] = 0.0f;
-            if (k < nz_max) {
-                col[u] = ld_stream(cidx_z + k);
-                val[u] = ld_stream(vals_z + k);
+            if (k < nzm) {
+                col[u] = ld_stream(p.cidx + zz + k);
+                val[u] = ld_stream(p.vals + zz + k);
             }
         }
+        row_ends_issue(p.offs + rr, win0, raw0, before0);
+    };
+    int n_items = min(kWarpChunk, left);
+    int rows_max = min(n_items, rows - r);  // row ends the chunk may hold
+    int nz_max = min(n_items, nnz - z);     // nonzeros the chunk may hold
+    if (left > 0) issue(z, r, nz_max, min(32, rows_max));
+
+    while (left > 0) {
+        const int32_t* offs_r = p.offs + r;
+        float* y_r = p.y + r;
         // row end k sits at merge position k + (its end - z) of the chunk;
         // those inside the chunk are a prefix of the rows
         int win = min(32, rows_max);
         int c_rows = __popc(__ballot_sync(
-            0xffffffffu, load_row_ends(offs_r, nnz, sm.endl, z, 0, win, nz_max, n_items)));
+            0xffffffffu, row_ends_consume(raw0, before0, nnz, sm.endl, z, win, nz_max, n_items)));
         while (c_rows == win && win < rows_max) {  // every row of the window closes: widen it
             const int k0 = win;
             win = min(win + 32, rows_max);
@@ -226,21 +264,36 @@ __global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
             flag_bad();
             c_nz = nz_max;
         }
-        // gather x and keep the products of the chunk's nonzeros
+        // gather x (the loads first, all in flight together)
+        float xv[kIpt];
 #pragma unroll
         for (int u = 0; u < kIpt; ++u) {
             const int k = u * 32 + lane;
+            xv[u] = 0.0f;
             if (k < c_nz) {
-                float xv = 0.0f;
-                if (col[u] >= 0 && col[u] < p.cols) xv = __ldg(p.x + col[u]);
+                if (col[u] >= 0 && col[u] < p.cols) xv[u] = __ldg(p.x + col[u]);
                 else flag_bad();
-                sm.prod[pad(k)] = val[u] * xv;
             }
+        }
+        // this chunk's products, then the next chunk's loads (in flight while
+        // this chunk is summed and written)
+#pragma unroll
+        for (int u = 0; u < kIpt; ++u) {
+            const int k = u * 32 + lane;
+            if (k < c_nz) sm.prod[pad(k)] = val[u] * xv[u];
+        }
+        const int chunk_items = n_items, chunk_nz = c_nz;
+        const int r_next = r + c_rows, z_next = z + c_nz, left_next = left - (c_rows + c_nz);
+        if (left_next > 0) {
+            n_items = min(kWarpChunk, left_next);
+            rows_max = min(n_items, rows - r_next);
+            nz_max = min(n_items, nnz - z_next);
+            issue(z_next, r_next, nz_max, min(32, rows_max));
         }
         sm.owned[lane] = 0;
         __syncwarp();
         for (int k = lane; k < c_rows; k += 32) {
-            const int pos = min(k + sm.endl[k], n_items - 1);
+            const int pos = min(k + sm.endl[k], chunk_items - 1);
             atomicAdd(&sm.owned[pos / kIpt], 1);  // the lane whose items hold this row end
         }
         __syncwarp();
@@ -256,9 +309,9 @@ __global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
         }
         const int rs = incl - owned;
         const int re = min(incl, c_rows);
-        const int items_here = max(0, min(kIpt, n_items - lane * kIpt));
-        int nz = min(max(lane * kIpt - rs, 0), c_nz);
-        const int nz_end = min(max(nz + items_here - owned, nz), c_nz);
+        const int items_here = max(0, min(kIpt, chunk_items - lane * kIpt));
+        int nz = min(max(lane * kIpt - rs, 0), chunk_nz);
+        const int nz_end = min(max(nz + items_here - owned, nz), chunk_nz);
         float run = 0.0f, head = 0.0f;
         for (int k = rs; k < re; ++k) {
             const int e = min(max(sm.endl[k], nz), nz_end);
@@ -301,9 +354,9 @@ __global__ void __launch_bounds__(kThreads, 5) spmv_merge_kernel(SpParams p) {
         const float tot_v = __shfl_sync(0xffffffffu, v, 31);
         const int tot_f = __shfl_sync(0xffffffffu, f, 31);
         carry = tot_f ? tot_v : carry + tot_v;
-        r += c_rows;
-        z += c_nz;
-        left -= c_rows + c_nz;
+        r = r_next;
+        z = z_next;
+        left = left_next;
         __syncwarp();  // the warp's shared arrays are reused by the next chunk
     }
     if (lane == 0) {
