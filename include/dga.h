@@ -146,7 +146,9 @@ int dga_gemm(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
  * -9 A, -10 lda, -11 B, -12 ldb, -13 beta, -14 C, -15 ldc, -17 workspace,
  * -19 path; the bias must not overlap C (DGA_ERR_OVERLAP).  Other arguments
  * as for dga_gemm_ex.  The SKINNY family needs a row-major A; the tensor-core
- * family repacks a column-major A into the workspace.
+ * family reads a column-major A in place (MN-major) and copies it into the
+ * workspace only for INT8 (re-encoded as bf16, layout kept), for TF32
+ * (transposed to K-major) or when TMA cannot express lda.
  */
 int dga_gemm_general(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_a,
                      dga_layout layout_b, int64_t M, int64_t N, int64_t K,
