@@ -28,10 +28,14 @@
 //    chunk has counted its row ends (which fixes where the next one starts),
 //    so they travel while that chunk gathers and sums: a chunk then waits on
 //    one round trip, its gathers, instead of two.
-//  * Lane ownership: a shared-memory count of the row ends falling in each
-//    lane's 8 items and a warp prefix sum tell every lane which row ends it
-//    closes; it sums the products between them (a tight loop over shared
-//    memory, padded so that the lanes' runs fall on different banks).  A row
+//  * Lane ownership: in the usual chunk (at most 32 row ends) lane l holds
+//    the nonzeros 8l .. 8l+7 and closes the rows whose last nonzero is
+//    among them; it reads its 8 products as two 16-byte vectors (a padding
+//    that keeps them on distinct banks) and sums them in registers.  A chunk
+//    with more row ends gives each lane 8 consecutive merge items instead, so
+//    that no lane closes more than 8 rows.  Either way a shared-memory count
+//    of each lane's row ends and a warp prefix sum tell every lane which
+//    row ends it closes.  A row
 //    that starts and ends inside one lane is written at once; the first row
 //    a lane closes may have begun in earlier lanes or chunks, so a warp-wide
 //    segmented scan of the lanes' trailing partial sums, seeded with the
@@ -189,9 +193,16 @@ __device__ __forceinline__ int pad(int k) { return k + (k >> 5); }
 // Per-warp shared memory.
 struct WarpSmem {
     int32_t endl[kWarpChunk];              // chunk rows' end offsets, relative to the chunk's first nonzero
-    float prod[kWarpChunk + kWarpChunk / 32];  // products of the chunk's nonzeros (padded)
+    // products of the chunk's nonzeros, padded (pad(k), or padv(k) in chunks
+    // read by nonzero ownership: see the kernel)
+    __align__(16) float prod[kWarpChunk + kWarpChunk / 8];
     int owned[32];                         // row ends among each lane's items
 };
+
+// Shared-memory index of product k when lane l reads its products 8l .. 8l+7
+// as two 16-byte vectors: 4 floats of padding per 32 put the 8 lanes of each
+// quarter-warp phase on 8 different 4-bank groups.
+__device__ __forceinline__ int padv(int k) { return k + ((k >> 5) << 2); }
 
 __global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
     __shared__ WarpSmem s_all[kThreads / 32];
@@ -264,6 +275,15 @@ __global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
             flag_bad();
             c_nz = nz_max;
         }
+        // Which lane closes which row (warp-uniform choice).  A chunk with at
+        // most 32 row ends (the usual case) gives lane l the nonzeros
+        // [8l, 8l + 8) and each row end to the lane holding the row's last
+        // nonzero (lane 0 for a row with none in the chunk); the lane reads
+        // its 8 products as two 16-byte vectors and sums them in registers.
+        // A chunk with more row ends (mostly empty rows) gives lane l the
+        // merge items [8l, 8l + 8) instead, row ends included, so that no
+        // lane closes more than 8 rows.
+        const bool by_nz = c_rows <= 32;
         // gather x (the loads first, all in flight together)
         float xv[kIpt];
 #pragma unroll
@@ -280,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
 #pragma unroll
         for (int u = 0; u < kIpt; ++u) {
             const int k = u * 32 + lane;
-            if (k < c_nz) sm.prod[pad(k)] = val[u] * xv[u];
+            if (k < c_nz) sm.prod[by_nz ? padv(k) : pad(k)] = val[u] * xv[u];
         }
         const int chunk_items = n_items, chunk_nz = c_nz;
         const int r_next = r + c_rows, z_next = z + c_nz, left_next = left - (c_rows + c_nz);
@@ -293,8 +313,9 @@ __global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
         sm.owned[lane] = 0;
         __syncwarp();
         for (int k = lane; k < c_rows; k += 32) {
-            const int pos = min(k + sm.endl[k], chunk_items - 1);
-            atomicAdd(&sm.owned[pos / kIpt], 1);  // the lane whose items hold this row end
+            const int e = sm.endl[k];
+            const int owner = by_nz ? (e > 0 ? (e - 1) / kIpt : 0) : min(k + e, chunk_items - 1) / kIpt;
+            atomicAdd(&sm.owned[owner], 1);
         }
         __syncwarp();
 
@@ -309,23 +330,56 @@ __global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
         }
         const int rs = incl - owned;
         const int re = min(incl, c_rows);
-        const int items_here = max(0, min(kIpt, chunk_items - lane * kIpt));
-        int nz = min(max(lane * kIpt - rs, 0), chunk_nz);
-        const int nz_end = min(max(nz + items_here - owned, nz), chunk_nz);
         float run = 0.0f, head = 0.0f;
-        for (int k = rs; k < re; ++k) {
-            const int e = min(max(sm.endl[k], nz), nz_end);
-            for (; nz < e; ++nz) run += sm.prod[pad(nz)];
+        // closes row end k with the running sum: the lane's first row end
+        // (which may have begun in earlier lanes) waits for the scan below
+        auto close_row = [&](int k) {
             if (k == rs) {
-                head = run;  // closes a row that may have begun in earlier lanes
+                head = run;
             } else {
                 float* dst = y_r + k;  // the whole row lies in this lane's items
                 const float old = p.beta != 0.0f ? *dst : 0.0f;
                 *dst = fmaf(p.beta, old, p.alpha * run);
             }
             run = 0.0f;
+        };
+        if (by_nz) {
+            const int base = lane * kIpt;
+            const float4 q0 = *reinterpret_cast<const float4*>(&sm.prod[padv(base)]);
+            const float4 q1 = *reinterpret_cast<const float4*>(&sm.prod[padv(base) + 4]);
+            float pv[kIpt] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+            for (int t = 0; t < kIpt; ++t)
+                if (base + t >= chunk_nz) pv[t] = 0.0f;
+            // row end k (rs <= k < re) closes before product endl[k] - base,
+            // a position in 0 .. 8
+            int k = rs;
+            int at = k < re ? sm.endl[k] - base : kIpt + 1;
+#pragma unroll
+            for (int t = 0; t < kIpt; ++t) {
+                while (at == t) {
+                    close_row(k);
+                    ++k;
+                    at = k < re ? sm.endl[k] - base : kIpt + 1;
+                }
+                run += pv[t];
+            }
+            while (at == kIpt) {
+                close_row(k);
+                ++k;
+                at = k < re ? sm.endl[k] - base : kIpt + 1;
+            }
+        } else {
+            const int items_here = max(0, min(kIpt, chunk_items - lane * kIpt));
+            int nz = min(max(lane * kIpt - rs, 0), chunk_nz);
+            const int nz_end = min(max(nz + items_here - owned, nz), chunk_nz);
+            for (int k = rs; k < re; ++k) {
+                const int e = min(max(sm.endl[k], nz), nz_end);
+                for (; nz < e; ++nz) run += sm.prod[pad(nz)];
+                close_row(k);
+            }
+            for (; nz < nz_end; ++nz) run += sm.prod[pad(nz)];
         }
-        for (; nz < nz_end; ++nz) run += sm.prod[pad(nz)];
 
         // --- segmented scan of (has_end, tail) over the lanes, the warp's
         // carry first: combine(a, b) = (a.f | b.f, b.f ? b.v : a.v + b.v)
