@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
         }
         __syncwarp();
 
-        // --- this lane's items [lane*kIpt, +kIpt): row ends rs .. re-1, and the
+        // --- this lane's row ends rs .. re-1 (from the counts), and the
         // nonzeros before, between and after them
         const int owned = sm.owned[lane];
         int incl = owned;
