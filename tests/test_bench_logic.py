@@ -113,3 +113,22 @@ def test_code_digest_ignores_comments_only(tmp_path):
     c.write_text("int f(int x) {\n    return x + 2;\n}\n")
     assert bench.code_digest(str(a)) == bench.code_digest(str(b))
     assert bench.code_digest(str(a)) != bench.code_digest(str(c))
+
+
+def test_spec_peak_fields():
+    # bf16-rate tensor rows also quote the unit-count peak: SMs x 8192 FLOP/clk
+    # at the maximum and at the sampled clock; TF32 and non-tensor rows do not
+    import bench
+    peaks = {"sm_count": 152, "sm_max_mhz": 2070.0}
+    rf = {"bound": "tensor", "achieved": 1800.0, "peak_kind": "bf16 tensor"}
+    bench.add_spec_peak(rf, peaks, 1035.0)
+    at_max = 152 * 8192 * 2070e6 / 1e12
+    assert abs(rf["spec"]["at_max_clock"] - at_max) < 1e-9
+    assert abs(rf["spec"]["frac_at_max_clock"] - 1800.0 / at_max) < 1e-12
+    assert abs(rf["spec"]["at_observed_clock"] - at_max / 2) < 1e-9
+    tf32 = {"bound": "tensor", "achieved": 900.0, "peak_kind": "tf32 tensor (measured bf16 x nominal 1.1/2.25)"}
+    bench.add_spec_peak(tf32, peaks, 2070.0)
+    assert "spec" not in tf32
+    hbm = {"bound": "hbm", "achieved": 6000.0}
+    bench.add_spec_peak(hbm, peaks, 2070.0)
+    assert "spec" not in hbm
