@@ -452,6 +452,6 @@ const char* dga_status_string(int status) {
     }
 }
 
-int dga_version(void) { return 100; }
+int dga_version(void) { return 200; }  // 0.2.0: the FP32 FMA-rate probe; 72 MiB no-alloc scratch
 
 }  // extern "C"
