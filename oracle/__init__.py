@@ -14,8 +14,10 @@ returns the per-element error bound
     bound = rel * sum_k |alpha * a_ik * b_kj| + |beta * c_ij| * 2**-22
 
 with rel = 1e-4, or 2**-9 + 2**-20 + 1e-4 for TF32 inputs (fp32 operands
-whose products the tensor cores form at 10 fraction bits), plus
-``ulp_bf16(ref)`` for bf16 output, via :func:`ulp_bf16`.
+whose products the tensor cores form at 10 fraction bits), plus one
+output-rounding ulp of ref for 16-bit output (:func:`ulp_bf16`,
+:func:`ulp_f16`).  :func:`round_bf16` and :func:`round_f16` give the
+nearest-even 16-bit encodings that exact cases must match.
 
 It also holds the CSR sparse matrix-vector product of the same page
 (sections "CSR" and "SpMV"): ``spmv_csr`` returns ``alpha * A @ x + beta * y``
@@ -25,7 +27,8 @@ row by row in fp64 and the bound ``1e-4 * |alpha| * sum |a_ip x_p| +
 Every function is pinned by ``tests/test_oracle.py`` against facts that do not
 come from this code: identity and permutation matrices, alpha/beta semantics,
 exact Python-integer and rational arithmetic on small cases, the MAC count
-M*N*K, and IEEE round-to-nearest-even for bf16.
+M*N*K, IEEE round-to-nearest-even for bf16 and fp16, and (for the sampled
+entry points) Python integers and the full matrix at the sampled elements.
 """
 from __future__ import annotations
 
@@ -97,6 +100,18 @@ def _ptr(a):
     return None if a is None else a.ctypes.data
 
 
+def _sampled_ldc(c, ldc, beta):
+    """The sampled entry points cannot infer C's leading dimension (they see
+    no N), so it must be passed whenever C is read."""
+    if c is None:
+        if beta != 0:
+            raise ValueError("beta != 0 needs C")
+        return 0
+    if ldc is None or ldc < 1:
+        raise ValueError("C given without its leading dimension ldc")
+    return ldc
+
+
 class Oracle:
     """ctypes view of one compiled copy of ``gemm_oracle.c``."""
 
@@ -128,6 +143,8 @@ class Oracle:
         lib.oracle_spmv_csr.argtypes = [i64, i64, vp, vp, vp, f64, vp, f64, vp, vp, vp]
         lib.oracle_round_bf16_array.argtypes = [vp, vp, i64]
         lib.oracle_ulp_bf16_array.argtypes = [vp, vp, i64]
+        lib.oracle_round_f16_array.argtypes = [vp, vp, i64]
+        lib.oracle_ulp_f16_array.argtypes = [vp, vp, i64]
         self.lib = lib
         self.path = path
 
@@ -193,17 +210,20 @@ class Oracle:
 
     def gemm_fp_sampled(self, in_dtype, out_dtype, layout_b, K, alpha, A, lda, B, ldb, beta,
                         C, ldc, rows, cols):
-        """ref, bound at the elements (rows[s], cols[s]) only."""
+        """ref, bound at the elements (rows[s], cols[s]) only.
+
+        C is indexed with ldc, which must be given whenever C is."""
         a = _buf(A, _FP_NP[in_dtype], "A")
         b = _buf(B, _FP_NP[in_dtype], "B")
         c = None if C is None else _buf(C, _FP_NP[out_dtype], "C")
+        ldc = _sampled_ldc(c, ldc, beta)
         rows = np.ascontiguousarray(rows, np.int64)
         cols = np.ascontiguousarray(cols, np.int64)
         ref = np.empty(rows.shape, np.float64)
         bound = np.empty(rows.shape, np.float64)
         rc = self.lib.oracle_gemm_fp_sampled(in_dtype, out_dtype, layout_b, K, float(alpha),
                                              _ptr(a), lda, _ptr(b), ldb, float(beta), _ptr(c),
-                                             ldc or 1, rows.size, _ptr(rows), _ptr(cols),
+                                             ldc, rows.size, _ptr(rows), _ptr(cols),
                                              _ptr(ref), _ptr(bound))
         if rc != 0:
             raise ValueError("oracle_gemm_fp_sampled: unsupported dtype pair")
@@ -222,14 +242,16 @@ class Oracle:
         return out
 
     def gemm_i8_sampled(self, layout_b, K, alpha, A, lda, B, ldb, beta, C, ldc, rows, cols):
+        """gemm_i8 at the elements (rows[s], cols[s]) only (ldc as for gemm_fp_sampled)."""
         a = _buf(A, np.int8, "A")
         b = _buf(B, np.int8, "B")
         c = None if C is None else _buf(C, np.int32, "C")
+        ldc = _sampled_ldc(c, ldc, beta)
         rows = np.ascontiguousarray(rows, np.int64)
         cols = np.ascontiguousarray(cols, np.int64)
         out = np.empty(rows.shape, np.int32)
         self.lib.oracle_gemm_i8_sampled(layout_b, K, int(alpha), _ptr(a), lda, _ptr(b), ldb,
-                                        int(beta), _ptr(c), ldc or 1, rows.size, _ptr(rows),
+                                        int(beta), _ptr(c), ldc, rows.size, _ptr(rows),
                                         _ptr(cols), _ptr(out))
         return out
 
@@ -266,6 +288,19 @@ class Oracle:
         flat = np.ascontiguousarray(np.asarray(x, np.float64).ravel())
         out = np.empty(flat.size, np.float64)
         self.lib.oracle_ulp_bf16_array(_ptr(flat), _ptr(out), flat.size)
+        return out.reshape(np.shape(x))
+
+    def round_f16(self, x) -> np.ndarray:
+        """Nearest-even IEEE binary16 encodings (uint16) of the fp64 values x."""
+        flat = np.ascontiguousarray(np.asarray(x, np.float64).ravel())
+        out = np.empty(flat.size, np.uint16)
+        self.lib.oracle_round_f16_array(_ptr(flat), _ptr(out), flat.size)
+        return out.reshape(np.shape(x))
+
+    def ulp_f16(self, x) -> np.ndarray:
+        flat = np.ascontiguousarray(np.asarray(x, np.float64).ravel())
+        out = np.empty(flat.size, np.float64)
+        self.lib.oracle_ulp_f16_array(_ptr(flat), _ptr(out), flat.size)
         return out.reshape(np.shape(x))
 
     def decode_bf16(self, bits) -> np.ndarray:
@@ -336,6 +371,14 @@ def round_bf16(x):
 
 def ulp_bf16(x):
     return default().ulp_bf16(x)
+
+
+def round_f16(x):
+    return default().round_f16(x)
+
+
+def ulp_f16(x):
+    return default().ulp_f16(x)
 
 
 SOURCE = _SRC

@@ -39,8 +39,9 @@
  *
  * Error bound returned beside ref (fp64):
  *   bound(i,j) = rel * sum_k |alpha*a(i,k)*b(k,j)| + (|beta*c(i,j)| + |bias(j)|) * 2^-22
- * with rel = 1e-4.  The bf16-output ulp term is a separate function
- * (oracle_ulp_bf16).
+ * with rel = 1e-4.  The output-rounding ulp terms are separate functions
+ * (oracle_ulp_bf16 for bf16 output, oracle_ulp_f16 for fp16 output), and so
+ * are the roundings themselves (oracle_round_bf16, oracle_round_f16).
  *
  * TF32 inputs (in_dtype OR_TF32): the operands are stored as fp32 and ref is
  * the same exact definition as for OR_F32.  "Matrix multiplication:
@@ -58,7 +59,9 @@
  * Parity pins: every function here is pinned by tests/test_oracle.py
  * (identity, permutation, alpha/beta semantics, exact small integers against
  * Python integers, tiny shapes against exact rationals, MAC count = M*N*K,
- * bf16 rounding against IEEE round-to-nearest-even).
+ * bf16 and fp16 rounding against IEEE round-to-nearest-even, the sampled
+ * entry points against Python integers and against the full matrix at the
+ * same elements, with padded leading dimensions).
  */
 #include <math.h>
 #include <stdint.h>
@@ -345,6 +348,41 @@ double oracle_ulp_bf16(double x) {
     return exp2 < -126 ? ldexp(1.0, -133) : ldexp(1.0, exp2 - 7);
 }
 
+/* Nearest IEEE binary16 to x, ties to even: 11 significant bits, exponent
+ * range [-14, 15], subnormal quantum 2^-24, largest finite value
+ * (2 - 2^-10) * 2^15 = 65504; anything that rounds above it is infinite.
+ * Returns the 16-bit encoding (sign, 5 exponent bits with bias 15, 10
+ * fraction bits). */
+uint16_t oracle_round_f16(double x) {
+    if (isnan(x)) return 0x7e00;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double ax = fabs(x);
+    if (ax == 0.0) return sign;
+    if (isinf(ax)) return sign | 0x7c00;
+    int e;
+    frexp(ax, &e);                            /* ax in [2^(e-1), 2^e) */
+    int exp2 = e - 1;                         /* floor(log2|x|) */
+    int q = exp2 < -14 ? -24 : exp2 - 10;     /* quantum: 2^(exp - 10) */
+    double r = ldexp(nearbyint(ldexp(ax, -q)), q);  /* ties-to-even (default mode) */
+    if (r > 65504.0) return sign | 0x7c00;
+    if (r < ldexp(1.0, -14))                  /* subnormal (or zero): fraction = r / 2^-24 */
+        return sign | (uint16_t)ldexp(r, 24);
+    frexp(r, &e);                             /* rounding may have moved r up a binade */
+    exp2 = e - 1;
+    uint16_t frac = (uint16_t)(ldexp(r, 10 - exp2) - 1024.0);
+    return sign | (uint16_t)((exp2 + 15) << 10) | frac;
+}
+
+/* One unit in the last place of the binary16 value nearest x:
+ * 2^(floor(log2|x|) - 10) in the normal range (|x| >= 2^-14), 2^-24 below it. */
+double oracle_ulp_f16(double x) {
+    if (x == 0.0 || !isfinite(x)) return ldexp(1.0, -24);
+    int e;
+    frexp(fabs(x), &e);
+    int exp2 = e - 1;
+    return exp2 < -14 ? ldexp(1.0, -24) : ldexp(1.0, exp2 - 10);
+}
+
 /* Exact decode, exposed so the tests can pin it. */
 double oracle_decode_bf16(uint16_t h) { return decode_bf16(h); }
 double oracle_decode_f16(uint16_t h) { return decode_f16(h); }
@@ -373,4 +411,14 @@ void oracle_round_bf16_array(const double* x, uint16_t* out, int64_t n) {
 void oracle_ulp_bf16_array(const double* x, double* out, int64_t n) {
 #pragma omp parallel for schedule(static)
     for (int64_t s = 0; s < n; ++s) out[s] = oracle_ulp_bf16(x[s]);
+}
+
+void oracle_round_f16_array(const double* x, uint16_t* out, int64_t n) {
+#pragma omp parallel for schedule(static)
+    for (int64_t s = 0; s < n; ++s) out[s] = oracle_round_f16(x[s]);
+}
+
+void oracle_ulp_f16_array(const double* x, double* out, int64_t n) {
+#pragma omp parallel for schedule(static)
+    for (int64_t s = 0; s < n; ++s) out[s] = oracle_ulp_f16(x[s]);
 }

@@ -12,7 +12,10 @@ disagrees with what the mathematics or the pages fix:
   summation error bound, and the error-bound formula itself;
 * INT8 against Python integers, including wrap-around mod 2**32;
 * the MAC count M*N*K (2MNK FLOPs) of the instrumented build;
-* bf16 decoding and IEEE round-to-nearest-even encoding;
+* bf16 decoding and IEEE round-to-nearest-even encoding, for bf16 and
+  fp16, and the one-ulp output-rounding terms of both;
+* the sampled entry points against Python integers and against the full
+  matrix at the sampled elements, with padded leading dimensions;
 * CSR SpMV: the page's worked 3 x 4 example, dense products of COO
   triplets in Python integers and exact rationals (empty rows, a long row,
   repeated columns), identity and permutation matrices, alpha/beta
@@ -350,6 +353,132 @@ def pin_ulp_bf16(o):
     assert np.array_equal(got, np.array(list(cases.values())))
 
 
+def pin_f16_round(o):
+    # hand cases from round-to-nearest-even on 11 significant bits
+    cases = [
+        (1.0, 0x3C00),
+        (1.0 + 2.0**-11, 0x3C00),            # tie -> even mantissa (0)
+        (1.0 + 3 * 2.0**-11, 0x3C02),        # tie -> even mantissa (2)
+        (1.0 + 2.0**-11 + 2.0**-30, 0x3C01),  # just above the tie
+        (-1.5, 0xBE00),
+        (2049.0, 0x6800),                    # quantum 2 at 2^11: tie -> 2048
+        (2051.0, 0x6802),                    # tie -> 2052
+        (2.0**-14, 0x0400),                  # smallest normal
+        (2.0**-14 - 2.0**-25, 0x0400),       # tie between 1023 and 1024 quanta -> normal
+        (2.0**-24, 0x0001),                  # smallest subnormal
+        (2.0**-25, 0x0000),                  # tie between 0 and 2^-24 -> 0
+        (3 * 2.0**-25, 0x0002),              # tie between 1 and 2 quanta -> 2
+        (65504.0, 0x7BFF),                   # largest finite
+        (65519.0, 0x7BFF),
+        (65520.0, 0x7C00),                   # tie with 2^16 -> overflow to inf
+        (1e5, 0x7C00),                       # far above the largest finite
+        (-70000.0, 0xFC00),
+        (-1e9, 0xFC00),
+        (0.0, 0x0000),
+        (-0.0, 0x8000),
+    ]
+    got = o.round_f16(np.array([x for x, _ in cases], np.float64))
+    for (x, want), g in zip(cases, got.tolist()):
+        assert g == want, (x, hex(g), hex(want))
+    # agreement with torch's float32 -> float16 round-to-nearest-even
+    g = _rng(18)
+    x = torch.randn(20000, generator=g) * torch.exp2(torch.randint(-30, 18, (20000,),
+                                                                  generator=g).float())
+    want = x.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    got = o.round_f16(x.double().numpy())
+    assert np.array_equal(got, want)
+
+
+def pin_ulp_f16(o):
+    cases = {1.0: 2.0**-10, 1.5: 2.0**-10, -3.0: 2.0**-9, 1024.0: 1.0, 65504.0: 32.0,
+             2.0**-14: 2.0**-24, 3 * 2.0**-20: 2.0**-24, 0.0: 2.0**-24}
+    got = o.ulp_f16(np.array(list(cases.keys())))
+    assert np.array_equal(got, np.array(list(cases.values())))
+
+
+# ------------------------------------------------------ sampled entries --
+
+def _padded(g, rows, cols, ld, make):
+    """A rows x ld buffer whose first cols columns hold make((rows, cols)) and
+    whose padding holds other values of the same kind, so that an element read
+    with the wrong leading dimension or index differs."""
+    full = make((rows, ld))
+    full[:, :cols] = make((rows, cols))
+    return full
+
+
+def pin_sampled(o):
+    """The sampled entry points (the checkers of full-size parity tests)
+    compute the same elements as the full oracle and as Python integers, with
+    padded leading dimensions for A, B and C: a swapped row/column index or a
+    wrong leading dimension fails."""
+    g = _rng(19)
+    rnd = np.random.default_rng(19)
+    M, N, K = 37, 53, 29
+    n_s = 240
+    rows = np.concatenate([[0, M - 1, 0, M - 1], rnd.integers(0, M, n_s)]).astype(np.int64)
+    cols = np.concatenate([[0, N - 1, N - 1, 0], rnd.integers(0, N, n_s)]).astype(np.int64)
+
+    def small_ints(shape):
+        return torch.randint(-4, 5, shape, generator=g).numpy()
+
+    for layout in (ROW, COL):
+        Bshape = (N, K) if layout == COL else (K, N)
+        lda, ldb, ldc = K + 3, Bshape[1] + 5, N + 7
+        A = _padded(g, M, K, lda, small_ints)
+        B = _padded(g, Bshape[0], Bshape[1], ldb, small_ints)
+        C = _padded(g, M, N, ldc, small_ints)
+        Ap, Bp, Cp = A[:, :K].tolist(), B[:, :Bshape[1]].tolist(), C[:, :N].tolist()
+        want = np.array(_py_gemm(Ap, Bp, Cp, 3, -2, layout), np.float64)[rows, cols]
+        for in_dtype, out_dtype in ((F32, F32), (BF16, BF16), (F16, F32), (BF16, F32)):
+            def enc(x, dt):
+                t = torch.from_numpy(x.astype(np.float32))
+                if dt == BF16:
+                    return _bf16_bits(t)
+                if dt == F16:
+                    return t.to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+                return t.numpy()
+            a, b, c = enc(A, in_dtype), enc(B, in_dtype), enc(C, out_dtype)
+            ref_s, bound_s = o.gemm_fp_sampled(in_dtype, out_dtype, layout, K, 3.0, a, lda, b,
+                                               ldb, -2.0, c, ldc, rows, cols)
+            ref_f, bound_f = o.gemm_fp(in_dtype, out_dtype, layout, M, N, K, 3.0, a, lda, b, ldb,
+                                       -2.0, c, ldc)
+            what = (in_dtype, out_dtype, layout)
+            assert np.array_equal(ref_s, ref_f[rows, cols]), ("ref vs full", what)
+            assert np.array_equal(bound_s, bound_f[rows, cols]), ("bound vs full", what)
+            assert np.array_equal(ref_s, want), ("ref vs Python integers", what)
+        # INT8: full range, wrap mod 2^32 with large alpha and beta
+        def i8(shape):
+            return torch.randint(-128, 128, shape, generator=g, dtype=torch.int8).numpy()
+
+        def i32(shape):
+            return torch.randint(-2**31, 2**31, shape, generator=g,
+                                 dtype=torch.int64).to(torch.int32).numpy()
+        A8 = _padded(g, M, K, lda, i8)
+        B8 = _padded(g, Bshape[0], Bshape[1], ldb, i8)
+        C32 = _padded(g, M, N, ldc, i32)
+        for alpha, beta in ((1, 0), (-7, 3), (1 << 20, 1 << 30)):
+            got_s = o.gemm_i8_sampled(layout, K, alpha, A8, lda, B8, ldb, beta, C32, ldc,
+                                      rows, cols)
+            got_f = o.gemm_i8(layout, M, N, K, alpha, A8, lda, B8, ldb, beta, C32, ldc)
+            py = _py_gemm(A8[:, :K].tolist(), B8[:, :Bshape[1]].tolist(), C32[:, :N].tolist(),
+                          alpha, beta, layout)
+            wrapped = np.array([[((v + 2**31) % 2**32) - 2**31 for v in r] for r in py], np.int64)
+            assert np.array_equal(got_s, got_f[rows, cols]), ("i8 vs full", layout, alpha)
+            assert np.array_equal(got_s, wrapped[rows, cols]), ("i8 vs Python", layout, alpha)
+    # C without its leading dimension is refused, not indexed with a guess
+    for call in (lambda: o.gemm_fp_sampled(F32, F32, ROW, 2, 1.0, np.ones(4, np.float32), 2,
+                                           np.ones(4, np.float32), 2, 1.0,
+                                           np.ones(4, np.float32), None, [1], [1]),
+                 lambda: o.gemm_i8_sampled(ROW, 2, 1, np.ones(4, np.int8), 2, np.ones(4, np.int8),
+                                           2, 1, np.ones(4, np.int32), None, [1], [1])):
+        try:
+            call()
+        except ValueError:
+            continue
+        raise AssertionError("sampled call without ldc accepted")
+
+
 # ---------------------------------------------- A layout, bias, row sums --
 
 def pin_transposed_a(o):
@@ -620,4 +749,5 @@ def pin_spmv(o):
 
 ALL_PINS = [pin_identity, pin_permutation, pin_alpha_beta, pin_small_integers, pin_int8,
             pin_tiny_rational, pin_bf16_decode, pin_f16_decode, pin_bf16_round, pin_ulp_bf16,
-            pin_transposed_a, pin_bias, pin_sum_rows, pin_tf32, pin_spmv]
+            pin_f16_round, pin_ulp_f16, pin_sampled, pin_transposed_a, pin_bias, pin_sum_rows,
+            pin_tf32, pin_spmv]

@@ -46,6 +46,18 @@ MUTANTS = [
     ("spmv_alpha_on_y", "ref[i] = alpha * sum + yterm;", "ref[i] = alpha * (sum + yterm);", 0),
     ("spmv_beta_zero_reads_y", "double yterm = beta != 0.0 ?", "double yterm = 1 ?", 0),
     ("spmv_no_column_check", "column_indices[p] >= cols) return -1;", "column_indices[p] > cols) return -1;", 0),
+    ("sampled_fp_rows_cols_swapped", "rows[s], cols[s], &ref[s]", "cols[s], rows[s], &ref[s]", 0),
+    ("sampled_i8_rows_cols_swapped", "NULL, rows[s], cols[s]);", "NULL, cols[s], rows[s]);", 0),
+    ("sampled_fp_ldc_one", "beta, C, ldc, NULL, rows[s]", "beta, C, 1, NULL, rows[s]", 0),
+    ("sampled_i8_ldc_one", "beta, C, ldc,\n                            NULL, rows[s]",
+     "beta, C, 1,\n                            NULL, rows[s]", 0),
+    ("sampled_fp_lda_ignored", "OR_ROW_MAJOR, layout_b, K, alpha, A, lda, B, ldb,\n                   beta",
+     "OR_ROW_MAJOR, layout_b, K, alpha, A, K, B, ldb,\n                   beta", 0),
+    ("f16_round_ties_away", "ldexp(nearbyint(ldexp(ax, -q)), q)", "ldexp(round(ldexp(ax, -q)), q)", 0),
+    ("f16_subnormal_quantum", "int q = exp2 < -14 ? -24 : exp2 - 10;", "int q = exp2 < -15 ? -25 : exp2 - 10;", 0),
+    ("f16_no_overflow", "if (r > 65504.0) return sign | 0x7c00;", "if (isinf(r)) return sign | 0x7c00;", 0),
+    ("ulp_f16_one_bit_off", "ldexp(1.0, exp2 - 10)", "ldexp(1.0, exp2 - 11)", 0),
+    ("ulp_f16_subnormal", "exp2 < -14 ? ldexp(1.0, -24)", "exp2 < -14 ? ldexp(1.0, -25)", 0),
     ("tf32_term_dropped", "in_dtype == OR_TF32 ? ldexp(1.0, -9) + ldexp(1.0, -20) + 1e-4 : 1e-4",
      "1e-4", 0),
     ("tf32_read_as_16_bit", "    case OR_F32:\n    case OR_TF32: return (double)((const float*)p)[idx];",
