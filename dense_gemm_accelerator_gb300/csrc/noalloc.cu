@@ -16,6 +16,7 @@
 // nothing in it needs to start at zero, because each call rewrites every byte
 // it later reads (the repack writes whole padded rows).  Calls that overlap on
 // the GPU (two streams, or two host threads) race on it.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -29,25 +30,86 @@ static_assert(kScratchBytes == DGA_NOALLOC_SCRATCH_BYTES, "header and library di
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-void* g_scratch[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
+// In host code the array's name is only a host-side handle; kernels need its
+// device address.  That address belongs to the CUDA context the library's
+// module is loaded in (normally a device's primary context), so it is looked
+// up with the device current, once per context, and cached under the
+// context's ID: unlike the context handle, which a context created after
+// cudaDeviceReset may reuse, the ID is never given to a second context in a
+// process.  A reset or another context therefore gets a fresh lookup instead
+// of a stale address.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// The array's name in host code is only a host-side handle; kernels need its
-// device address, which is looked up once per device with that device current.
-cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::call_once(g_once[dev], [dev] {
+struct DriverFns {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+};
+
+const DriverFns& driver_fns() {
+    static DriverFns fns;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void* p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        g_scratch[dev] = p;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fns.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fns.get_id = reinterpret_cast<CtxGetIdFn>(p);
     });
-    *out = g_scratch[dev];
-    return g_scratch_err[dev];
+    return fns;
+}
+
+// The ID of the current context, or false when there is none yet or the
+// driver cannot say.
+bool current_context_id(unsigned long long* id) {
+    const DriverFns& f = driver_fns();
+    if (!f.get_current || !f.get_id) return false;
+    CUcontext ctx = nullptr;
+    if (f.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return f.get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+constexpr int kCacheSlots = 64;
+std::mutex g_cache_mutex;
+unsigned long long g_cache_id[kCacheSlots];
+void* g_cache_addr[kCacheSlots];
+int g_cache_used = 0;
+int g_cache_next = 0;  // once all slots are taken: the oldest entry, replaced next
+
+cudaError_t scratch_address(void** out) {
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    if (have_id) {
+        std::lock_guard<std::mutex> lock(g_cache_mutex);
+        for (int i = 0; i < g_cache_used; ++i)
+            if (g_cache_id[i] == id) {
+                *out = g_cache_addr[i];
+                return cudaSuccess;
+            }
+    }
+    // Not seen yet (or no context made current so far: this call creates the
+    // device's primary context).  Look the address up with the device current.
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    if (current_context_id(&id)) {
+        std::lock_guard<std::mutex> lock(g_cache_mutex);
+        int slot;
+        if (g_cache_used < kCacheSlots) {
+            slot = g_cache_used++;
+        } else {  // every slot taken: the oldest entry makes room
+            slot = g_cache_next;
+            g_cache_next = (g_cache_next + 1) % kCacheSlots;
+        }
+        g_cache_id[slot] = id;
+        g_cache_addr[slot] = p;
+    }
+    *out = p;
+    return cudaSuccess;
 }
 
 // dga_gemm_ex reports a bad argument as -(its position there); this entry

@@ -282,10 +282,17 @@ const char* dga_status_string(int status);
  *     (nothing in it needs to start at zero: each call rewrites all it reads);
  *     calls that overlap on the GPU -- other streams, other host threads --
  *     race on it, so serialise them;
- *   - the first call on a device looks up the area's device address with that
- *     device current; make that first call before any stream capture.
- * Argument errors are -(position in this function's argument list); other
- * codes as for dga_gemm_ex.
+ *   - the first call in a CUDA context (normally: the first call on each
+ *     device, in its primary context) looks up the area's device address with
+ *     that device current; make that first call before any stream capture.
+ *     The address is kept per context, so after cudaDeviceReset, or in another
+ *     context on the same device, the next call looks it up again.
+ * Argument errors are -(position in this function's argument list).  The
+ * product always runs on the tensor-core path: where that path is
+ * unavailable on the device (no tensor-map encoder in the driver, or not an
+ * sm_103 GPU) the call returns DGA_ERR_PATH (or DGA_ERR_DEVICE) rather than
+ * falling back to another kernel as dga_gemm does.  Other codes as for
+ * dga_gemm_ex.
  */
 #define DGA_NOALLOC_SCRATCH_BYTES (72ull << 20)
 int dga_gemm_i8_noalloc(dga_layout layout_b, int64_t M, int64_t N, int64_t K,

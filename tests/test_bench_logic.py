@@ -132,3 +132,44 @@ def test_spec_peak_fields():
     hbm = {"bound": "hbm", "achieved": 6000.0}
     bench.add_spec_peak(hbm, peaks, 2070.0)
     assert "spec" not in hbm
+
+
+def test_per_dtype_rows_fit_a_short_tail():
+    # The driver keeps only the end of the bench's output line, so the extra
+    # keys come last and a full set of per_dtype rows -- each with the fields
+    # its kind of workload carries, a throttle reason on every tensor row --
+    # must stay well within a few thousand characters.
+    peaks = bench.load_peaks(152)
+    peaks["fp32_ffma_probe"] = {"ffma_tflops": 79.91234, "ffma2_tflops": 79.81234}
+    per = {}
+    names = [n for n in bench.PER_DTYPE] + [n + "_sustained" for n in bench.SUSTAINED]
+    for i, name in enumerate(names):
+        hbm = name.startswith(("skinny", "spmv"))
+        bound = "hbm" if hbm else ("alu" if name == "fc_f32_4096" else "tensor")
+        rf = {"bound": bound, "achieved": 1772.123456789 + i,
+              "unit": "GB/s" if hbm else "TFLOP/s", "frac": 0.93412345678,
+              "peak_kind": "bf16 tensor", "ms_mean": 0.620512345,
+              "traffic": None if name.startswith("fc") else 1340498400.0,
+              "launches_per_call": 4.0 if name.startswith("fc") else 1.0,
+              "clocks": {"sm_mhz": 1965.0, "sm_max_mhz": 2070.0, "samples": 2,
+                         "reasons": ["sw_power_cap"] if bound == "tensor" else []}}
+        if name.startswith("spmv"):
+            rf["nnz"] = 92038930.0
+        if name.endswith("_sustained"):
+            rf["calls"], rf["seconds"] = 6450.0, 4.00123
+        bench.add_spec_peak(rf, peaks, 1965.0)
+        per[name] = bench.compact_row(rf)
+    tail = json.dumps({"peaks": bench.compact_peaks(peaks), "per_dtype": per})
+    assert len(tail) < 2600, len(tail)
+    assert set(per) >= {"bf16_8192", "skinny_m1", "skinny_m8", "skinny_m16", "int8_ragged"}
+    row = per["bf16_8192"]
+    assert row["frac"] == 0.934 and row["achieved"] == 1772.0 and row["traffic_mb"] == 1340.0
+    assert row["spec_frac_obs"] == round(1772.123456789 / (152 * 8192 * 1965e-6), 3)
+
+
+def test_sig_rounds_to_significant_digits():
+    assert bench.sig(1772.123456, 4) == 1772.0
+    assert bench.sig(0.000123456, 3) == 0.000123
+    assert bench.sig(58.34934825, 6) == 58.3493
+    assert bench.sig(1340498400.0, 3) == 1340000000.0
+    assert bench.sig(0.0) == 0.0 and bench.sig(7) == 7 and bench.sig(None) is None
