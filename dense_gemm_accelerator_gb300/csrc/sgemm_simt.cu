@@ -70,6 +70,11 @@ struct Params {
     int parts;
     float* partials;
     const float* bias;  // N values added to every row, or null
+    // Wide kernel, stream-K schedule (sk_ctas > 0): the (tile, 16-deep
+    // K-slice) units, sk_slices per tile, are cut into sk_ctas equal
+    // contiguous ranges, one per block; see sgemm_wide_kernel.
+    int64_t sk_units, sk_slices;
+    int sk_ctas;
 };
 
 struct Smem {
@@ -398,14 +403,21 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sgemm_128x128_interior_k
 
 // Sums the K-range partials of each tail tile in part order (so the result
 // does not depend on which block finished first) and applies the epilogue.
+// kTailSlabs blocks share a tile, 8 rows each (one float4 per thread), so
+// that enough loads are in flight to keep this short step bandwidth-bound.
+constexpr int kTailSlabs = BM / 8;
+
 __global__ void __launch_bounds__(kThreads) sgemm_tail_reduce(Params p) {
-    const int64_t tile = p.full_tiles + blockIdx.x;
+    const int64_t slot = blockIdx.x / kTailSlabs;
+    const int slab = static_cast<int>(blockIdx.x % kTailSlabs);
+    const int64_t tile = p.full_tiles + slot;
     int64_t tm, tn;
     grouped_tile(tile, (p.M + BM - 1) / BM, p.tiles_n, tm, tn);
     const int64_t row0 = tm * BM;
     const int64_t col0 = tn * BN;
-    const float* base = p.partials + static_cast<int64_t>(blockIdx.x) * p.parts * (BM * BN);
-    for (int e = threadIdx.x; e < BM * BN / 4; e += kThreads) {
+    const float* base = p.partials + slot * p.parts * (BM * BN);
+    {
+        const int e = slab * (8 * BN / 4) + threadIdx.x;
         const int r = e / (BN / 4), c = (e % (BN / 4)) * 4;
         float4 sum = *reinterpret_cast<const float4*>(base + r * BN + c);
         for (int q = 1; q < p.parts; ++q) {
@@ -416,7 +428,7 @@ __global__ void __launch_bounds__(kThreads) sgemm_tail_reduce(Params p) {
             sum.w += v.w;
         }
         const int64_t row = row0 + r, col = col0 + c;
-        if (row >= p.M) continue;
+        if (row >= p.M) return;
         float* crow = p.C + row * p.ldc;
         const float v[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
@@ -463,6 +475,352 @@ Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int sm_count) {
     sc.part_k = part_k;
     sc.partial_bytes = static_cast<size_t>(tail) * parts * BM * BN * sizeof(float);
     return sc;
+}
+
+// ---- the wide kernel: 128 x 256 block tiles, 8 x 16 per thread --------------
+//
+// For problems made of whole 128 x 256 tiles with at least one full wave of
+// them, one block per SM holding twice the accumulators of the 128 x 128
+// kernel does more FMAs per shared-memory read and per broadcast (per k, 8 A
+// and 16 B values feed 128 FMAs: 64 packed fma.rn.f32x2 behind 8 pair
+// broadcasts and 6 128-bit shared loads), and its 16-deep K slices halve the
+// barriers per FMA.  It uses up to 255 registers, so one block of 8 warps per
+// SM.  Measured on GB300 at whole waves (M = 4864, N = K = 4096): 64.6
+// TFLOP/s against 60.6 for two 128 x 128 blocks per SM.  With one block per
+// SM a part-filled last wave would leave SMs idle for a whole tile time, so
+// problems that are not a whole number of waves run a stream-K schedule (see
+// sgemm_wide_kernel): every block does the same share of the (tile, K-slice)
+// work, and the tiles split between blocks are summed in a fixed order by
+// sgemm_wide_sk_reduce.  Thread layout: 8 warps as 2 (M) x 4 (N)
+// warp tiles of 64 x 64; lane = lm * 4 + ln; a thread owns rows {wm*64 +
+// lm*4 + i, wm*64 + 32 + lm*4 + i} and columns {wn*64 + h*16 + ln*4 + j},
+// i, j in 0..3, h in 0..3.  The results equal the 128 x 128 kernel's bit for
+// bit (the same FMAs per element in the same k order).
+
+constexpr int kWBM = 128, kWBN = 256, kWBK = 16;
+constexpr int kWAStride = kWBM + 4;  // floats per k-row of the A tile
+constexpr int kWBStride = kWBN + 4;  // and of the B tile (the padding keeps the
+                                     // transposing stores of a column-major B
+                                     // free of bank conflicts)
+
+struct WideSmem {
+    float A[2][kWBK][kWAStride];
+    float B[2][kWBK][kWBStride];
+};
+
+__device__ __forceinline__ void wide_tile(int64_t t, int64_t tiles_m, int64_t tiles_n,
+                                          int64_t& tm, int64_t& tn) {
+    grouped_tile(t, tiles_m, tiles_n, tm, tn);
+}
+
+// One 128 x 256 tile over K in [k_begin, k_end) (a whole number of slices,
+// every element inside the matrices).  partial non-null: the raw
+// accumulators go there (128 x 256 floats, row-major) instead of the
+// epilogue.
+template <bool kTransA, bool kTransB, int kReadC, int kBias>
+__device__ __forceinline__ void wide_block_tile(const Params& p, WideSmem& sm, int64_t row0,
+                                                int64_t col0, int64_t k_begin, int64_t k_end,
+                                                float* partial) {
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    // Staging roles per 16-deep slice (2 float4 of A and 4 of B per thread):
+    //  row-major A: row 16*warp + lane/2, k 4*(lane%2) + 8v (v = 0, 1): a lane
+    //    pair reads a whole 32-byte sector; transposing stores, conflict-free;
+    //  column-major A (stored K x M): k = warp + 8v, rows 4*lane .. 4*lane+3;
+    //  row-major B: k = warp + 8v, columns 4*lane + 128u (u = 0, 1);
+    //  column-major B (stored N x K): column 16*warp + lane/2 + 128u, k
+    //    4*(lane%2) + 8v, staged like row-major A.
+    const float* a_run;
+    const float* b_run;
+    if constexpr (kTransA) a_run = p.A + (k_begin + warp) * p.lda + row0 + lane * 4;
+    else a_run = p.A + (row0 + warp * 16 + (lane >> 1)) * p.lda + k_begin + (lane & 1) * 4;
+    if constexpr (kTransB) b_run = p.B + (col0 + warp * 16 + (lane >> 1)) * p.ldb + k_begin + (lane & 1) * 4;
+    else b_run = p.B + (k_begin + warp) * p.ldb + col0 + lane * 4;
+    const int64_t a_step = kTransA ? kWBK * p.lda : kWBK;
+    const int64_t b_step = kTransB ? kWBK : kWBK * p.ldb;
+    float4 ra[2], rb[4];
+    auto fetch = [&]() {
+#pragma unroll
+        for (int v = 0; v < 2; ++v) ra[v] = ld_f4(a_run + (kTransA ? 8 * v * p.lda : 8 * v));
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int v = 0; v < 2; ++v)
+                rb[u * 2 + v] = kTransB ? ld_f4(b_run + 128 * u * p.ldb + 8 * v)
+                                        : ld_f4(b_run + 8 * v * p.ldb + 128 * u);
+        a_run += a_step;
+        b_run += b_step;
+    };
+    auto stash = [&](int buf) {
+#pragma unroll
+        for (int v = 0; v < 2; ++v) {
+            if constexpr (kTransA) {
+                *reinterpret_cast<float4*>(&sm.A[buf][warp + 8 * v][lane * 4]) = ra[v];
+            } else {
+                const int k = (lane & 1) * 4 + 8 * v, r = warp * 16 + (lane >> 1);
+                sm.A[buf][k + 0][r] = ra[v].x;
+                sm.A[buf][k + 1][r] = ra[v].y;
+                sm.A[buf][k + 2][r] = ra[v].z;
+                sm.A[buf][k + 3][r] = ra[v].w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int v = 0; v < 2; ++v) {
+                const float4 x = rb[u * 2 + v];
+                if constexpr (kTransB) {
+                    const int k = (lane & 1) * 4 + 8 * v, c = warp * 16 + (lane >> 1) + 128 * u;
+                    sm.B[buf][k + 0][c] = x.x;
+                    sm.B[buf][k + 1][c] = x.y;
+                    sm.B[buf][k + 2][c] = x.z;
+                    sm.B[buf][k + 3][c] = x.w;
+                } else {
+                    *reinterpret_cast<float4*>(&sm.B[buf][warp + 8 * v][lane * 4 + 128 * u]) = x;
+                }
+            }
+    };
+
+    const int wm = warp >> 2, wn = warp & 3;
+    const int lm = lane >> 2, ln = lane & 3;
+    const int am0 = wm * 64 + lm * 4, am1 = am0 + 32;
+    const int bn0 = wn * 64 + ln * 4;  // + 16h, h = 0..3
+
+    // acc2[i][q]: row i, columns 2q and 2q+1 of the thread's 16 (q = 2h, 2h+1)
+    uint64_t acc2[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc2[i][q] = 0ull;
+
+    const int64_t n_slices = (k_end - k_begin) / kWBK;
+    fetch();
+    stash(0);
+    __syncthreads();
+    for (int64_t s = 0; s < n_slices; ++s) {
+        const int buf = static_cast<int>(s & 1);
+        const bool more = s + 1 < n_slices;
+        float a[2][8];
+        uint64_t b[2][8];
+        auto frag = [&](int d, int k) {
+            *reinterpret_cast<float4*>(&a[d][0]) = *reinterpret_cast<const float4*>(&sm.A[buf][k][am0]);
+            *reinterpret_cast<float4*>(&a[d][4]) = *reinterpret_cast<const float4*>(&sm.A[buf][k][am1]);
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                *reinterpret_cast<ulonglong2*>(&b[d][2 * h]) =
+                    *reinterpret_cast<const ulonglong2*>(&sm.B[buf][k][bn0 + h * 16]);
+        };
+        frag(0, 0);
+#pragma unroll
+        for (int k = 0; k < kWBK; ++k) {
+            if (k == 2 && more) fetch();
+            if (k + 1 < kWBK) frag((k + 1) & 1, k + 1);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint64_t ai = pair_of(a[k & 1][i]);  // (a_i, a_i)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) fma2(acc2[i][q], ai, b[k & 1][q]);
+            }
+        }
+        // the other buffer was last read in slice s-1, before the barrier that ended it
+        if (more) stash(buf ^ 1);
+        __syncthreads();
+    }
+
+    if (partial != nullptr) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float* prow = partial + (i < 4 ? am0 + i : am1 + (i - 4)) * kWBN;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float v[4];
+                unpair(acc2[i][2 * h], v[0], v[1]);
+                unpair(acc2[i][2 * h + 1], v[2], v[3]);
+                *reinterpret_cast<float4*>(prow + bn0 + h * 16) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+        }
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int64_t r = row0 + (i < 4 ? am0 + i : am1 + (i - 4));
+        float* crow = p.C + r * p.ldc + col0;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float v[4];
+            unpair(acc2[i][2 * h], v[0], v[1]);
+            unpair(acc2[i][2 * h + 1], v[2], v[3]);
+            const int c = bn0 + h * 16;
+            float4* dst = reinterpret_cast<float4*>(crow + c);
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (kReadC) o = *dst;
+            o.x = axpby(p.alpha, v[0], p.beta, o.x);
+            o.y = axpby(p.alpha, v[1], p.beta, o.y);
+            o.z = axpby(p.alpha, v[2], p.beta, o.z);
+            o.w = axpby(p.alpha, v[3], p.beta, o.w);
+            if (kBias) {
+                const float4 bb = ld_f4(p.bias + col0 + c);
+                o.x += bb.x;
+                o.y += bb.y;
+                o.z += bb.z;
+                o.w += bb.w;
+            }
+            *dst = o;
+        }
+    }
+}
+
+// Grid over the wide schedule.  Whole waves (sk_ctas == 0): block b owns tile
+// b.  Stream-K (sk_ctas > 0, one block per SM): the units (tile t, K-slice s)
+// in the order t * sk_slices + s are cut into sk_ctas equal contiguous
+// ranges, u0(c) = c * units / sk_ctas, so that every SM does the same work
+// whatever the tile count.  A block walks its range tile by tile: a tile it
+// covers whole gets the epilogue; its first and last segments, when they
+// cover only part of a tile, go to the workspace as raw partial sums (slots
+// 2c and 2c + 1, 128 x 256 floats each), and sgemm_wide_sk_reduce adds the
+// pieces of each such tile in block order, i.e. in K order.  No block ever
+// waits for another.
+template <bool kTransA, bool kTransB, int kReadC, int kBias>
+__global__ void __launch_bounds__(kThreads, 1) sgemm_wide_kernel(Params p) {
+    extern __shared__ __align__(16) unsigned char wide_smem_raw[];
+    WideSmem& sm = *reinterpret_cast<WideSmem*>(wide_smem_raw);
+    const int64_t tiles_m = p.M / kWBM;
+    if (p.sk_ctas == 0) {
+        int64_t tm, tn;
+        wide_tile(blockIdx.x, tiles_m, p.tiles_n, tm, tn);
+        wide_block_tile<kTransA, kTransB, kReadC, kBias>(p, sm, tm * kWBM, tn * kWBN, 0, p.K,
+                                                         nullptr);
+        return;
+    }
+    const int64_t c = blockIdx.x, S = p.sk_slices;
+    const int64_t u0 = c * p.sk_units / p.sk_ctas, u1 = (c + 1) * p.sk_units / p.sk_ctas;
+    for (int64_t u = u0; u < u1;) {
+        const int64_t t = u / S, s0 = u - t * S;
+        const int64_t end = min(u1, (t + 1) * S);
+        const bool whole = s0 == 0 && end == (t + 1) * S;
+        float* partial =
+            whole ? nullptr : p.partials + (2 * c + (u == u0 ? 0 : 1)) * (kWBM * kWBN);
+        int64_t tm, tn;
+        wide_tile(t, tiles_m, p.tiles_n, tm, tn);
+        wide_block_tile<kTransA, kTransB, kReadC, kBias>(p, sm, tm * kWBM, tn * kWBN,
+                                                         s0 * kWBK, (end - t * S) * kWBK, partial);
+        u = end;
+    }
+}
+
+// The block whose stream-K range holds unit u: the largest c with
+// c * units / ctas <= u.
+__device__ __forceinline__ int64_t sk_owner(const Params& p, int64_t u) {
+    return ((u + 1) * p.sk_ctas - 1) / p.sk_units;
+}
+
+// Adds the stream-K pieces of every tile split between blocks and applies
+// the epilogue (float4 everywhere: the wide path runs only on aligned
+// shapes).  Work item b = 1 .. sk_ctas - 1 is the range boundary between
+// blocks b - 1 and b; the first boundary inside a tile handles that tile.
+// kReduceSlabs blocks share a tile, 8 rows each, two float4 per thread, so
+// that enough loads are in flight to keep this short step bandwidth-bound.
+constexpr int kReduceSlabs = kWBM / 8;
+
+__global__ void __launch_bounds__(kThreads) sgemm_wide_sk_reduce(Params p) {
+    const int64_t b = blockIdx.x / kReduceSlabs + 1;
+    const int slab = static_cast<int>(blockIdx.x % kReduceSlabs);
+    const int64_t S = p.sk_slices;
+    const int64_t ub = b * p.sk_units / p.sk_ctas;
+    const int64_t T = ub / S;
+    if (ub - T * S == 0) return;  // the boundary falls between tiles: nothing split here
+    const int64_t prev = (b - 1) * p.sk_units / p.sk_ctas;
+    if (b > 1 && prev / S == T && prev - T * S != 0) return;  // an earlier boundary owns T
+    const int64_t c_first = sk_owner(p, T * S), c_last = sk_owner(p, (T + 1) * S - 1);
+    int64_t tm, tn;
+    wide_tile(T, p.M / kWBM, p.tiles_n, tm, tn);
+    const int64_t row0 = tm * kWBM, col0 = tn * kWBN;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = slab * (8 * kWBN / 4) + h * kThreads + threadIdx.x;
+        const int r = e / (kWBN / 4), c = (e % (kWBN / 4)) * 4;
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t q = c_first; q <= c_last; ++q) {
+            // block q's piece of T is its first segment if its range starts in T
+            const int64_t slot = 2 * q + ((q * p.sk_units / p.sk_ctas) / S == T ? 0 : 1);
+            const float4 v =
+                *reinterpret_cast<const float4*>(p.partials + slot * (kWBM * kWBN) + r * kWBN + c);
+            if (q == c_first) {
+                sum = v;
+            } else {
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+        }
+        float4* dst = reinterpret_cast<float4*>(p.C + (row0 + r) * p.ldc + col0 + c);
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (p.beta != 0.0f) o = *dst;
+        o.x = axpby(p.alpha, sum.x, p.beta, o.x);
+        o.y = axpby(p.alpha, sum.y, p.beta, o.y);
+        o.z = axpby(p.alpha, sum.z, p.beta, o.z);
+        o.w = axpby(p.alpha, sum.w, p.beta, o.w);
+        if (p.bias != nullptr) {
+            const float4 bb = ld_f4(p.bias + col0 + c);
+            o.x += bb.x;
+            o.y += bb.y;
+            o.z += bb.z;
+            o.w += bb.w;
+        }
+        *dst = o;
+    }
+}
+
+// The wide schedule for a problem of whole 128 x 256 tiles with at least one
+// full wave of them (one block per SM); ok == false: not used.  A whole
+// number of waves runs tile by tile; otherwise stream-K over one block per SM
+// (sk_ctas), with 2 partial tiles per block of workspace (ws_bytes).
+struct WidePlan {
+    bool ok;
+    int64_t tiles, tiles_n, slices;
+    int sk_ctas;  // 0: tile by tile
+    size_t ws_bytes;
+};
+
+WidePlan plan_wide(const GemmArgs& a, int sm_count) {
+    WidePlan w{};
+    const bool shape = a.M % kWBM == 0 && a.N % kWBN == 0 && a.K % kWBK == 0 && a.K > 0 &&
+                       a.lda % 4 == 0 && a.ldb % 4 == 0 && a.ldc % 4 == 0 &&
+                       aligned(a.A, 16) && aligned(a.B, 16) && aligned(a.C, 16) &&
+                       (a.bias == nullptr || aligned(a.bias, 16));
+    if (!shape || sm_count <= 0) return w;
+    w.tiles_n = a.N / kWBN;
+    w.tiles = (a.M / kWBM) * w.tiles_n;
+    w.slices = a.K / kWBK;
+    if (w.tiles < sm_count || w.tiles > 0x7fffffff) return w;
+    // units * ctas must not overflow 64 bits in the range arithmetic
+    if (w.tiles > (INT64_MAX / sm_count) / w.slices) return w;
+    w.ok = true;
+    if (w.tiles % sm_count != 0) {
+        w.sk_ctas = sm_count;
+        w.ws_bytes = static_cast<size_t>(2) * sm_count * kWBM * kWBN * sizeof(float);
+    }
+    return w;
+}
+
+template <bool kTransA, bool kTransB, int kReadC, int kBias>
+cudaError_t launch_wide(const Params& p, int64_t blocks, cudaStream_t s) {
+    auto kern = sgemm_wide_kernel<kTransA, kTransB, kReadC, kBias>;
+    const int smem = static_cast<int>(sizeof(WideSmem));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(blocks), kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+template <bool kTransA, bool kTransB>
+cudaError_t launch_wide_layout(const Params& p, int64_t blocks, bool read_c, bool bias,
+                               cudaStream_t s) {
+    if (read_c && bias) return launch_wide<kTransA, kTransB, 1, 1>(p, blocks, s);
+    if (read_c) return launch_wide<kTransA, kTransB, 1, 0>(p, blocks, s);
+    if (bias) return launch_wide<kTransA, kTransB, 0, 1>(p, blocks, s);
+    return launch_wide<kTransA, kTransB, 0, 0>(p, blocks, s);
 }
 
 }  // namespace
@@ -530,11 +888,56 @@ cudaError_t simt_run(const GemmArgs& a, const DeviceInfo& dev, int* launches);
 }  // namespace
 
 size_t simt_workspace_size(const GemmArgs& a, int sm_count) {
+    const WidePlan w = plan_wide(a, sm_count);
+    if (w.ok) return w.ws_bytes;
     const int64_t top = simt_top_band_rows(a, sm_count, simt_interior_shape(a));
     return plan_schedule(a.M - top, a.N, a.K, sm_count).partial_bytes;
 }
 
+namespace {
+
+// The wide kernel (and, for stream-K, its reduction) for a problem plan_wide
+// accepted; stream_k false runs whole tiles, one block per tile.
+cudaError_t wide_run(const GemmArgs& a, const WidePlan& w, bool stream_k, int* launches) {
+    Params p{a.M, a.N, a.K, static_cast<const float*>(a.A), a.lda,
+             static_cast<const float*>(a.B), a.ldb, static_cast<float*>(a.C), a.ldc,
+             a.alpha_f, a.beta_f, 1, 1, 1, w.tiles_n, w.tiles, a.K, 1,
+             stream_k ? static_cast<float*>(a.ws) : nullptr, static_cast<const float*>(a.bias),
+             w.tiles * w.slices, w.slices, stream_k ? w.sk_ctas : 0};
+    const int64_t blocks = stream_k ? w.sk_ctas : w.tiles;
+    const bool ta = a.layout_a == DGA_COL_MAJOR, tb = a.layout_b == DGA_COL_MAJOR;
+    const bool rc = a.beta_f != 0.0f, bias = a.bias != nullptr;
+    cudaError_t e;
+    if (ta && tb) e = launch_wide_layout<true, true>(p, blocks, rc, bias, a.stream);
+    else if (ta) e = launch_wide_layout<true, false>(p, blocks, rc, bias, a.stream);
+    else if (tb) e = launch_wide_layout<false, true>(p, blocks, rc, bias, a.stream);
+    else e = launch_wide_layout<false, false>(p, blocks, rc, bias, a.stream);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    if (stream_k) {
+        sgemm_wide_sk_reduce<<<static_cast<unsigned>((w.sk_ctas - 1) * kReduceSlabs), kThreads, 0,
+                               a.stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        ++*launches;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t simt_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
+    // Whole 128 x 256 tiles, at least one full wave: the wide kernel, with the
+    // stream-K schedule when the waves are not whole and the workspace for it
+    // was given.  Without that workspace a last wave at most half full goes
+    // to the 128 x 128 kernel below (one block per SM would idle most SMs for
+    // a whole tile time), a fuller one stays on the wide kernel, whole tiles.
+    const WidePlan w = plan_wide(a, dev.sm_count);
+    if (w.ok) {
+        if (w.sk_ctas == 0) return wide_run(a, w, false, launches);
+        if (a.ws != nullptr && a.ws_bytes >= w.ws_bytes) return wide_run(a, w, true, launches);
+        if (2 * (w.tiles % dev.sm_count) > dev.sm_count) return wide_run(a, w, false, launches);
+    }
     const int64_t top = simt_top_band_rows(a, dev.sm_count, simt_interior_shape(a));
     if (top > 0 && a.ws != nullptr &&
         a.ws_bytes >= plan_schedule(a.M - top, a.N, a.K, dev.sm_count).partial_bytes) {
@@ -582,7 +985,7 @@ cudaError_t simt_run(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     if (e != cudaSuccess) return e;
     ++*launches;
     if (tail > 0 && sc.parts > 1) {
-        sgemm_tail_reduce<<<static_cast<unsigned>(tail), kThreads, 0, a.stream>>>(p);
+        sgemm_tail_reduce<<<static_cast<unsigned>(tail * kTailSlabs), kThreads, 0, a.stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         ++*launches;

@@ -93,19 +93,20 @@ def test_simt_split_tail(M, N, K):
 
 @pytest.mark.parametrize("layout", [gen.ROW_MAJOR, gen.COL_MAJOR])
 def test_simt_split_last_wave(layout):
-    """2560^2 x 768: 400 tiles on 304 two-per-SM slots, a last wave under
-    half full.  The top 1920 rows (15 tile rows, 300 tiles) run on the
-    interior kernel; the bottom 640 rows (100 tiles) are cut into three K
+    """2560 x 2432 x 768 (N not a multiple of 256, so not the wide kernel's
+    shape): 380 tiles of 128 x 128 on 304 two-per-SM slots, a last wave
+    under a third full.  The top 2048 rows (16 tile rows, 304 tiles) run on
+    the interior kernel; the bottom 512 rows (76 tiles) are cut into three K
     parts by the general kernel and reduced by a third launch.  Checked
     against the oracle on the rows around the band boundary and the last
     rows."""
     import oracle
-    M = N = 2560
+    M, N = 2560, 2432
     K = 768
     A, B, C = _mats(gen.F32, gen.F32, layout, M, N, K, seed=21)
     got = run_gpu(S, gen.F32, gen.F32, layout, A, B, C, 1.5, 0.5, M=M, N=N, K=K)
     assert dga.dga_last_launch_count() == 3
-    for r0, r1 in ((1792, 2048), (2432, 2560)):
+    for r0, r1 in ((1920, 2176), (2432, 2560)):
         ref, bound = oracle.gemm_fp(gen.F32, gen.F32, layout, r1 - r0, N, K, 1.5,
                                     A[r0:r1].contiguous(), K, B, B.shape[1], 0.5,
                                     C[r0:r1].contiguous(), N)
