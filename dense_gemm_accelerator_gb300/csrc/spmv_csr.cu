@@ -10,15 +10,20 @@
 // does both by construction with a merge-path split: the rows' end offsets
 // and the nonzero indices form two sorted lists whose merge has rows + nnz
 // items; every warp takes an equal share of that merge, whatever the row
-// lengths, and inside a chunk every lane takes 8 consecutive items.
+// lengths, and inside a chunk every lane takes 16 consecutive items.
 //
 //  * Warps are independent workers: no block-wide barrier anywhere, so while
-//    one warp waits on its loads the SM runs the others (32 warps per SM).
+//    one warp waits on its loads the SM runs the others (24 warps per SM:
+//    three blocks of eight at up to 85 registers).
 //  * Start: a warp finds where its share begins (how many row ends and
 //    nonzeros precede it) with a search over row_offsets in which each lane
 //    probes one of 32 positions per round: 5 dependent rounds for 4M rows.
 //    Its end needs no search: the chunks simply stop at the share's end.
-//  * Chunks of 256 merge items: in one round trip the warp loads the values
+//  * Chunks of 512 merge items (16 per lane: the per-chunk work -- row-end
+//    counts, scans, the carry -- is shared by twice the items of 8 per lane,
+//    which measured 5.6% faster over the whole call at three blocks per SM;
+//    24 per lane at two blocks per SM and 12 per lane at three or four were
+//    slower, and 16 per lane at four spilled): in one round trip the warp loads the values
 //    and column indices of every nonzero the chunk may hold (coalesced) and
 //    the next 32 row ends; a ballot over the row ends' merge positions
 //    (row end k sits at k + its end offset within the chunk) counts how many
@@ -29,11 +34,11 @@
 //    so they travel while that chunk gathers and sums: a chunk then waits on
 //    one round trip, its gathers, instead of two.
 //  * Lane ownership: in the usual chunk (at most 32 row ends) lane l holds
-//    the nonzeros 8l .. 8l+7 and closes the rows whose last nonzero is
-//    among them; it reads its 8 products as two 16-byte vectors (a padding
+//    the nonzeros 16l .. 16l+15 and closes the rows whose last nonzero is
+//    among them; it reads its 16 products as four 16-byte vectors (a padding
 //    that keeps them on distinct banks) and sums them in registers.  A chunk
-//    with more row ends gives each lane 8 consecutive merge items instead, so
-//    that no lane closes more than 8 rows.  Either way a shared-memory count
+//    with more row ends gives each lane 16 consecutive merge items instead, so
+//    that no lane closes more than 16 rows.  Either way a shared-memory count
 //    of each lane's row ends and a warp prefix sum tell every lane which
 //    row ends it closes.  A row
 //    that starts and ends inside one lane is written at once; the first row
@@ -65,8 +70,8 @@ __device__ int g_spmv_status;  // non-zero: the CSR arrays were malformed
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kIpt = 8;                      // merge items per lane per chunk
-constexpr int kWarpChunk = 32 * kIpt;        // 256 merge items per warp chunk
+constexpr int kIpt = 16;                     // merge items per lane per chunk
+constexpr int kWarpChunk = 32 * kIpt;        // 512 merge items per warp chunk
 constexpr int kMaxCtasPerSm = 8;             // 2048 threads per SM; the workspace allows this many
 
 struct SpParams {
@@ -199,12 +204,13 @@ struct WarpSmem {
     int owned[32];                         // row ends among each lane's items
 };
 
-// Shared-memory index of product k when lane l reads its products 8l .. 8l+7
-// as two 16-byte vectors: 4 floats of padding per 32 put the 8 lanes of each
-// quarter-warp phase on 8 different 4-bank groups.
+// Shared-memory index of product k when lane l reads its products
+// kIpt*l .. kIpt*l + kIpt - 1 as 16-byte vectors: 4 floats of padding per 32
+// put the 8 lanes of each quarter-warp phase on 8 different 4-bank groups
+// (lane l's run starts at 16l + 4 * (l / 2): bank group 4l + l/2 mod 8).
 __device__ __forceinline__ int padv(int k) { return k + ((k >> 5) << 2); }
 
-__global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
+__global__ void __launch_bounds__(kThreads, 3) spmv_merge_kernel(SpParams p) {
     __shared__ WarpSmem s_all[kThreads / 32];
     const int lane = threadIdx.x & 31;
     WarpSmem& sm = s_all[threadIdx.x >> 5];
@@ -277,12 +283,12 @@ __global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
         }
         // Which lane closes which row (warp-uniform choice).  A chunk with at
         // most 32 row ends (the usual case) gives lane l the nonzeros
-        // [8l, 8l + 8) and each row end to the lane holding the row's last
+        // [16l, 16l + 16) and each row end to the lane holding the row's last
         // nonzero (lane 0 for a row with none in the chunk); the lane reads
-        // its 8 products as two 16-byte vectors and sums them in registers.
+        // its 16 products as four 16-byte vectors and sums them in registers.
         // A chunk with more row ends (mostly empty rows) gives lane l the
-        // merge items [8l, 8l + 8) instead, row ends included, so that no
-        // lane closes more than 8 rows.
+        // merge items [16l, 16l + 16) instead, row ends included, so that no
+        // lane closes more than 16 rows.
         const bool by_nz = c_rows <= 32;
         // gather x (the loads first, all in flight together)
         float xv[kIpt];
@@ -345,14 +351,20 @@ __global__ void __launch_bounds__(kThreads, 4) spmv_merge_kernel(SpParams p) {
         };
         if (by_nz) {
             const int base = lane * kIpt;
-            const float4 q0 = *reinterpret_cast<const float4*>(&sm.prod[padv(base)]);
-            const float4 q1 = *reinterpret_cast<const float4*>(&sm.prod[padv(base) + 4]);
-            float pv[kIpt] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+            float pv[kIpt];
+#pragma unroll
+            for (int q = 0; q < kIpt / 4; ++q) {
+                const float4 v4 = *reinterpret_cast<const float4*>(&sm.prod[padv(base) + 4 * q]);
+                pv[4 * q] = v4.x;
+                pv[4 * q + 1] = v4.y;
+                pv[4 * q + 2] = v4.z;
+                pv[4 * q + 3] = v4.w;
+            }
 #pragma unroll
             for (int t = 0; t < kIpt; ++t)
                 if (base + t >= chunk_nz) pv[t] = 0.0f;
             // row end k (rs <= k < re) closes before product endl[k] - base,
-            // a position in 0 .. 8
+            // a position in 0 .. kIpt
             int k = rs;
             int at = k < re ? sm.endl[k] - base : kIpt + 1;
 #pragma unroll
