@@ -245,14 +245,16 @@ __global__ void __launch_bounds__(kThreads, 3) spmv_merge_kernel(SpParams p) {
     float val[kIpt];
     int raw0 = 0, before0 = 0;
     auto issue = [&](int zz, int rr, int nzm, int win0) {
+        // one base address per array, the 32-element steps as constant offsets
+        const int32_t* cb = p.cidx + zz + lane;
+        const float* vb = p.vals + zz + lane;
 #pragma unroll
         for (int u = 0; u < kIpt; ++u) {
-            const int k = u * 32 + lane;
             col[u] = -1;
             val[u] = 0.0f;
-            if (k < nzm) {
-                col[u] = ld_stream(p.cidx + zz + k);
-                val[u] = ld_stream(p.vals + zz + k);
+            if (u * 32 + lane < nzm) {
+                col[u] = ld_stream(cb + u * 32);
+                val[u] = ld_stream(vb + u * 32);
             }
         }
         row_ends_issue(p.offs + rr, win0, raw0, before0);
@@ -292,21 +294,31 @@ __global__ void __launch_bounds__(kThreads, 3) spmv_merge_kernel(SpParams p) {
         const bool by_nz = c_rows <= 32;
         // gather x (the loads first, all in flight together)
         float xv[kIpt];
+        const uint32_t ucols = static_cast<uint32_t>(p.cols);  // cols < 2^31
 #pragma unroll
         for (int u = 0; u < kIpt; ++u) {
-            const int k = u * 32 + lane;
             xv[u] = 0.0f;
-            if (k < c_nz) {
-                if (col[u] >= 0 && col[u] < p.cols) xv[u] = __ldg(p.x + col[u]);
+            if (u * 32 + lane < c_nz) {
+                // one unsigned compare: a negative index is a large unsigned one
+                if (static_cast<uint32_t>(col[u]) < ucols) xv[u] = __ldg(p.x + col[u]);
                 else flag_bad();
             }
         }
         // this chunk's products, then the next chunk's loads (in flight while
         // this chunk is summed and written)
+        // zero past the chunk's nonzeros, so that a lane reading all its
+        // products by vector finds zeros there (a select, not val * 0: an
+        // infinite value of the next chunk would make a NaN).  Product
+        // u * 32 + lane sits at padv = lane + 36u or pad = lane + 33u: one
+        // base address and constant offsets per ownership mode.
+        if (by_nz) {
+            float* pb = sm.prod + lane;
 #pragma unroll
-        for (int u = 0; u < kIpt; ++u) {
-            const int k = u * 32 + lane;
-            if (k < c_nz) sm.prod[by_nz ? padv(k) : pad(k)] = val[u] * xv[u];
+            for (int u = 0; u < kIpt; ++u) pb[36 * u] = u * 32 + lane < c_nz ? val[u] * xv[u] : 0.0f;
+        } else {
+            float* pb = sm.prod + lane;
+#pragma unroll
+            for (int u = 0; u < kIpt; ++u) pb[33 * u] = u * 32 + lane < c_nz ? val[u] * xv[u] : 0.0f;
         }
         const int chunk_items = n_items, chunk_nz = c_nz;
         const int r_next = r + c_rows, z_next = z + c_nz, left_next = left - (c_rows + c_nz);
@@ -360,26 +372,53 @@ __global__ void __launch_bounds__(kThreads, 3) spmv_merge_kernel(SpParams p) {
                 pv[4 * q + 2] = v4.z;
                 pv[4 * q + 3] = v4.w;
             }
-#pragma unroll
-            for (int t = 0; t < kIpt; ++t)
-                if (base + t >= chunk_nz) pv[t] = 0.0f;
             // row end k (rs <= k < re) closes before product endl[k] - base,
             // a position in 0 .. kIpt
-            int k = rs;
-            int at = k < re ? sm.endl[k] - base : kIpt + 1;
+            if (!__any_sync(0xffffffffu, re - rs > 2)) {
+                // No lane closes more than two rows (the usual chunk): one
+                // straight pass over the products with the two cut positions
+                // as predicated resets, in the same order of additions as the
+                // general loop below, so the sums are the same bits -- without
+                // its branches, which the warp takes at almost every step
+                // because some lane closes a row there.
+                const int n_ends = re - rs;
+                const int a1 = n_ends >= 1 ? sm.endl[rs] - base : -1;
+                const int a2 = n_ends >= 2 ? sm.endl[rs + 1] - base : -1;
+                float mid = 0.0f;
 #pragma unroll
-            for (int t = 0; t < kIpt; ++t) {
-                while (at == t) {
+                for (int t = 0; t <= kIpt; ++t) {
+                    if (a1 == t) {
+                        head = run;
+                        run = 0.0f;
+                    }
+                    if (a2 == t) {
+                        mid = run;
+                        run = 0.0f;
+                    }
+                    if (t < kIpt) run += pv[t];
+                }
+                if (n_ends >= 2) {
+                    float* dst = y_r + rs + 1;  // the whole row lies in this lane's items
+                    const float old = p.beta != 0.0f ? *dst : 0.0f;
+                    *dst = fmaf(p.beta, old, p.alpha * mid);
+                }
+            } else {
+                int k = rs;
+                int at = k < re ? sm.endl[k] - base : kIpt + 1;
+#pragma unroll
+                for (int t = 0; t < kIpt; ++t) {
+                    while (at == t) {
+                        close_row(k);
+                        ++k;
+                        at = k < re ? sm.endl[k] - base : kIpt + 1;
+                    }
+                    run += pv[t];
+                }
+                while (at == kIpt) {
                     close_row(k);
                     ++k;
                     at = k < re ? sm.endl[k] - base : kIpt + 1;
                 }
-                run += pv[t];
-            }
-            while (at == kIpt) {
-                close_row(k);
-                ++k;
-                at = k < re ? sm.endl[k] - base : kIpt + 1;
             }
         } else {
             const int items_here = max(0, min(kIpt, chunk_items - lane * kIpt));
