@@ -1134,8 +1134,10 @@ cudaError_t launch_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const Tc
     return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
 }
 
-// Clusters of two that fit at once on this device (queried once per kernel).
-template <typename Kern>
+// Clusters of two that fit at once on this device (queried once per kernel
+// and device: the template arguments name the kernel, since every pair
+// kernel has the same function type and would otherwise share one cache).
+template <uint32_t kFmt, bool kI8, typename TOut, typename Kern>
 int max_pair_clusters(Kern kern, int smem, int threads, const DeviceInfo& dev) {
     static int cached[64] = {};
     static std::mutex mu;
@@ -1170,7 +1172,8 @@ cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, con
     if (smem > dev.max_smem_optin) return cudaErrorInvalidConfiguration;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    const int clusters = std::min<int64_t>(p.num_tiles, max_pair_clusters(kern, smem, threads, dev));
+    const int clusters = std::min<int64_t>(
+        p.num_tiles, max_pair_clusters<kFmt, kI8, TOut>(kern, smem, threads, dev));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * std::max(clusters, 1)));
     cfg.blockDim = dim3(threads);
