@@ -91,7 +91,6 @@ struct SpParams {
 
 __device__ __forceinline__ void flag_bad() { atomicExch(&g_spmv_status, 1); }
 
-__device__ __forceinline__ int64_t lmin(int64_t a, int64_t b) { return a < b ? a : b; }
 
 // Streamed arrays (values, column indices) are read once: keep them out of L1
 // so that L1 holds the x elements the gathers reuse.
@@ -241,8 +240,10 @@ __global__ void __launch_bounds__(kThreads, 3) spmv_merge_kernel(SpParams p) {
     // chunk) and its first 32 row ends.  They are issued one chunk ahead --
     // while the previous chunk gathers x and sums -- so that a chunk waits on
     // one round trip (its gathers) instead of two.
-    int32_t col[kIpt];
-    float val[kIpt];
+    // (entries past a chunk's nonzeros keep stale values: only the first c_nz
+    // are ever read, so they are set once here rather than every chunk)
+    int32_t col[kIpt] = {};
+    float val[kIpt] = {};
     int raw0 = 0, before0 = 0;
     auto issue = [&](int zz, int rr, int nzm, int win0) {
         // one base address per array, the 32-element steps as constant offsets
@@ -250,8 +251,6 @@ __global__ void __launch_bounds__(kThreads, 3) spmv_merge_kernel(SpParams p) {
         const float* vb = p.vals + zz + lane;
 #pragma unroll
         for (int u = 0; u < kIpt; ++u) {
-            col[u] = -1;
-            val[u] = 0.0f;
             if (u * 32 + lane < nzm) {
                 col[u] = ld_stream(cb + u * 32);
                 val[u] = ld_stream(vb + u * 32);
