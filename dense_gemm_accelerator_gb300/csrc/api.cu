@@ -436,6 +436,26 @@ int dga_probe_fp32_fma(int packed, int64_t iters, float* out, int64_t out_floats
     return DGA_OK;
 }
 
+int dga_probe_naive_sgemm(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+                          dga_stream_t stream) {
+    constexpr int64_t kMaxElems = int64_t{1} << 31;  // every index stays below 2^31
+    if (M < 1 || M > 65536) return -1;
+    if (N < 1 || N > 65536) return -2;
+    if (K < 1 || K > 65536 || M * K >= kMaxElems || K * N >= kMaxElems || M * N >= kMaxElems)
+        return -3;
+    if (A == nullptr) return -4;
+    if (B == nullptr) return -5;
+    if (C == nullptr) return -6;
+    DeviceInfo dev;
+    cudaError_t e = current_device_info(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev.major != 10 || dev.minor != 3) return DGA_ERR_DEVICE;
+    e = naive_probe_launch(M, N, K, A, B, C, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_launches = 1;
+    return DGA_OK;
+}
+
 const char* dga_status_string(int status) {
     if (status < 0) return "invalid argument (the negated value is its 1-based position)";
     switch (status) {
@@ -452,6 +472,6 @@ const char* dga_status_string(int status) {
     }
 }
 
-int dga_version(void) { return 200; }  // 0.2.0: the FP32 FMA-rate probe; 72 MiB no-alloc scratch
+int dga_version(void) { return 300; }  // 0.3.0: wide SIMT kernel with stream-K; naive-GEMM counter probe
 
 }  // extern "C"

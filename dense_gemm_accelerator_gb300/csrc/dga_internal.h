@@ -86,6 +86,11 @@ int64_t fma_probe_out_floats(int sm_count);
 cudaError_t fma_probe_launch(int packed, int64_t iters, float* out, int sm_count, double* flops,
                              cudaStream_t stream);
 
+// Naive GEMM for counter calibration (measurement only): C = A * B, all
+// row-major and contiguous, one thread per output in 16 x 16 blocks.
+cudaError_t naive_probe_launch(int64_t M, int64_t N, int64_t K, const float* A, const float* B,
+                               float* C, cudaStream_t stream);
+
 bool tc_supports(const GemmArgs& a);
 size_t tc_workspace_size(const GemmArgs& a);
 cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);

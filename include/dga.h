@@ -251,6 +251,25 @@ int dga_probe_fp32_fma(int packed, int64_t iters, float* out, int64_t out_floats
  * (152 SMs assumed when no device can be queried). */
 int64_t dga_probe_fp32_fma_out_floats(void);
 
+/*
+ * Measurement helper, not part of any GEMM: the naive GEMM of "GEMM
+ * optimisation, part 0" (chongfengling.github.io), section 2 -- one thread
+ * per element of C, accumulating A(i, k) * B(k, j) over k in fp32 (fused
+ * multiply-adds in ascending k), launched in blocks of 16 x 16 threads with
+ * the block's x along the columns of C.  It is the kernel whose hardware
+ * counters that page prints (section 2.3: at M = N = K = 2048, 536,870,912
+ * global load requests and 1,073,741,824 sectors), kept so that the counter
+ * method behind this library's profiles can be checked against them.
+ *
+ * C <- A * B with A (M x K), B (K x N) and C (M x N) row-major and contiguous
+ * (leading dimensions K, N and N), device pointers, enqueued on `stream`.
+ * Errors: -1 M, -2 N outside [1, 65536]; -3 K outside [1, 65536] or a matrix
+ * of 2^31 elements or more; -4 A, -5 B, -6 C null; DGA_ERR_DEVICE,
+ * DGA_ERR_CUDA.
+ */
+int dga_probe_naive_sgemm(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
+                          dga_stream_t stream);
+
 /* The cudaError_t value behind the last DGA_ERR_CUDA on this host thread. */
 int dga_last_cuda_error(void);
 

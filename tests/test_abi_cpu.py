@@ -256,3 +256,15 @@ def test_fma_probe_argument_errors(lib):
     # valid arguments need the device, absent here
     assert dga.dga_probe_fp32_fma(0, 10, 0x1000, out_floats, ctypes.byref(flops),
                                   None) in (dga.ERR_CUDA, dga.ERR_DEVICE)
+
+
+def test_naive_probe_argument_errors_before_the_device():
+    # the counter-calibration probe checks its arguments before touching a device
+    f = dga.dga_probe_naive_sgemm
+    assert f(0, 8, 8, 0x1000, 0x2000, 0x3000, None) == -1
+    assert f(8, 65537, 8, 0x1000, 0x2000, 0x3000, None) == -2
+    assert f(8, 8, 0, 0x1000, 0x2000, 0x3000, None) == -3
+    assert f(65536, 8, 65536, 0x1000, 0x2000, 0x3000, None) == -3  # M * K = 2^32 elements
+    assert f(8, 8, 8, None, 0x2000, 0x3000, None) == -4
+    assert f(8, 8, 8, 0x1000, None, 0x3000, None) == -5
+    assert f(8, 8, 8, 0x1000, 0x2000, None, None) == -6

@@ -55,3 +55,31 @@ def test_probe_outputs_and_flops(packed):
     got = out.cpu().numpy()
     np.testing.assert_array_equal(got, _expected(packed, iters, n))
     assert dga.dga_probe_fp32_fma(packed, iters, out.data_ptr(), n - 1, ctypes.byref(flops), s) == -4
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (67, 53, 45), (130, 257, 300)])
+def test_naive_probe_matches_the_oracle(M, N, K):
+    # the counter-calibration kernel computes C = A * B: exact on small
+    # integers (all partial sums below 2^24), within the oracle's bound on
+    # uniform inputs
+    import oracle
+    from dense_gemm_accelerator_gb300 import inputs as gen
+    from tests.helpers import assert_close, assert_exact
+    g = torch.Generator().manual_seed(M + N + K)
+    s = torch.cuda.current_stream().cuda_stream
+    for small in (True, False):
+        if small:
+            A = gen.small_int_matrix((M, K), gen.F32, g)
+            B = gen.small_int_matrix((K, N), gen.F32, g)
+        else:
+            A = gen.random_matrix((M, K), gen.F32, g)
+            B = gen.random_matrix((K, N), gen.F32, g)
+        Ad, Bd = A.cuda(), B.cuda()
+        C = torch.full((M, N), float("nan"), device="cuda")
+        assert dga.dga_probe_naive_sgemm(M, N, K, Ad.data_ptr(), Bd.data_ptr(), C.data_ptr(), s) == dga.OK
+        assert dga.dga_sync_status(s) == dga.OK
+        ref, bound = oracle.gemm_fp(gen.F32, gen.F32, gen.ROW_MAJOR, M, N, K, 1.0, A, K, B, N, 0.0)
+        if small:
+            assert_exact(C.cpu(), ref, gen.F32, f"naive {M}x{N}x{K} small integers")
+        else:
+            assert_close(C.cpu(), ref, bound, gen.F32, f"naive {M}x{N}x{K}")
