@@ -193,3 +193,51 @@ def test_full_size_workload():
     ref, bound = oracle.spmv_csr(w.M, w.N, offs, ci, vals, x)
     err = np.abs(y.cpu().double().numpy() - ref)
     assert (err <= bound).all(), f"{int((err > bound).sum())} rows outside the bound"
+
+
+@pytest.mark.parametrize("length", [1, 5, 8, 16, 17, "mixed"])
+def test_row_lengths_at_lane_boundaries(length):
+    # a lane of a chunk holds 16 consecutive entries: rows of 8 close exactly
+    # two rows in every lane (the branch-free path), rows of 5 close three in
+    # some lanes (the general loop), rows of 16 and 17 end on and just past
+    # lane boundaries, rows of 1 give chunks of more than 32 row ends (each
+    # lane then takes 16 consecutive merge items); mixed lengths 0-40 combine
+    # them within a warp
+    g = torch.Generator().manual_seed(40 + (length if isinstance(length, int) else 0))
+    n_rows = 30000
+    if length == "mixed":
+        lengths = torch.randint(0, 41, (n_rows,), generator=g).tolist()
+    else:
+        lengths = [length] * n_rows
+    offs, ci, vals = _from_lengths(lengths, 7000, g)
+    x = torch.rand(7000, generator=g) * 2 - 1
+    y = torch.rand(n_rows, generator=g)
+    _check(offs, ci, vals, x, what=f"rows of {length}")
+    _check(offs, ci, vals, x, y, alpha=-1.5, beta=0.25, what=f"rows of {length}, alpha beta")
+    # integer-valued inputs: every order of the sums gives the same exact value
+    vi = torch.randint(-3, 4, vals.shape, generator=g).float()
+    xi = torch.randint(-3, 4, x.shape, generator=g).float()
+    got, ref = _check(offs, ci, vi, xi, what=f"rows of {length}, integers")
+    assert np.array_equal(got.double().numpy(), ref)
+
+
+def test_infinite_values_stay_in_their_rows():
+    # every other row holds +inf entries (x > 0, so each of its products is
+    # +inf): those rows are +inf and no NaN or inf reaches the rows between
+    # them, wherever the chunk boundaries fall
+    g = torch.Generator().manual_seed(50)
+    lengths = torch.randint(1, 30, (40000,), generator=g).tolist()
+    offs, ci, vals = _from_lengths(lengths, 3000, g)
+    row_of = torch.repeat_interleave(torch.arange(len(lengths)), torch.tensor(lengths))
+    inf_rows = row_of % 2 == 0
+    vals[inf_rows] = float("inf")
+    x = torch.rand(3000, generator=g) * 0.5 + 0.5
+    got = _run(offs, ci, vals, x)
+    even = torch.arange(len(lengths)) % 2 == 0
+    assert torch.isinf(got[even]).all() and (got[even] > 0).all()
+    finite_vals = vals.clone()
+    finite_vals[inf_rows] = 0.0
+    ref, bound = oracle.spmv_csr(len(lengths), 3000, offs, ci, finite_vals, x)
+    odd = ~even.numpy()
+    err = np.abs(got.double().numpy()[odd] - ref[odd])
+    assert np.isfinite(got.numpy()[odd]).all() and (err <= bound[odd]).all()
