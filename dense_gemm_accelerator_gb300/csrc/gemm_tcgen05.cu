@@ -794,6 +794,11 @@ struct PackJob {
     // used when fast_div, i.e. when the job has fewer than 2^31 units
     uint64_t div_m;
     int div_s, fast_div;
+    // int8 only: the source is the operand's transpose, element (k, r) at
+    // src[k*ld_src + r] for k < K, r < rows, and the copy transposes it in
+    // 64 (k) x 128 (r) tiles, tiles_k of them along each 128 rows
+    int transpose;
+    int64_t tiles_k;
 };
 
 // Eight int8 values (byte q of v is value q) as eight exact bf16, in memory
@@ -876,6 +881,31 @@ __device__ __forceinline__ void pack_rows_body<int8_t>(const PackJob<int8_t>& j,
         const int64_t r = unit_row(j, wu), seg = wu - r * j.units_per_row;
         const int8_t* row = j.src + r * j.ld_src;
         uint64_t w[4];
+        // a unit whose 1024 elements all lie in the row (and, for unaligned
+        // rows, whose word pairs all lie in the operand) loads without checks
+        const int8_t* p = row + seg * 1024 + 8 * lane;
+        const uintptr_t ulast = reinterpret_cast<uintptr_t>(row + seg * 1024 + 1016);
+        const bool whole = seg * 1024 + 1024 <= j.K &&
+                           (j.vec_src || ((reinterpret_cast<uintptr_t>(row + seg * 1024) & ~static_cast<uintptr_t>(7)) >= lo &&
+                                          (ulast & ~static_cast<uintptr_t>(7)) + 16 <= hi));
+        if (whole) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uintptr_t a = reinterpret_cast<uintptr_t>(p + 256 * q);
+                if (j.vec_src) {
+                    w[q] = ldg_u64(a);
+                } else {
+                    const uintptr_t base = a & ~static_cast<uintptr_t>(7);
+                    const uint64_t x0 = ldg_u64(base), x1 = ldg_u64(base + 8);
+                    const int sh = static_cast<int>(a - base) * 8;
+                    w[q] = sh ? (x0 >> sh) | (x1 << (64 - sh)) : x0;
+                }
+            }
+            uint16_t* d = j.dst + r * j.ld_dst + seg * 1024 + 8 * lane;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(d + 256 * q) = int8x8_to_bf16(w[q]);
+            continue;
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int64_t v = seg * 128 + lane + 32 * q;
@@ -912,20 +942,143 @@ __device__ __forceinline__ void pack_rows_body<int8_t>(const PackJob<int8_t>& j,
     }
 }
 
-// Both operands' 16-bit repacks in one launch: blocks [0, a.blocks) do A's
-// job, the rest B's (a job with 0 blocks is absent).  Every repack copies its
-// source row by row, keeping the layout (an MN-major operand stays MN-major),
-// so none transposes.  One launch lets B's blocks fill the SMs while A's
+// The 8 source bytes (k, r .. r + 7) of a transposing int8 job, zero past
+// the source's extent: one aligned word where rows are 8-byte aligned, else
+// the two aligned words around them funnel-shifted (only where both lie in
+// [src, src_end)), else byte by byte.
+__device__ __forceinline__ uint64_t load_i8x8(const PackJob<int8_t>& j, int64_t k, int64_t r) {
+    if (k >= j.K || r >= j.rows) return 0;
+    const int8_t* p = j.src + k * j.ld_src + r;
+    if (r + 8 <= j.rows) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        if (j.vec_src) return ldg_u64(a);
+        const uintptr_t base = a & ~static_cast<uintptr_t>(7);
+        if (base >= reinterpret_cast<uintptr_t>(j.src) &&
+            base + 16 <= reinterpret_cast<uintptr_t>(j.src_end)) {
+            const uint64_t x0 = ldg_u64(base), x1 = ldg_u64(base + 8);
+            const int sh = static_cast<int>(a - base) * 8;
+            return sh ? (x0 >> sh) | (x1 << (64 - sh)) : x0;
+        }
+    }
+    uint64_t w = 0;
+    for (int b = 0; b < 8 && r + b < j.rows; ++b)
+        w |= static_cast<uint64_t>(static_cast<uint8_t>(p[b])) << (8 * b);
+    return w;
+}
+
+// Transposing int8 job: dst[r][k] = src[k*ld_src + r] as bf16, a 64 (k) x
+// 128 (r) tile per block at a time.  Thread t loads the 8 source bytes at
+// r = 8*(t % 16) of the 4 rows k = 4*(t / 16) .. + 3 (a warp reads 2 x 128
+// contiguous bytes per load), regroups them with byte permutes into 8 words
+// of 4 consecutive k, one per r, and stores them to a shared tile of 128 rows
+// x 16 words, word kq of row r at kq ^ h(r), h(r) = ((r >> 1) & 1) |
+// (((r >> 3) & 7) << 1): the stores hit 16 banks per instruction (every
+// lane's row has the same parity, so 16 is the most a row stride of 64 bytes
+// allows) and the reads below all 32.  A warp then converts and writes whole
+// 128-byte output segments, 4 rows x 8 vectors of 8 k per instruction.
+__device__ __forceinline__ void pack_tiles_i8_body(const PackJob<int8_t>& j, int64_t blk,
+                                                   int64_t nblocks, uint32_t* tile) {
+    const int t = threadIdx.x;
+    const int64_t tiles = ((j.rows + 127) / 128) * j.tiles_k;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(j.src), hi = reinterpret_cast<uintptr_t>(j.src_end);
+    for (int64_t i = blk; i < tiles; i += nblocks) {
+        const int64_t tr = unit_row(j, i), tk = i - tr * j.tiles_k;
+        const int64_t r0 = tr * 128, k0 = tk * 64;
+        const int wn = t & 15, kq = t >> 4;
+        // an interior tile (all 64 x 128 bytes inside the operand, and for
+        // unaligned rows every word pair around them too) loads without checks
+        const uintptr_t first = reinterpret_cast<uintptr_t>(j.src + k0 * j.ld_src + r0);
+        const uintptr_t last = reinterpret_cast<uintptr_t>(j.src + (k0 + 63) * j.ld_src + r0 + 120);
+        const bool interior = k0 + 64 <= j.K && r0 + 128 <= j.rows &&
+                              (j.vec_src || ((first & ~static_cast<uintptr_t>(7)) >= lo &&
+                                             (last & ~static_cast<uintptr_t>(7)) + 16 <= hi));
+        uint64_t w[4];
+        if (interior) {
+            const int8_t* p = j.src + (k0 + 4 * kq) * j.ld_src + r0 + 8 * wn;
+            if (j.vec_src) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) w[q] = ldg_u64(reinterpret_cast<uintptr_t>(p + q * j.ld_src));
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(p + q * j.ld_src);
+                    const uintptr_t base = a & ~static_cast<uintptr_t>(7);
+                    const uint64_t x0 = ldg_u64(base), x1 = ldg_u64(base + 8);
+                    const int sh = static_cast<int>(a - base) * 8;
+                    w[q] = sh ? (x0 >> sh) | (x1 << (64 - sh)) : x0;
+                }
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = load_i8x8(j, k0 + 4 * kq + q, r0 + 8 * wn);
+        }
+        // column c of the 4 x 8 byte block: bytes (k0 + 4kq + 0..3, r0 + 8wn + c)
+        uint32_t col[8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t x0 = static_cast<uint32_t>(w[0] >> (32 * h));
+            const uint32_t x1 = static_cast<uint32_t>(w[1] >> (32 * h));
+            const uint32_t x2 = static_cast<uint32_t>(w[2] >> (32 * h));
+            const uint32_t x3 = static_cast<uint32_t>(w[3] >> (32 * h));
+            const uint32_t p01 = __byte_perm(x0, x1, 0x5140), q01 = __byte_perm(x0, x1, 0x7362);
+            const uint32_t p23 = __byte_perm(x2, x3, 0x5140), q23 = __byte_perm(x2, x3, 0x7362);
+            col[4 * h + 0] = __byte_perm(p01, p23, 0x5410);
+            col[4 * h + 1] = __byte_perm(p01, p23, 0x7632);
+            col[4 * h + 2] = __byte_perm(q01, q23, 0x5410);
+            col[4 * h + 3] = __byte_perm(q01, q23, 0x7632);
+        }
+        __syncthreads();  // the previous tile's reads are done
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int r = 8 * wn + c;
+            const int hr = ((r >> 1) & 1) | (((r >> 3) & 7) << 1);
+            tile[r * 16 + (kq ^ hr)] = col[c];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int pass = 0; pass < 4; ++pass) {
+            const int r = pass * 32 + (t >> 3), g = t & 7;
+            const int hr = ((r >> 1) & 1) | (((r >> 3) & 7) << 1);
+            // words 2g and 2g + 1 sit together at 2 (g ^ (hr >> 1)), swapped when hr is odd
+            const uint2 v = *reinterpret_cast<const uint2*>(tile + r * 16 + 2 * (g ^ (hr >> 1)));
+            const uint32_t k_lo = (hr & 1) ? v.y : v.x, k_hi = (hr & 1) ? v.x : v.y;
+            const int64_t row = r0 + r, k = k0 + 8 * g;
+            if (row < j.rows && k < j.ld_dst)
+                *reinterpret_cast<uint4*>(j.dst + row * j.ld_dst + k) =
+                    int8x8_to_bf16(static_cast<uint64_t>(k_lo) | (static_cast<uint64_t>(k_hi) << 32));
+        }
+    }
+}
+
+// Both operands' repacks in one launch: blocks [0, a.blocks) do A's job, the
+// rest B's (a job with 0 blocks is absent).  A 16-bit repack copies its
+// source row by row, keeping the layout (an MN-major operand stays MN-major);
+// an int8 one re-encodes as bf16 and leaves both operands K-major, copying
+// row-major A and column-major B by rows and transposing column-major A and
+// row-major B by tiles.  One launch lets B's blocks fill the SMs while A's
 // drain, and the GEMM behind it is released (griddepcontrol.launch_dependents)
 // as soon as every block has started: its prologue overlaps the repack's
 // tail, and it reads the output only after griddepcontrol.wait, i.e. after
 // this grid has completed.
 template <typename TSrc>
+__device__ __forceinline__ void pack_job_body(const PackJob<TSrc>& j, int64_t blk, uint32_t* tile) {
+    if constexpr (sizeof(TSrc) == 1) {
+        if (j.transpose) {
+            pack_tiles_i8_body(j, blk, j.blocks, tile);
+            return;
+        }
+    }
+    pack_rows_body(j, blk, j.blocks);
+}
+
+template <typename TSrc>
 __global__ void __launch_bounds__(256) pack_pair_kernel(PackJob<TSrc> a, PackJob<TSrc> b) {
+    // the transposing int8 tiles' staging (unused by 16-bit repacks)
+    __shared__ __align__(16) uint32_t tile[sizeof(TSrc) == 1 ? 128 * 16 : 1];
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t blk = blockIdx.x;
-    if (blk < a.blocks) pack_rows_body(a, blk, a.blocks);
-    else pack_rows_body(b, blk - a.blocks, b.blocks);
+    if (blk < a.blocks) pack_job_body(a, blk, tile);
+    else pack_job_body(b, blk - a.blocks, tile);
 }
 
 // fp32 operands of the TF32 path, same contract with 4-byte elements:
@@ -1075,12 +1228,13 @@ PackPlan plan_for(const GemmArgs& a) {
     }
     pl.kp = round_up(a.K, 8);
     // TMA needs 16-byte row strides and a 16-byte aligned base; INT8 is
-    // always re-encoded (as bf16).  Either way the copy keeps the layout, so
-    // no repack transposes: MN-major operands are read MN-major from it.
+    // always re-encoded (as bf16), into K-major rows whatever the source's
+    // layout (the MMA reads a K-major B faster).  A 16-bit copy keeps the
+    // layout: MN-major operands are read MN-major from it.
     pl.pack_a = i8 || a.lda % 8 != 0 || !aligned(a.A, 16);
     pl.pack_b = i8 || a.ldb % 8 != 0 || !aligned(a.B, 16);
-    pl.a_mn = a.layout_a == DGA_COL_MAJOR;
-    pl.b_mn = a.layout_b == DGA_ROW_MAJOR;
+    pl.a_mn = !i8 && a.layout_a == DGA_COL_MAJOR;
+    pl.b_mn = !i8 && a.layout_b == DGA_ROW_MAJOR;
     pl.a_ld = pl.a_mn ? round_up(a.M, 8) : pl.kp;
     pl.b_ld = pl.b_mn ? round_up(a.N, 8) : pl.kp;
     pl.a_bytes = pl.pack_a ? round_up((pl.a_mn ? a.K : a.M) * pl.a_ld * 2, kWsAlign) : 0;
@@ -1227,6 +1381,34 @@ PackJob<TSrc> pack_job(const void* src, int64_t ld_src, int64_t rows, int64_t K,
     return j;
 }
 
+// A transposing int8 job: dst (rows x ld_dst) with dst[r][k] = src[k*ld_src + r]
+// for k < K, r < rows; one block per 64 x 128 tile, up to 256 per SM.
+PackJob<int8_t> pack_job_transposed(const void* src, int64_t ld_src, int64_t rows, int64_t K,
+                                    void* dst, int64_t ld_dst, int sm_count) {
+    PackJob<int8_t> j{};
+    j.src = static_cast<const int8_t*>(src);
+    j.src_end = j.src + (K - 1) * ld_src + rows;
+    j.ld_src = ld_src;
+    j.rows = rows;
+    j.K = K;
+    j.dst = static_cast<uint16_t*>(dst);
+    j.ld_dst = ld_dst;
+    j.vec_src = ld_src % 8 == 0 && aligned(src, 8);
+    j.transpose = 1;
+    j.tiles_k = (ld_dst + 63) / 64;
+    const int64_t tiles = (rows + 127) / 128 * j.tiles_k;
+    j.blocks = std::max<int64_t>(1, std::min<int64_t>(tiles, static_cast<int64_t>(sm_count) * 256));
+    // tile i -> its 128 rows i / tiles_k through the reciprocal, as for row units
+    j.units_per_row = j.tiles_k;
+    j.fast_div = tiles < (int64_t{1} << 31) ? 1 : 0;
+    int l = 0;
+    while ((int64_t{1} << l) < j.tiles_k) ++l;
+    j.div_s = 31 + l;
+    j.div_m = ((uint64_t{1} << (31 + l)) + static_cast<uint64_t>(j.tiles_k) - 1) /
+              static_cast<uint64_t>(j.tiles_k);
+    return j;
+}
+
 // Launches the repack jobs (either may be absent: blocks = 0) as one grid.
 template <typename TSrc>
 cudaError_t launch_pack_pair(const PackJob<TSrc>& a, const PackJob<TSrc>& b, cudaStream_t s) {
@@ -1303,7 +1485,7 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
             ++*launches;
         }
     } else if (pl.pack_a || pl.pack_b) {
-        // both 16-bit repacks in one launch, each copying its source row by
+        // both repacks in one launch; a 16-bit one copies its source row by
         // row (an MN-major operand's rows run along M or N, one per k)
         auto run = [&](auto tag) {
             using T = decltype(tag);
@@ -1316,7 +1498,17 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
                              : pack_job<T>(a.B, a.ldb, a.N, a.K, dst_b, pl.b_ld, dev.sm_count);
             return launch_pack_pair<T>(ja, jb, a.stream);
         };
-        e = i8 ? run(int8_t{}) : (bf16 ? run(__nv_bfloat16{}) : run(__half{}));
+        if (i8) {
+            // both operands to K-major bf16: column-major A and row-major B
+            // are transposed on the way
+            PackJob<int8_t> ja = tr_a ? pack_job_transposed(a.A, a.lda, a.M, a.K, dst_a, pl.kp, dev.sm_count)
+                                      : pack_job<int8_t>(a.A, a.lda, a.M, a.K, dst_a, pl.kp, dev.sm_count);
+            PackJob<int8_t> jb = tr_b ? pack_job_transposed(a.B, a.ldb, a.N, a.K, dst_b, pl.kp, dev.sm_count)
+                                      : pack_job<int8_t>(a.B, a.ldb, a.N, a.K, dst_b, pl.kp, dev.sm_count);
+            e = launch_pack_pair<int8_t>(ja, jb, a.stream);
+        } else {
+            e = bf16 ? run(__nv_bfloat16{}) : run(__half{});
+        }
         if (e != cudaSuccess) return e;
         ++*launches;
     }

@@ -2,7 +2,7 @@
 // device memory.
 //
 // The regular INT8 path needs a scratch buffer (the operands re-encoded as
-// bf16, each in its own layout) that the caller passes in as `workspace`.  Some callers have
+// bf16, both K-major) that the caller passes in as `workspace`.  Some callers have
 // no way to provide one: a plugin that is handed only its input and output
 // buffers by a host application, a serving engine that reserves all device
 // memory when it starts and refuses allocations afterwards, or a

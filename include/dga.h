@@ -147,8 +147,8 @@ int dga_gemm(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
  * -19 path; the bias must not overlap C (DGA_ERR_OVERLAP).  Other arguments
  * as for dga_gemm_ex.  The SKINNY family needs a row-major A; the tensor-core
  * family reads a column-major A in place (MN-major) and copies it into the
- * workspace only for INT8 (re-encoded as bf16, layout kept), for TF32
- * (transposed to K-major) or when TMA cannot express lda.
+ * workspace only for INT8 (re-encoded as bf16 and transposed to K-major), for
+ * TF32 (transposed to K-major) or when TMA cannot express lda (layout kept).
  */
 int dga_gemm_general(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_a,
                      dga_layout layout_b, int64_t M, int64_t N, int64_t K,
@@ -293,10 +293,9 @@ const char* dga_status_string(int status);
  *   - every GPU on which it is called holds that area until the process exits;
  *   - the call is refused with DGA_ERR_WORKSPACE, before anything is
  *     enqueued, when the operands re-encoded as bf16 exceed it: A takes
- *     M * round_up(K, 8) * 2 bytes, B N * round_up(K, 8) * 2 bytes when
- *     column-major and K * round_up(N, 8) * 2 bytes when row-major (each
- *     rounded up to 256 bytes); e.g. M = 4093, N = 4099, K = 4096 with a
- *     row-major B (64.04 MiB) fits;
+ *     M * round_up(K, 8) * 2 bytes and B N * round_up(K, 8) * 2 bytes in
+ *     either layout (both are re-encoded K-major; each rounded up to 256
+ *     bytes); e.g. M = 4093, N = 4099, K = 4096 (64 MiB) fits;
  *   - all calls share the area and it keeps the last call's contents
  *     (nothing in it needs to start at zero: each call rewrites all it reads);
  *     calls that overlap on the GPU -- other streams, other host threads --

@@ -93,6 +93,14 @@ def test_workspace_size_query(lib):
     ws = dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
                                      w.N, w.N, dga.PATH_TCGEN05)
     assert ws >= 2 * (w.M + w.N) * w.K
+    # ... both K-major whatever B's layout: K padded to 8, each copy to 256 bytes
+    def ru(x, m):
+        return (x + m - 1) // m * m
+    for M, N, K in ((4093, 4099, 4096), (77, 91, 601), (5, 3, 1)):
+        want = ru(M * ru(K, 8) * 2, 256) + ru(N * ru(K, 8) * 2, 256)
+        for layout, ldb in ((gen.ROW_MAJOR, N + 3), (gen.COL_MAJOR, K + 5)):
+            assert dga.dga_gemm_workspace_size(gen.I8, gen.I32, layout, M, N, K, K, ldb, N,
+                                               dga.PATH_TCGEN05) == want, (M, N, K, layout)
     # column-major bf16 with aligned leading dimensions needs nothing
     w = W["bf16_8192"]
     assert dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,

@@ -136,6 +136,23 @@ def test_tc_int8_col_major_a(M, N, K):
                   with_bias=False)
 
 
+@pytest.mark.parametrize("M,N,K,pad", [(5, 3, 1, 0), (130, 7, 9, 3), (129, 129, 65, 0),
+                                       (131, 300, 200, 3), (257, 136, 72, 1), (70, 1025, 130, 5)])
+@pytest.mark.parametrize("layout_a,layout_b", [(gen.ROW_MAJOR, gen.ROW_MAJOR),
+                                               (gen.COL_MAJOR, gen.ROW_MAJOR),
+                                               (gen.COL_MAJOR, gen.COL_MAJOR),
+                                               (gen.ROW_MAJOR, gen.COL_MAJOR)])
+def test_tc_int8_transposing_repack_edges(M, N, K, pad, layout_a, layout_b):
+    # int8 operands are re-encoded K-major: a column-major A and a row-major B
+    # are transposed in 64 (k) x 128 (row) tiles.  The shapes put ragged edges
+    # in both tile directions (N, M one past or short of 128-row tiles; K one,
+    # a few, or past 64-deep tiles, padded to 8), and the padded leading
+    # dimensions make source rows that are not 8-byte aligned (the
+    # funnel-shifted loads and the bytewise ones at the operand's end)
+    check_general(T, gen.I8, gen.I32, layout_a, layout_b, M, N, K, 3, -2, with_bias=True,
+                  seed=M + N + K, pad=pad)
+
+
 @pytest.mark.parametrize("pair", [(gen.F32, gen.F32), (gen.BF16, gen.BF16), (gen.F16, gen.F32),
                                   (gen.I8, gen.I32)])
 def test_generic_col_major_a(pair):

@@ -159,9 +159,10 @@ def test_tc_int8_col_major_alpha_beta():
 
 
 def test_tc_int8_one_repack_launch():
-    # both operands are repacked (each by rows, a row-major B staying row-major)
-    # in one launch, and the GEMM follows it as a programmatic dependent: two
-    # launches, the result still bit-exact (ragged sizes, ldb not a multiple of 16)
+    # both operands are repacked (A by rows, the row-major B transposed to
+    # K-major) in one launch, and the GEMM follows it as a programmatic
+    # dependent: two launches, the result still bit-exact (ragged sizes, ldb
+    # not a multiple of 16)
     check(T, gen.I8, gen.I32, gen.ROW_MAJOR, 300, 259, 1030, 1, 0, seed=4, ldb=263)
     assert dga.dga_last_launch_count() == 2
     # bf16 with leading dimensions TMA cannot express (lda = 99, ldb = 101):

@@ -75,10 +75,10 @@ def test_noalloc_matches_dga_gemm_on_two_calls(first, second):
 
 
 def test_noalloc_refuses_sizes_beyond_its_scratch():
-    # bf16-encoded operands: A takes M * K * 2 bytes, the row-major B
-    # K * round_up(N, 8) * 2; 5200 * 4096 * 2 + 4096 * 4104 * 2 > 72 MiB
+    # bf16-encoded operands, both K-major: A takes M * K * 2 bytes, B
+    # N * K * 2 (K a multiple of 8); 5200 * 4096 * 2 + 4099 * 4096 * 2 > 72 MiB
     M, N, K = 5200, 4099, 4096
-    assert M * K * 2 + K * 4104 * 2 > dga.NOALLOC_SCRATCH_BYTES
+    assert M * K * 2 + N * K * 2 > dga.NOALLOC_SCRATCH_BYTES
     A, B, C = _problem(M, N, K, gen.ROW_MAJOR, 7)
     before = C.clone()
     assert _run_noalloc(gen.ROW_MAJOR, A, B, C, 1, 0) == dga.ERR_WORKSPACE
