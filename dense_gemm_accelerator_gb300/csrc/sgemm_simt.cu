@@ -48,6 +48,7 @@ namespace {
 constexpr int BM = 128, BN = 128, BK = 8;
 constexpr int kThreads = 256;
 constexpr int kAStride = BM + 4;  // floats per k-row of the A and B tiles (BM == BN)
+constexpr int64_t kSimtMaxK = int64_t{1} << 33;  // larger K: the generic kernel
 constexpr int kSimtBlocksPerSm = 2;  // register budget: 65536 / (256 * 2) = 128 per thread
 
 struct Params {
@@ -72,7 +73,7 @@ struct Params {
     const float* bias;  // N values added to every row, or null
     // Wide kernel, stream-K schedule (sk_ctas > 0): the (tile, 16-deep
     // K-slice) units, sk_slices per tile, are cut into sk_ctas equal
-    // contiguous ranges, one per block; see sgemm_wide_kernel.
+    // contiguous ranges, one per block; see sgemm_wide_sk_kernel.
     int64_t sk_units, sk_slices;
     int sk_ctas;
 };
@@ -216,11 +217,15 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc2[i][q] = 0ull;  // (+0.0f, +0.0f)
 
-    const int64_t n_slices = (k_end - k_begin + BK - 1) / BK;
+    // slices counted in 32 bits (simt_supports keeps K below 2^33): a 64-bit
+    // counter measured 1.5-5% slower in the wide kernel's main loop; here the
+    // same on average (58.0 against 57.8 TFLOP/s over the eight layout and
+    // epilogue variants at 4096^3)
+    const int n_slices = static_cast<int>((k_end - k_begin + BK - 1) / BK);
     fetch(k_begin);
     stash(0);
     __syncthreads();
-    for (int64_t s = 0; s < n_slices; ++s) {
+    for (int s = 0; s < n_slices; ++s) {
         const int buf = static_cast<int>(s & 1);
         const bool more = s + 1 < n_slices;
         // Fragments are double-buffered in registers: the shared-memory loads
@@ -247,7 +252,7 @@ __device__ __forceinline__ void block_tile(const Params& p, Smem& sm, int64_t ro
         frag(0, 0);
 #pragma unroll
         for (int k = 0; k < BK; ++k) {
-            if (k == 2 && more) fetch(k_begin + (s + 1) * BK);
+            if (k == 2 && more) fetch(k_begin + static_cast<int64_t>(s + 1) * BK);
             if (k + 1 < BK) frag((k + 1) & 1, k + 1);
             if constexpr (kColOuter) {
                 uint64_t ap[8];
@@ -486,12 +491,14 @@ Schedule plan_schedule(int64_t M, int64_t N, int64_t K, int sm_count) {
 // broadcasts and 6 128-bit shared loads), and its 16-deep K slices halve the
 // barriers per FMA.  It uses up to 255 registers, so one block of 8 warps per
 // SM.  Measured on GB300 at whole waves (M = 4864, N = K = 4096): 64.6
-// TFLOP/s against 60.6 for two 128 x 128 blocks per SM.  With one block per
-// SM a part-filled last wave would leave SMs idle for a whole tile time, so
-// problems that are not a whole number of waves run a stream-K schedule (see
-// sgemm_wide_kernel): every block does the same share of the (tile, K-slice)
-// work, and the tiles split between blocks are summed in a fixed order by
-// sgemm_wide_sk_reduce.  Thread layout: 8 warps as 2 (M) x 4 (N)
+// TFLOP/s against 60.6 for two 128 x 128 blocks per SM (66.8 once the slice
+// loop counted in 32 bits).  With one block per SM a part-filled last wave
+// would leave SMs idle for a whole tile time, so problems that are not a
+// whole number of waves run the whole waves tile by tile and the rest on a
+// stream-K schedule (sgemm_wide_sk_kernel): every block does the same share
+// of the remaining (tile, K-slice) work, and the tiles split between blocks
+// are summed in a fixed order by sgemm_wide_sk_reduce.  Thread layout: 8
+// warps as 2 (M) x 4 (N)
 // warp tiles of 64 x 64; lane = lm * 4 + ln; a thread owns rows {wm*64 +
 // lm*4 + i, wm*64 + 32 + lm*4 + i} and columns {wn*64 + h*16 + ln*4 + j},
 // i, j in 0..3, h in 0..3.  The results equal the 128 x 128 kernel's bit for
@@ -594,11 +601,14 @@ __device__ __forceinline__ void wide_block_tile(const Params& p, WideSmem<kTrans
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc2[i][q] = 0ull;
 
-    const int64_t n_slices = (k_end - k_begin) / kWBK;
+    // slices counted in 32 bits (simt_supports keeps K below 2^33): with a
+    // 64-bit counter this loop measured 1.5-5% slower (4096^3 and 4864 x
+    // 4096 x 4096, both B layouts)
+    const int n_slices = static_cast<int>((k_end - k_begin) / kWBK);
     fetch();
     stash(0);
     __syncthreads();
-    for (int64_t s = 0; s < n_slices; ++s) {
+    for (int s = 0; s < n_slices; ++s) {
         const int buf = static_cast<int>(s & 1);
         const bool more = s + 1 < n_slices;
         float a[2][8];
@@ -675,37 +685,41 @@ __device__ __forceinline__ void wide_block_tile(const Params& p, WideSmem<kTrans
     }
 }
 
-// Grid over the wide schedule.  Tile by tile (sk_ctas == 0): block b owns
-// tile b.  Otherwise one block per SM (sk_ctas blocks): the first
-// full_tiles tiles -- whole waves -- go to the blocks in turn (block c owns
-// tiles c, c + sk_ctas, ...; blocks resident together work on neighbouring
-// tiles of the grouped order, so they share A and B panels in L2), and the
-// remaining tiles are shared stream-K fashion: their units (tile t, K-slice
-// s), in the order t * sk_slices + s, are cut into sk_ctas equal contiguous
-// ranges, u0(c) = c * sk_units / sk_ctas, so that every SM does the same
-// work.  A tile a block covers whole gets the epilogue; a block's first and
-// last segments, when they cover only part of a tile, go to the workspace as
-// raw partial sums (slots 2c and 2c + 1, 128 x 256 floats each), and
-// sgemm_wide_sk_reduce adds the pieces of each such tile in block order,
-// i.e. in K order.  No block ever waits for another.
+// The wide schedule's whole tiles: block b owns tile b of the grouped order
+// (every tile, or, under stream-K, the full_tiles tiles of the whole waves:
+// blocks resident together work on neighbouring tiles, so they share A and B
+// panels in L2).  The stream-K remainder is a kernel of its own
+// (sgemm_wide_sk_kernel), so that each is compiled for its own loop alone;
+// it is released as soon as every block here has started
+// (griddepcontrol.launch_dependents) and its blocks take the SMs this grid's
+// last wave frees.
 template <bool kTransA, bool kTransB, int kReadC, int kBias>
 __global__ void __launch_bounds__(kThreads, 1) sgemm_wide_kernel(Params p) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    extern __shared__ __align__(16) unsigned char wide_smem_raw[];
+    WideSmem<kTransB>& sm = *reinterpret_cast<WideSmem<kTransB>*>(wide_smem_raw);
+    int64_t tm, tn;
+    wide_tile(blockIdx.x, p.M / kWBM, p.tiles_n, tm, tn);
+    wide_block_tile<kTransA, kTransB, kReadC, kBias>(p, sm, tm * kWBM, tn * kWBN, 0, p.K, nullptr);
+}
+
+// The stream-K remainder (one block per SM, sk_ctas blocks): the tiles after
+// the first full_tiles are shared out as units (tile t, K-slice s), in the
+// order t * sk_slices + s, cut into sk_ctas equal contiguous ranges,
+// u0(c) = c * sk_units / sk_ctas, so that every SM does the same work.  A
+// tile a block covers whole gets the epilogue; a block's first and last
+// segments, when they cover only part of a tile, go to the workspace as raw
+// partial sums (slots 2c and 2c + 1, 128 x 256 floats each), and
+// sgemm_wide_sk_reduce adds the pieces of each such tile in block order,
+// i.e. in K order.  No block waits for another; each waits at its end for
+// the whole-tile grid (griddepcontrol.wait), so that this grid completes
+// after it and work behind it in the stream sees both.
+template <bool kTransA, bool kTransB, int kReadC, int kBias>
+__global__ void __launch_bounds__(kThreads, 1) sgemm_wide_sk_kernel(Params p) {
     extern __shared__ __align__(16) unsigned char wide_smem_raw[];
     WideSmem<kTransB>& sm = *reinterpret_cast<WideSmem<kTransB>*>(wide_smem_raw);
     const int64_t tiles_m = p.M / kWBM;
-    int64_t tm, tn;
-    if (p.sk_ctas == 0) {
-        wide_tile(blockIdx.x, tiles_m, p.tiles_n, tm, tn);
-        wide_block_tile<kTransA, kTransB, kReadC, kBias>(p, sm, tm * kWBM, tn * kWBN, 0, p.K,
-                                                         nullptr);
-        return;
-    }
     const int64_t c = blockIdx.x, S = p.sk_slices;
-    for (int64_t t = c; t < p.full_tiles; t += p.sk_ctas) {
-        wide_tile(t, tiles_m, p.tiles_n, tm, tn);
-        wide_block_tile<kTransA, kTransB, kReadC, kBias>(p, sm, tm * kWBM, tn * kWBN, 0, p.K,
-                                                         nullptr);
-    }
     const int64_t base = p.full_tiles * S;  // the first stream-K unit
     const int64_t u0 = base + c * p.sk_units / p.sk_ctas;
     const int64_t u1 = base + (c + 1) * p.sk_units / p.sk_ctas;
@@ -715,11 +729,13 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_wide_kernel(Params p) {
         const bool whole = s0 == 0 && end == (t + 1) * S;
         float* partial =
             whole ? nullptr : p.partials + (2 * c + (u == u0 ? 0 : 1)) * (kWBM * kWBN);
+        int64_t tm, tn;
         wide_tile(t, tiles_m, p.tiles_n, tm, tn);
         wide_block_tile<kTransA, kTransB, kReadC, kBias>(p, sm, tm * kWBM, tn * kWBN,
                                                          s0 * kWBK, (end - t * S) * kWBK, partial);
         u = end;
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // The block whose stream-K range holds unit u (counted from the first
@@ -827,29 +843,48 @@ WidePlan plan_wide(const GemmArgs& a, int sm_count) {
     return w;
 }
 
+// The whole-tile grid (blocks = its tiles), then, when sk is set, the
+// stream-K grid (p.sk_ctas blocks) as its programmatic dependent.
 template <bool kTransA, bool kTransB, int kReadC, int kBias>
-cudaError_t launch_wide(const Params& p, int64_t blocks, cudaStream_t s) {
-    auto kern = sgemm_wide_kernel<kTransA, kTransB, kReadC, kBias>;
+cudaError_t launch_wide(const Params& p, int64_t blocks, bool sk, cudaStream_t s, int* launches) {
     const int smem = static_cast<int>(sizeof(WideSmem<kTransB>));
+    auto kern = sgemm_wide_kernel<kTransA, kTransB, kReadC, kBias>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<static_cast<unsigned>(blocks), kThreads, smem, s>>>(p);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !sk) return e;
+    ++*launches;
+    auto sk_kern = sgemm_wide_sk_kernel<kTransA, kTransB, kReadC, kBias>;
+    e = cudaFuncSetAttribute(sk_kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.sk_ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, sk_kern, p);
 }
 
 template <bool kTransA, bool kTransB>
-cudaError_t launch_wide_layout(const Params& p, int64_t blocks, bool read_c, bool bias,
-                               cudaStream_t s) {
-    if (read_c && bias) return launch_wide<kTransA, kTransB, 1, 1>(p, blocks, s);
-    if (read_c) return launch_wide<kTransA, kTransB, 1, 0>(p, blocks, s);
-    if (bias) return launch_wide<kTransA, kTransB, 0, 1>(p, blocks, s);
-    return launch_wide<kTransA, kTransB, 0, 0>(p, blocks, s);
+cudaError_t launch_wide_layout(const Params& p, int64_t blocks, bool sk, bool read_c, bool bias,
+                               cudaStream_t s, int* launches) {
+    if (read_c && bias) return launch_wide<kTransA, kTransB, 1, 1>(p, blocks, sk, s, launches);
+    if (read_c) return launch_wide<kTransA, kTransB, 1, 0>(p, blocks, sk, s, launches);
+    if (bias) return launch_wide<kTransA, kTransB, 0, 1>(p, blocks, sk, s, launches);
+    return launch_wide<kTransA, kTransB, 0, 0>(p, blocks, sk, s, launches);
 }
 
 }  // namespace
 
 bool simt_supports(const GemmArgs& a) {
-    return a.in_dtype == DGA_F32 && a.out_dtype == DGA_F32;
+    // the kernels count K-slices (8 or 16 deep) in 32 bits
+    return a.in_dtype == DGA_F32 && a.out_dtype == DGA_F32 && a.K < kSimtMaxK;
 }
 
 namespace {
@@ -927,14 +962,14 @@ cudaError_t wide_run(const GemmArgs& a, const WidePlan& w, bool stream_k, int* l
              a.alpha_f, a.beta_f, 1, 1, 1, w.tiles_n, stream_k ? w.full_tiles : w.tiles, a.K, 1,
              stream_k ? static_cast<float*>(a.ws) : nullptr, static_cast<const float*>(a.bias),
              (w.tiles - w.full_tiles) * w.slices, w.slices, stream_k ? w.sk_ctas : 0};
-    const int64_t blocks = stream_k ? w.sk_ctas : w.tiles;
+    const int64_t blocks = stream_k ? w.full_tiles : w.tiles;
     const bool ta = a.layout_a == DGA_COL_MAJOR, tb = a.layout_b == DGA_COL_MAJOR;
     const bool rc = a.beta_f != 0.0f, bias = a.bias != nullptr;
     cudaError_t e;
-    if (ta && tb) e = launch_wide_layout<true, true>(p, blocks, rc, bias, a.stream);
-    else if (ta) e = launch_wide_layout<true, false>(p, blocks, rc, bias, a.stream);
-    else if (tb) e = launch_wide_layout<false, true>(p, blocks, rc, bias, a.stream);
-    else e = launch_wide_layout<false, false>(p, blocks, rc, bias, a.stream);
+    if (ta && tb) e = launch_wide_layout<true, true>(p, blocks, stream_k, rc, bias, a.stream, launches);
+    else if (ta) e = launch_wide_layout<true, false>(p, blocks, stream_k, rc, bias, a.stream, launches);
+    else if (tb) e = launch_wide_layout<false, true>(p, blocks, stream_k, rc, bias, a.stream, launches);
+    else e = launch_wide_layout<false, false>(p, blocks, stream_k, rc, bias, a.stream, launches);
     if (e != cudaSuccess) return e;
     ++*launches;
     if (stream_k) {

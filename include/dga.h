@@ -65,7 +65,7 @@ typedef enum { DGA_ROW_MAJOR = 0, DGA_COL_MAJOR = 1 } dga_layout;
  * arguments; the others force one family (for tests and measurement) and make
  * the call fail with DGA_ERR_PATH when that family cannot run the arguments.
  *   GENERIC  any dtype pair, any layout, alignment or leading dimension
- *   SIMT     FP32 register-tiled FFMA kernel (F32 -> F32)
+ *   SIMT     FP32 register-tiled FFMA kernel (F32 -> F32, K < 2^33)
  *   TCGEN05  5th-generation tensor cores, TMA + mbarrier pipeline, TMEM
  *            accumulators (BF16/F16 inputs, TF32 inputs; INT8 through exact
  *            bf16 encoding)

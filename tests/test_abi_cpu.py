@@ -127,6 +127,16 @@ def test_workspace_size_query(lib):
                                        100, 512, dga.PATH_TCGEN05) >= 256 * 100 * 4
 
 
+def test_fp32_path_by_k(lib):
+    # the SIMT kernels count K-slices in 32 bits: from K = 2^33 on, FP32 goes
+    # to the generic kernel (addresses far apart: nothing is dereferenced)
+    A, B, C = 0x100000000000, 0x200000000000, 0x300000000000
+    for K, want in ((4096, dga.PATH_SIMT), ((1 << 33) - 1, dga.PATH_SIMT),
+                    (1 << 33, dga.PATH_GENERIC)):
+        assert dga.dga_select_path(gen.F32, gen.F32, gen.COL_MAJOR, 2, 3, K, A, K, B, K, C,
+                                   3) == want, K
+
+
 def test_binding_layout_from_strides():
     A = torch.empty(6, 5)
     C = torch.empty(6, 7)

@@ -4,9 +4,10 @@ CPU oracle element by element.
 
 The wide kernel runs for problems of whole 128 x 256 tiles with at least one
 full wave of them (152 tiles on a GB300).  A whole number of waves runs tile
-by tile; otherwise every block takes an equal contiguous share of the (tile,
-16-deep K-slice) units, and the tiles split between blocks are summed in
-block order by a second kernel.  The shapes below reach: one exact wave,
+by tile, one launch; otherwise the whole waves run tile by tile, a second
+kernel's blocks (one per SM) each take an equal contiguous share of the
+remaining (tile, 16-deep K-slice) units, and the tiles split between blocks
+are summed in block order by a third kernel.  The shapes below reach: one exact wave,
 stream-K with a small and a large remainder of tiles, K of one and of three
 slices per tile (a share boundary can then fall only between tiles, or at a
 third of one), and a deep K; without the workspace the 128 x 128 kernel (or,
@@ -112,7 +113,7 @@ def test_wide_schedule_exact_small_integers(case, layouts):
     A, B, C, bias = _operands(la, lb, M, N, K, seed=case * 7 + la * 2 + lb, small_ints=True)
     got, launches = _run(la, lb, M, N, K, A, B, C, bias, 1.0, -1.0)
     assert (M // WBM) * (N // WBN) >= sms, name
-    assert launches == (2 if _stream_k(M, N, sms) else 1), (name, launches)
+    assert launches == (3 if _stream_k(M, N, sms) else 1), (name, launches)
     ref, _ = oracle.gemm_fp_ex(gen.F32, gen.F32, la, lb, M, N, K, 1.0, A, A.shape[1], B,
                                B.shape[1], -1.0, C, N, bias)
     assert_exact(got, ref, gen.F32, f"{name} A={la} B={lb}")
