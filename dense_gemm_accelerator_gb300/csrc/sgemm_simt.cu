@@ -716,6 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) sgemm_wide_kernel(Params p) {
 // after it and work behind it in the stream sees both.
 template <bool kTransA, bool kTransB, int kReadC, int kBias>
 __global__ void __launch_bounds__(kThreads, 1) sgemm_wide_sk_kernel(Params p) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // the reduce
     extern __shared__ __align__(16) unsigned char wide_smem_raw[];
     WideSmem<kTransB>& sm = *reinterpret_cast<WideSmem<kTransB>*>(wide_smem_raw);
     const int64_t tiles_m = p.M / kWBM;
@@ -748,11 +749,20 @@ __device__ __forceinline__ int64_t sk_owner(const Params& p, int64_t u) {
 // the epilogue (float4 everywhere: the wide path runs only on aligned
 // shapes).  Work item b = 1 .. sk_ctas - 1 is the range boundary between
 // blocks b - 1 and b; the first boundary inside a tile handles that tile.
-// kReduceSlabs blocks share a tile, 8 rows each, two float4 per thread, so
-// that enough loads are in flight to keep this short step bandwidth-bound.
+// kReduceSlabs blocks share a tile, 8 rows each, two float4 per thread.  The
+// tile's pieces (the workspace slots of the blocks whose ranges meet it, in
+// block order) are listed once per block; with at most kReducePieces of them
+// every thread issues all its loads before adding them up, in block order
+// (K order).  The block waits for the stream-K grid (griddepcontrol.wait)
+// only after that set-up, so when it is launched as that grid's programmatic
+// dependent its start overlaps the grid's end.
 constexpr int kReduceSlabs = kWBM / 8;
+constexpr int kReducePieces = 8;
 
 __global__ void __launch_bounds__(kThreads) sgemm_wide_sk_reduce(Params p) {
+    __shared__ int64_t s_slot[kReducePieces];
+    __shared__ int s_pieces;  // < 0: the tile has more pieces than fit the list
+    __shared__ int64_t s_first, s_last;
     const int64_t b = blockIdx.x / kReduceSlabs + 1;
     const int slab = static_cast<int>(blockIdx.x % kReduceSlabs);
     const int64_t S = p.sk_slices;
@@ -762,7 +772,28 @@ __global__ void __launch_bounds__(kThreads) sgemm_wide_sk_reduce(Params p) {
     if (ub - T * S == 0) return;  // the boundary falls between tiles: nothing split here
     const int64_t prev = (b - 1) * p.sk_units / p.sk_ctas;
     if (b > 1 && prev / S == T && prev - T * S != 0) return;  // an earlier boundary owns T
-    const int64_t c_first = sk_owner(p, T * S), c_last = sk_owner(p, min((T + 1) * S, p.sk_units) - 1);
+    if (threadIdx.x == 0) {
+        const int64_t c_first = sk_owner(p, T * S);
+        const int64_t c_last = sk_owner(p, min((T + 1) * S, p.sk_units) - 1);
+        int n = 0;
+        for (int64_t q = c_first; q <= c_last; ++q) {
+            // blocks with an empty range (fewer units than blocks) wrote nothing
+            const int64_t q0 = q * p.sk_units / p.sk_ctas;
+            if ((q + 1) * p.sk_units / p.sk_ctas == q0) continue;
+            if (n == kReducePieces) {
+                n = -1;
+                break;
+            }
+            // block q's piece of T is its first segment if its range starts in T
+            s_slot[n++] = 2 * q + (q0 / S == T ? 0 : 1);
+        }
+        s_pieces = n;
+        s_first = c_first;
+        s_last = c_last;
+    }
+    __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n = s_pieces;
     int64_t tm, tn;
     wide_tile(p.full_tiles + T, p.M / kWBM, p.tiles_n, tm, tn);
     const int64_t row0 = tm * kWBM, col0 = tn * kWBN;
@@ -770,24 +801,40 @@ __global__ void __launch_bounds__(kThreads) sgemm_wide_sk_reduce(Params p) {
     for (int h = 0; h < 2; ++h) {
         const int e = slab * (8 * kWBN / 4) + h * kThreads + threadIdx.x;
         const int r = e / (kWBN / 4), c = (e % (kWBN / 4)) * 4;
-        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-        bool first = true;
-        for (int64_t q = c_first; q <= c_last; ++q) {
-            // blocks with an empty range (fewer units than blocks) wrote nothing
-            const int64_t q0 = q * p.sk_units / p.sk_ctas;
-            if ((q + 1) * p.sk_units / p.sk_ctas == q0) continue;
-            // block q's piece of T is its first segment if its range starts in T
-            const int64_t slot = 2 * q + (q0 / S == T ? 0 : 1);
-            const float4 v =
-                *reinterpret_cast<const float4*>(p.partials + slot * (kWBM * kWBN) + r * kWBN + c);
-            if (first) {
-                sum = v;
-                first = false;
-            } else {
-                sum.x += v.x;
-                sum.y += v.y;
-                sum.z += v.z;
-                sum.w += v.w;
+        const float* at = p.partials + r * kWBN + c;
+        float4 sum;
+        if (n > 0) {
+            float4 v[kReducePieces];
+#pragma unroll
+            for (int i = 0; i < kReducePieces; ++i)
+                if (i < n) v[i] = *reinterpret_cast<const float4*>(at + s_slot[i] * (kWBM * kWBN));
+            sum = v[0];
+#pragma unroll
+            for (int i = 1; i < kReducePieces; ++i) {
+                if (i < n) {
+                    sum.x += v[i].x;
+                    sum.y += v[i].y;
+                    sum.z += v[i].z;
+                    sum.w += v[i].w;
+                }
+            }
+        } else {  // a long list: the same sum, one piece at a time
+            sum = make_float4(0.f, 0.f, 0.f, 0.f);
+            bool first = true;
+            for (int64_t q = s_first; q <= s_last; ++q) {
+                const int64_t q0 = q * p.sk_units / p.sk_ctas;
+                if ((q + 1) * p.sk_units / p.sk_ctas == q0) continue;
+                const int64_t slot = 2 * q + (q0 / S == T ? 0 : 1);
+                const float4 w = *reinterpret_cast<const float4*>(at + slot * (kWBM * kWBN));
+                if (first) {
+                    sum = w;
+                    first = false;
+                } else {
+                    sum.x += w.x;
+                    sum.y += w.y;
+                    sum.z += w.z;
+                    sum.w += w.w;
+                }
             }
         }
         float4* dst = reinterpret_cast<float4*>(p.C + (row0 + r) * p.ldc + col0 + c);
@@ -973,9 +1020,17 @@ cudaError_t wide_run(const GemmArgs& a, const WidePlan& w, bool stream_k, int* l
     if (e != cudaSuccess) return e;
     ++*launches;
     if (stream_k) {
-        sgemm_wide_sk_reduce<<<static_cast<unsigned>((w.sk_ctas - 1) * kReduceSlabs), kThreads, 0,
-                               a.stream>>>(p);
-        e = cudaGetLastError();
+        // the reduce as a programmatic dependent of the stream-K grid
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(static_cast<unsigned>((w.sk_ctas - 1) * kReduceSlabs));
+        cfg.blockDim = dim3(kThreads);
+        cfg.stream = a.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, sgemm_wide_sk_reduce, p);
         if (e != cudaSuccess) return e;
         ++*launches;
     }
