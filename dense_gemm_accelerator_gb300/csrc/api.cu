@@ -174,10 +174,11 @@ int sm_count_or_default() {
     return 152;
 }
 
-// Workspace the call would use if given: required bytes, or for the SIMT
-// path the optional bytes of its split last wave.
+// Workspace the call would use if given: required bytes, plus for the SIMT
+// and tensor-core paths the optional bytes of their split last waves.
 size_t workspace_wanted(int path, const GemmArgs& g) {
     if (path == DGA_PATH_SIMT) return simt_workspace_size(g, sm_count_or_default());
+    if (path == DGA_PATH_TCGEN05) return tc_workspace_wanted(g, sm_count_or_default());
     return workspace_required(path, g);
 }
 

@@ -93,6 +93,8 @@ cudaError_t naive_probe_launch(int64_t M, int64_t N, int64_t K, const float* A, 
 
 bool tc_supports(const GemmArgs& a);
 size_t tc_workspace_size(const GemmArgs& a);
+// tc_workspace_size plus what the split last wave can use (optional)
+size_t tc_workspace_wanted(const GemmArgs& a, int sm_count);
 cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);
 // Launches a kernel whose bounded wait runs out after limit_ns (self-test).
 cudaError_t tc_selftest_wait(uint64_t limit_ns, cudaStream_t stream);

@@ -103,6 +103,13 @@ struct TcParams {
     uint32_t a_mn, b_mn;  // operand stored MN-major (column-major A / row-major B)
     uint32_t tiles_m, tiles_n, num_tiles, num_kb;
     uint32_t group_m;  // tile rows per raster group
+    // CTA-pair kernel, floating point: the tiles after the first full_tiles
+    // (the last, part-filled wave) are each cut along K into `splits` parts,
+    // one work unit each, whose raw fp32 sums go to `partials` (256 x 256
+    // floats per unit) for tc_split_reduce_kernel; num_units = full_tiles +
+    // (num_tiles - full_tiles) * splits.  splits == 1: every unit is a tile.
+    uint32_t full_tiles, splits, num_units;
+    float* partials;
 };
 
 // Shared-memory plan (dynamic, 1024-byte aligned): the stage ring, the
@@ -135,6 +142,25 @@ __device__ __forceinline__ void tile_coords(uint32_t t, const TcParams& p, uint3
     const uint32_t r = t % group_size;
     tm = first_m + r % gm;
     tn = r / gm;
+}
+
+// Work unit u of the CTA-pair kernel: its tile, its k-blocks [kb_begin,
+// kb_end) and, for a part of a split tile, its partial-sum slot (else -1).
+__device__ __forceinline__ void unit_coords(uint32_t u, const TcParams& p, uint32_t& tm,
+                                            uint32_t& tn, uint32_t& kb_begin, uint32_t& kb_end,
+                                            int32_t& slot) {
+    uint32_t t = u;
+    kb_begin = 0;
+    kb_end = p.num_kb;
+    slot = -1;
+    if (u >= p.full_tiles) {
+        const uint32_t v = u - p.full_tiles, part = v % p.splits;
+        t = p.full_tiles + v / p.splits;
+        kb_begin = part * p.num_kb / p.splits;
+        kb_end = (part + 1) * p.num_kb / p.splits;
+        slot = p.splits > 1 ? static_cast<int32_t>(v) : -1;
+    }
+    tile_coords(t, p, tm, tn);
 }
 
 __device__ __forceinline__ void record_failure(int role, volatile int* abort_flag) {
@@ -464,6 +490,22 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
 constexpr int kPairStages = 6;
 constexpr int kPairBN = 256;
 
+// A 32 x 32 block of raw fp32 sums into a split tile's partial slot (256 x
+// 256 floats, row-major, tile-relative; rows and columns past the matrix are
+// written too and never read), transposed through the staging square like
+// the stores above.
+__device__ __forceinline__ void store_block_partial(float* slot_base, uint32_t* stage, int lane,
+                                                    int row_base, int col_base,
+                                                    const uint32_t (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = v[j];
+    __syncwarp();
+#pragma unroll 4
+    for (int i = 0; i < 32; ++i)
+        slot_base[(row_base + i) * kPairBN + col_base + lane] = __uint_as_float(stage[i * 33 + lane]);
+    __syncwarp();
+}
+
 // kSquares: epilogue staging squares, 4 for floating point (one per epilogue
 // warp), 8 for INT8 (16 epilogue warps store in two rounds).
 template <int kSquares>
@@ -543,12 +585,13 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (uint32_t t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
-                uint32_t tm, tn;
-                tile_coords(t, p, tm, tn);
+            for (uint32_t u = cluster_id; ok && u < p.num_units; u += n_clusters) {
+                uint32_t tm, tn, kb_begin, kb_end;
+                int32_t slot;
+                unit_coords(u, p, tm, tn, kb_begin, kb_end, slot);
                 const int32_t a_row = static_cast<int32_t>(tm * 256 + rank * 128);
                 const int32_t b_row = static_cast<int32_t>(tn * kPairBN + rank * (kPairBN / 2));
-                for (uint32_t kb = 0; kb < p.num_kb; ++kb) {
+                for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
                     if (!mbar_wait_bounded<true>(&empty[stage], phase ^ 1, abort_flag,
                                                  kWaitLimitNs)) {
                         record_failure(kRoleProducer, abort_flag);
@@ -590,8 +633,12 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
             // INT8: the K loop of a tile is cut into exact 1024-deep chunks, each
             // in its own accumulator (see the single-CTA kernel); otherwise one
             // chunk spans the whole K loop
-            const uint32_t n_chunks = kI8 ? (p.num_kb + kI8ChunkBlocks - 1) / kI8ChunkBlocks : 1;
-            for (uint32_t t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
+            for (uint32_t u = cluster_id; ok && u < p.num_units; u += n_clusters) {
+                uint32_t tm, tn, kb_first, kb_last;
+                int32_t slot;
+                unit_coords(u, p, tm, tn, kb_first, kb_last, slot);
+                const uint32_t n_chunks =
+                    kI8 ? (kb_last - kb_first + kI8ChunkBlocks - 1) / kI8ChunkBlocks : 1;
                 for (uint32_t ch = 0; ok && ch < n_chunks; ++ch) {
                     if (!mbar_wait_bounded<true>(&acc_empty[acc], acc_phase ^ 1, abort_flag,
                                                  kWaitLimitNs)) {
@@ -601,8 +648,8 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + acc * kPairBN;
-                    const uint32_t kb_begin = kI8 ? ch * kI8ChunkBlocks : 0;
-                    const uint32_t kb_end = kI8 ? min(p.num_kb, kb_begin + kI8ChunkBlocks) : p.num_kb;
+                    const uint32_t kb_begin = kI8 ? kb_first + ch * kI8ChunkBlocks : kb_first;
+                    const uint32_t kb_end = kI8 ? min(kb_last, kb_begin + kI8ChunkBlocks) : kb_last;
                     for (uint32_t kb = kb_begin; kb < kb_end; ++kb) {
                         if (!mbar_wait_bounded<true>(&full[stage], phase, abort_flag, kWaitLimitNs)) {
                             record_failure(kRoleMma, abort_flag);
@@ -645,9 +692,13 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
         constexpr int kColsPerWarp = kI8 ? kPairBN / 4 : kPairBN;
         uint32_t acc = 0, acc_phase = 0;
         bool ok = true;
-        for (uint32_t t = cluster_id; ok && t < p.num_tiles; t += n_clusters) {
-            uint32_t tm, tn;
-            tile_coords(t, p, tm, tn);
+        for (uint32_t u = cluster_id; ok && u < p.num_units; u += n_clusters) {
+            // INT8 never splits (each unit a whole tile): its 64 running sums
+            // leave no registers for the unit's k-range
+            uint32_t tm, tn, kb_first = 0, kb_last = p.num_kb;
+            int32_t slot = -1;
+            if constexpr (kI8) tile_coords(u, p, tm, tn);
+            else unit_coords(u, p, tm, tn, kb_first, kb_last, slot);
             const int64_t row_base = static_cast<int64_t>(tm) * 256 + rank * 128 + quarter * 32;
             const int64_t col0 = static_cast<int64_t>(tn) * kPairBN + col_group * kColsPerWarp;
             if constexpr (!kI8) {
@@ -661,7 +712,12 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                     uint32_t r[32];
                     tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + c * 32, r);
                     tmem_ld_wait();
-                    store_block_staged<TOut>(p, stage, lane, row_base, col0 + c * 32, r);
+                    if (slot < 0)
+                        store_block_staged<TOut>(p, stage, lane, row_base, col0 + c * 32, r);
+                    else
+                        store_block_partial(p.partials + static_cast<int64_t>(slot) * (256 * kPairBN),
+                                            stage, lane, static_cast<int>(rank * 128 + quarter * 32),
+                                            c * 32, r);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -726,6 +782,51 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
         __syncwarp();
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+// ---- the split last wave's reduce ------------------------------------------------
+//
+// Adds the K-parts of each split tile (full_tiles + j) in part order, i.e. in
+// K order, so that the result repeats bit for bit, and applies the epilogue
+// as store_block_staged does (alpha, beta -- C is read only when beta != 0 --
+// the bias row, the edge masks, the output type).  One block per 8 rows of a
+// tile, a warp per row, lane l taking columns l, l + 32, ..., l + 224: every
+// load and store instruction covers 32 consecutive elements.  Launched as a
+// programmatic dependent of the GEMM: it reads the partial sums only after
+// griddepcontrol.wait.
+template <typename TOut>
+__global__ void __launch_bounds__(256) tc_split_reduce_kernel(TcParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const uint32_t j = blockIdx.x / 32;
+    const int r = static_cast<int>(blockIdx.x % 32) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    uint32_t tm, tn;
+    tile_coords(p.full_tiles + j, p, tm, tn);
+    const int64_t row = static_cast<int64_t>(tm) * 256 + r;
+    if (row >= p.M) return;
+    constexpr int64_t kSlot = 256 * kPairBN;
+    const float* base = p.partials + static_cast<int64_t>(j) * p.splits * kSlot + r * kPairBN + lane;
+    float sum[kPairBN / 32];
+#pragma unroll
+    for (int q = 0; q < kPairBN / 32; ++q) sum[q] = base[q * 32];
+    for (uint32_t part = 1; part < p.splits; ++part) {
+        const float* b = base + part * kSlot;
+        float v[kPairBN / 32];
+#pragma unroll
+        for (int q = 0; q < kPairBN / 32; ++q) v[q] = b[q * 32];
+#pragma unroll
+        for (int q = 0; q < kPairBN / 32; ++q) sum[q] += v[q];
+    }
+#pragma unroll
+    for (int q = 0; q < kPairBN / 32; ++q) {
+        const int64_t col = static_cast<int64_t>(tn) * kPairBN + q * 32 + lane;
+        if (col < p.N) {
+            TOut* dst = static_cast<TOut*>(p.C) + row * p.ldc + col;
+            const float old = p.beta != 0.0f ? OutT<TOut>::load(dst) : 0.0f;
+            const float bv = p.bias != nullptr ? OutT<TOut>::load(static_cast<const TOut*>(p.bias) + col) : 0.0f;
+            OutT<TOut>::store(dst, axpby(p.alpha, sum[q], p.beta, old) + bv);
+        }
     }
 }
 
@@ -1317,9 +1418,21 @@ int max_pair_clusters(Kern kern, int smem, int threads, const DeviceInfo& dev) {
     return n;
 }
 
+// The split of the last wave: at most kMaxSplits parts per tile, none
+// shallower than kMinSplitKb k-blocks, 256 x 256 floats of workspace per part.
+constexpr uint32_t kMaxSplits = 4;
+constexpr uint32_t kMinSplitKb = 8;
+constexpr size_t kSplitSlotBytes = size_t{256} * kPairBN * sizeof(float);
+
+// The CTA-pair GEMM, and for floating point, when split_ws holds enough and
+// the last wave is at most half full, the split of that wave's tiles along K
+// into work units of their own (one round of parts instead of a round of
+// whole tiles that leaves clusters idle) and the reduce that adds the parts
+// (*extra_launches is incremented for it).
 template <uint32_t kFmt, bool kI8, typename TOut>
-cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p,
-                               const DeviceInfo& dev, cudaStream_t s, bool pdl) {
+cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p0,
+                               const DeviceInfo& dev, cudaStream_t s, bool pdl, float* split_ws,
+                               size_t split_bytes, int* extra_launches) {
     auto kern = tc_gemm_pair_kernel<kFmt, kI8, TOut>;
     const int smem = static_cast<int>(PairSmem<kI8 ? 8 : 4>::kLaunchBytes);
     const int threads = kI8 ? 576 : 192;
@@ -1327,7 +1440,25 @@ cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, con
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int clusters = std::min<int64_t>(
-        p.num_tiles, max_pair_clusters<kFmt, kI8, TOut>(kern, smem, threads, dev));
+        p0.num_tiles, max_pair_clusters<kFmt, kI8, TOut>(kern, smem, threads, dev));
+    TcParams p = p0;
+    p.full_tiles = p.num_tiles;
+    p.splits = 1;
+    p.num_units = p.num_tiles;
+    p.partials = nullptr;
+    const uint32_t nc = static_cast<uint32_t>(std::max(clusters, 1));
+    if (!kI8 && split_ws != nullptr && p.num_tiles > nc) {
+        const uint32_t rem = p.num_tiles % nc;
+        if (rem > 0 && 2 * rem <= nc) {
+            const uint32_t sp = std::min(std::min(nc / rem, kMaxSplits), p.num_kb / kMinSplitKb);
+            if (sp >= 2 && static_cast<size_t>(rem) * sp * kSplitSlotBytes <= split_bytes) {
+                p.full_tiles = p.num_tiles - rem;
+                p.splits = sp;
+                p.num_units = p.full_tiles + rem * sp;
+                p.partials = split_ws;
+            }
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * std::max(clusters, 1)));
     cfg.blockDim = dim3(threads);
@@ -1342,7 +1473,22 @@ cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, con
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;  // see launch_kernel
-    return cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, p);
+    if (e != cudaSuccess || p.splits == 1) return e;
+    if constexpr (!kI8) {
+        cudaLaunchConfig_t rc = {};
+        rc.gridDim = dim3((p.num_tiles - p.full_tiles) * 32);
+        rc.blockDim = dim3(256);
+        rc.stream = s;
+        cudaLaunchAttribute ra[1];
+        ra[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        ra[0].val.programmaticStreamSerializationAllowed = 1;
+        rc.attrs = ra;
+        rc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&rc, tc_split_reduce_kernel<TOut>, p);
+        if (e == cudaSuccess) ++*extra_launches;
+    }
+    return e;
 }
 
 // One operand's 16-bit repack job: dst (rows x ld_dst) from the source's
@@ -1454,6 +1600,19 @@ size_t tc_workspace_size(const GemmArgs& a) {
     return pl.a_bytes + pl.b_bytes;
 }
 
+size_t tc_workspace_wanted(const GemmArgs& a, int sm_count) {
+    const size_t need = tc_workspace_size(a);
+    // the split last wave (CTA-pair kernel, floating point): at most one part
+    // per cluster, sm_count / 2 clusters; only for more tiles than clusters
+    // and K deep enough for two parts
+    if (a.in_dtype == DGA_I8 || a.M <= BM || sm_count < 2) return need;
+    const int64_t tiles = ((a.M + 255) / 256) * ((a.N + kPairBN - 1) / kPairBN);
+    const int64_t kb = (a.K + k_per_stage(a.in_dtype == DGA_TF32 ? kFmtTF32 : kFmtBF16) - 1) /
+                       k_per_stage(a.in_dtype == DGA_TF32 ? kFmtTF32 : kFmtBF16);
+    if (tiles <= sm_count / 2 || kb < 2 * static_cast<int64_t>(kMinSplitKb)) return need;
+    return need + static_cast<size_t>(sm_count / 2) * kSplitSlotBytes;
+}
+
 cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     const bool i8 = a.in_dtype == DGA_I8;
     const bool tf32 = a.in_dtype == DGA_TF32;
@@ -1555,20 +1714,33 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.num_kb = static_cast<uint32_t>((a.K + k_per_stage(fmt) - 1) / k_per_stage(fmt));
     p.group_m = raster_group_rows(a.K, p.tiles_m, tile_m);
+    p.full_tiles = p.num_tiles;
+    p.splits = 1;
+    p.num_units = p.num_tiles;
 
-    if (i8 && pair) e = launch_pair_kernel<kFmtBF16, true, int32_t>(ma, mb, p, dev, a.stream, pdl);
+    // workspace past the repacked operands: room for the split last wave
+    float* split_ws = nullptr;
+    size_t split_bytes = 0;
+    const size_t used = pl.a_bytes + pl.b_bytes;  // multiples of 256 bytes
+    if (a.ws != nullptr && a.ws_bytes > used && aligned(static_cast<uint8_t*>(a.ws) + used, 16)) {
+        split_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + used);
+        split_bytes = a.ws_bytes - used;
+    }
+    int extra = 0;  // the split's reduce
+
+    if (i8 && pair) e = launch_pair_kernel<kFmtBF16, true, int32_t>(ma, mb, p, dev, a.stream, pdl, split_ws, split_bytes, &extra);
     else if (i8) e = launch_kernel<kFmtBF16, true, kBnI8, int32_t>(ma, mb, p, dev, a.stream, pdl);
-    else if (tf32 && pair) e = launch_pair_kernel<kFmtTF32, false, float>(ma, mb, p, dev, a.stream, pdl);
+    else if (tf32 && pair) e = launch_pair_kernel<kFmtTF32, false, float>(ma, mb, p, dev, a.stream, pdl, split_ws, split_bytes, &extra);
     else if (tf32) e = launch_kernel<kFmtTF32, false, kBnFloat, float>(ma, mb, p, dev, a.stream, pdl);
-    else if (pair && bf16 && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtBF16, false, float>(ma, mb, p, dev, a.stream, pdl);
-    else if (pair && bf16) e = launch_pair_kernel<kFmtBF16, false, __nv_bfloat16>(ma, mb, p, dev, a.stream, pdl);
-    else if (pair && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtF16, false, float>(ma, mb, p, dev, a.stream, pdl);
-    else if (pair) e = launch_pair_kernel<kFmtF16, false, __half>(ma, mb, p, dev, a.stream, pdl);
+    else if (pair && bf16 && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtBF16, false, float>(ma, mb, p, dev, a.stream, pdl, split_ws, split_bytes, &extra);
+    else if (pair && bf16) e = launch_pair_kernel<kFmtBF16, false, __nv_bfloat16>(ma, mb, p, dev, a.stream, pdl, split_ws, split_bytes, &extra);
+    else if (pair && a.out_dtype == DGA_F32) e = launch_pair_kernel<kFmtF16, false, float>(ma, mb, p, dev, a.stream, pdl, split_ws, split_bytes, &extra);
+    else if (pair) e = launch_pair_kernel<kFmtF16, false, __half>(ma, mb, p, dev, a.stream, pdl, split_ws, split_bytes, &extra);
     else if (bf16 && a.out_dtype == DGA_F32) e = launch_kernel<kFmtBF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream, pdl);
     else if (bf16) e = launch_kernel<kFmtBF16, false, kBnFloat, __nv_bfloat16>(ma, mb, p, dev, a.stream, pdl);
     else if (a.out_dtype == DGA_F32) e = launch_kernel<kFmtF16, false, kBnFloat, float>(ma, mb, p, dev, a.stream, pdl);
     else e = launch_kernel<kFmtF16, false, kBnFloat, __half>(ma, mb, p, dev, a.stream, pdl);
-    if (e == cudaSuccess) ++*launches;
+    if (e == cudaSuccess) *launches += 1 + extra;
     return e;
 }
 

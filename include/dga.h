@@ -110,14 +110,17 @@ typedef enum {
  *   C, ldc               device pointer, C(i, j) = C[i*ldc + j], ldc >= max(1, N)
  *   workspace            device scratch of at least workspace_bytes, or NULL
  *   workspace_bytes      bytes at `workspace`.  The tensor-core path needs
- *                        dga_gemm_workspace_size() bytes when it repacks
- *                        operands (INT8 inputs; TF32 inputs with a row-major
- *                        B; leading dimensions TMA cannot express) and fails with
- *                        DGA_ERR_WORKSPACE without them.  The FP32 SIMT path
- *                        uses workspace only if given enough: then the tiles
- *                        of its last, partial wave are split along K (faster
- *                        for shapes whose tile count is not a multiple of the
- *                        resident blocks); with less it runs whole tiles.
+ *                        the bytes of its operand repacks (INT8 inputs; TF32
+ *                        inputs with a row-major B; leading dimensions TMA
+ *                        cannot express) and fails with DGA_ERR_WORKSPACE
+ *                        without them.  dga_gemm_workspace_size() reports
+ *                        those plus optional bytes: given them, the FP32 SIMT
+ *                        path and, for floating point, the tensor-core CTA-pair
+ *                        kernel split the tiles of a last, partly filled wave
+ *                        along K (faster for tile counts that are not a
+ *                        multiple of what runs at once; the parts are added in
+ *                        a fixed order by a further launch, so results repeat
+ *                        bit for bit); with less they run whole tiles.
  *   stream               CUDA stream the kernels are enqueued on
  *
  * M == 0 or N == 0 returns DGA_OK and touches no memory.  Returns a status

@@ -101,10 +101,17 @@ def test_workspace_size_query(lib):
         for layout, ldb in ((gen.ROW_MAJOR, N + 3), (gen.COL_MAJOR, K + 5)):
             assert dga.dga_gemm_workspace_size(gen.I8, gen.I32, layout, M, N, K, K, ldb, N,
                                                dga.PATH_TCGEN05) == want, (M, N, K, layout)
-    # column-major bf16 with aligned leading dimensions needs nothing
+    # column-major bf16 with aligned leading dimensions needs nothing; the
+    # query reports the optional room for the split last wave of the CTA-pair
+    # kernel (one 256 x 256 fp32 slot per pair: 76 on the default 152 SMs),
+    # nothing for a single wave or a K too shallow to split
     w = W["bf16_8192"]
     assert dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
-                                       w.K, w.N, dga.PATH_TCGEN05) == 0
+                                       w.K, w.N, dga.PATH_TCGEN05) == 76 * 256 * 256 * 4
+    assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.COL_MAJOR, 512, 512, 8192, 8192,
+                                       8192, 512, dga.PATH_TCGEN05) == 0
+    assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.COL_MAJOR, 8192, 8192, 512, 512,
+                                       512, 8192, dga.PATH_TCGEN05) == 0
     # row-major B is read in place (MN-major) unless TMA cannot express its
     # leading dimension; then it is copied row by row (K rows of N, padded to
     # 8 elements) and still read MN-major
@@ -116,11 +123,12 @@ def test_workspace_size_query(lib):
                                        513, 510, dga.PATH_TCGEN05) == 100 * 512 * 2
     assert dga.dga_gemm_workspace_size(gen.F32, gen.F32, gen.ROW_MAJOR, 64, 64, 64, 64, 64, 64,
                                        dga.PATH_SIMT) == 0
-    # TF32 reads K-major only: column-major B in place, a row-major B is
-    # transposed into the workspace as fp32 (4 bytes x N x K4)
+    # TF32 reads K-major only: column-major B in place (only the split last
+    # wave's optional slots), a row-major B is transposed into the workspace
+    # as fp32 (4 bytes x N x K4)
     w = W["tf32_8192"]
     assert dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
-                                       w.K, w.N, dga.PATH_AUTO) == 0
+                                       w.K, w.N, dga.PATH_TCGEN05) == 76 * 256 * 256 * 4
     assert dga.dga_gemm_workspace_size(gen.TF32, gen.F32, gen.ROW_MAJOR, 256, 512, 100, 100,
                                        512, 512, dga.PATH_TCGEN05) >= 512 * 100 * 4
     assert dga.dga_gemm_workspace_size(gen.TF32, gen.F32, gen.COL_MAJOR, 256, 512, 100, 102,

@@ -1,0 +1,194 @@
+"""GPU parity of the tensor-core CTA-pair kernel's split last wave, through
+the C ABI, against the CPU oracle element by element.
+
+A floating-point problem of more 256 x 256 tiles than there are CTA pairs
+(76 on a GB300) whose last wave is at most half full runs that wave's tiles
+cut along K into parts (as many as fit one round of the pairs, at most 4,
+none shallower than 8 k-blocks) when the workspace the size query reports is
+given: the parts' raw fp32 sums go to the workspace and a second launch adds
+them in part (K) order and applies alpha, beta, the bias row and the output
+type.  The shapes below split 2 and 4 ways, put the remainder at exactly
+half a wave (split) and one tile past it (not split), and leave ragged edges
+in both directions; with small-integer inputs every partial sum is exact, so
+the result must equal the oracle's exactly rounded once to the output type.
+The GEMM is the BLAS update of "AI Programming: Matrix Product", section
+"Dense matrix multiplication", with the bias row of its "Fully-connected
+layer" section.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import dense_gemm_accelerator_gb300 as dga
+import oracle
+from dense_gemm_accelerator_gb300 import inputs as gen
+from tests.helpers import assert_close, assert_exact
+
+pytestmark = pytest.mark.gpu
+
+T = dga.PATH_TCGEN05
+
+
+def _clusters():
+    return torch.cuda.get_device_properties(0).multi_processor_count // 2
+
+
+def _tiles(M, N):
+    return ((M + 255) // 256) * ((N + 255) // 256)
+
+
+def _splits(M, N, K, in_dtype):
+    """The split the rule gives (1: none) for a device with _clusters() pairs."""
+    nc = _clusters()
+    tiles = _tiles(M, N)
+    if tiles <= nc:
+        return 1
+    rem = tiles % nc
+    if rem == 0 or 2 * rem > nc:
+        return 1
+    kb = (K + (31 if in_dtype == gen.TF32 else 63)) // (32 if in_dtype == gen.TF32 else 64)
+    return max(1, min(nc // rem, 4, kb // 8))
+
+
+def _operands(in_dtype, out_dtype, M, N, K, seed, small_ints):
+    g = torch.Generator().manual_seed(seed)
+
+    def draw(shape, dt):
+        if small_ints:
+            return gen.small_int_matrix(shape, dt, g, -8, 8)
+        return gen.random_matrix(shape, dt, g)
+    A = draw((M, K), in_dtype)
+    B = draw((N, K), in_dtype)  # column-major B (N x K), the layout of a Linear weight
+    C = draw((M, N), out_dtype)
+    bias = draw((1, N), out_dtype).reshape(N)
+    return A, B, C, bias
+
+
+def _run(in_dtype, out_dtype, M, N, K, A, B, C, bias, alpha, beta, workspace=True):
+    dev = torch.device("cuda")
+    Ad, Bd, Cd = A.to(dev), B.to(dev), C.to(dev)
+    bd = bias.to(dev) if bias is not None else None
+    ws_bytes = dga.dga_gemm_general_workspace_size(in_dtype, out_dtype, gen.ROW_MAJOR,
+                                                   gen.COL_MAJOR, M, N, K, K, K, N, T)
+    if not workspace:
+        ws_bytes = 0
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    al, be = dga.scalar(alpha, in_dtype), dga.scalar(beta, in_dtype)
+    stream = torch.cuda.current_stream().cuda_stream
+    st = dga.dga_gemm_general(in_dtype, out_dtype, gen.ROW_MAJOR, gen.COL_MAJOR, M, N, K,
+                              ctypes.byref(al), Ad.data_ptr(), K, Bd.data_ptr(), K,
+                              ctypes.byref(be), Cd.data_ptr(), N,
+                              bd.data_ptr() if bd is not None else None,
+                              ws.data_ptr() if ws_bytes else None, ws_bytes, T, stream)
+    assert st == dga.OK, dga.dga_status_string(st)
+    assert dga.dga_sync_status(stream) == dga.OK
+    assert dga.dga_last_path() == T
+    return Cd.cpu(), dga.dga_last_launch_count()
+
+
+def _shapes(nc):
+    """(name, M, N, K): 8 tile columns, the tile rows giving one wave plus a
+    remainder of 4 tiles, exactly half a wave, and one tile past half."""
+    rows_one = nc // 8  # 9 full tile rows of 8 on a GB300 (72 tiles) ...
+    return [
+        # 80 tiles on 76 pairs: remainder 4, K = 1024 (16 k-blocks): 2 parts
+        ("rem4_two_parts", 256 * 10, 256 * 8, 1024),
+        # the same with K = 2048 (32 k-blocks): 4 parts
+        ("rem4_four_parts", 256 * 10, 256 * 8, 2048),
+        # ragged edges on the split tiles (10 x 8 tiles, the last row and column
+        # short) and a partial last k-block (K = 1096: rows of 2192 or 4384
+        # bytes, which TMA reads in place)
+        ("ragged", 256 * 9 + 100, 256 * 7 + 70, 1096),
+        # remainder exactly half a wave: 76 + 38 = 114 tiles (19 x 6)
+        ("half_wave", 256 * 19, 256 * 6, 1024),
+        # one tile past half: 76 + 39 = 115 tiles (23 x 5), not split
+        ("past_half", 256 * 23, 256 * 5, 1024),
+    ] if rows_one * 8 <= nc else []
+
+
+CASES = [(gen.BF16, gen.F32), (gen.BF16, gen.BF16), (gen.F16, gen.F32), (gen.F16, gen.F16),
+         (gen.TF32, gen.F32)]
+
+
+@pytest.mark.parametrize("case", range(5))
+@pytest.mark.parametrize("dtypes", CASES, ids=["bf16_f32", "bf16_bf16", "f16_f32", "f16_f16",
+                                                "tf32_f32"])
+def test_split_last_wave_exact(case, dtypes):
+    # entries in [-8, 8], K <= 2048: every partial and total sum is an integer
+    # below 2^24 in magnitude, exact in fp32 in any order; alpha = 1, beta =
+    # -1 and an integer C and bias keep the epilogue exact before the single
+    # rounding to the output type
+    nc = _clusters()
+    shapes = _shapes(nc)
+    if not shapes:
+        pytest.skip("the shapes assume a device with 8k CTA pairs")
+    name, M, N, K = shapes[case]
+    in_dtype, out_dtype = dtypes
+    A, B, C, bias = _operands(in_dtype, out_dtype, M, N, K, seed=case * 5 + CASES.index(dtypes),
+                              small_ints=True)
+    got, launches = _run(in_dtype, out_dtype, M, N, K, A, B, C, bias, 1.0, -1.0)
+    sp = _splits(M, N, K, in_dtype)
+    assert launches == (2 if sp > 1 else 1), (name, launches, sp)
+    if name != "past_half":
+        assert sp > 1, name
+    ref, _ = oracle.gemm_fp_ex(in_dtype, out_dtype, gen.ROW_MAJOR, gen.COL_MAJOR, M, N, K, 1.0,
+                               A, K, B, K, -1.0, C, N, bias)
+    assert_exact(got, ref, out_dtype, f"{name} {in_dtype}->{out_dtype}")
+    # without the workspace: whole tiles, one launch, the same exact result
+    got0, launches0 = _run(in_dtype, out_dtype, M, N, K, A, B, C, bias, 1.0, -1.0,
+                           workspace=False)
+    assert launches0 == 1
+    assert torch.equal(got0, got), name
+
+
+@pytest.mark.parametrize("dtypes", CASES, ids=["bf16_f32", "bf16_bf16", "f16_f32", "f16_f16",
+                                                "tf32_f32"])
+@pytest.mark.parametrize("beta,with_bias", [(0.0, False), (0.5, True)])
+def test_split_last_wave_uniform(dtypes, beta, with_bias):
+    # uniform inputs within the oracle's bound (the split changes the order
+    # of the fp32 additions, not the bound), beta = 0 never reading C
+    nc = _clusters()
+    shapes = _shapes(nc)
+    if not shapes:
+        pytest.skip("the shapes assume a device with 8k CTA pairs")
+    name, M, N, K = shapes[2]
+    in_dtype, out_dtype = dtypes
+    A, B, C, bias = _operands(in_dtype, out_dtype, M, N, K, seed=40 + CASES.index(dtypes),
+                              small_ints=False)
+    if beta == 0.0:
+        C = torch.full_like(C, float("nan"))
+    bias = bias if with_bias else None
+    got, launches = _run(in_dtype, out_dtype, M, N, K, A, B, C, bias, 1.5, beta)
+    assert launches == 2
+    ref, bound = oracle.gemm_fp_ex(in_dtype, out_dtype, gen.ROW_MAJOR, gen.COL_MAJOR, M, N, K,
+                                   1.5, A, K, B, K, beta, C, N, bias)
+    assert_close(got, ref, bound, out_dtype, f"{name} {in_dtype}->{out_dtype} beta={beta}")
+
+
+def test_split_last_wave_repeats_bit_for_bit():
+    # the parts are added in a fixed order: repeated calls agree bit for bit
+    nc = _clusters()
+    shapes = _shapes(nc)
+    if not shapes:
+        pytest.skip("the shapes assume a device with 8k CTA pairs")
+    _, M, N, K = shapes[1]
+    A, B, C, bias = _operands(gen.BF16, gen.F32, M, N, K, seed=77, small_ints=False)
+    first, _ = _run(gen.BF16, gen.F32, M, N, K, A, B, C, bias, 1.0, 0.25)
+    for _ in range(5):
+        again, _ = _run(gen.BF16, gen.F32, M, N, K, A, B, C, bias, 1.0, 0.25)
+        assert torch.equal(again, first)
+
+
+def test_split_workspace_query():
+    # the query adds one 256 x 256 fp32 slot per CTA pair when a split is
+    # possible; INT8 and single-wave problems get none
+    nc = _clusters()
+    slot = 256 * 256 * 4
+    q = dga.dga_gemm_general_workspace_size
+    assert q(gen.BF16, gen.F32, gen.ROW_MAJOR, gen.COL_MAJOR, 2560, 2048, 1024, 1024, 1024, 2048,
+             T) == nc * slot
+    assert q(gen.BF16, gen.F32, gen.ROW_MAJOR, gen.COL_MAJOR, 512, 512, 1024, 1024, 1024, 512,
+             T) == 0
+    assert q(gen.BF16, gen.F32, gen.ROW_MAJOR, gen.COL_MAJOR, 2560, 2048, 512, 512, 512, 2048,
+             T) == 0  # 8 k-blocks: too shallow for two parts
