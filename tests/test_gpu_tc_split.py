@@ -192,3 +192,54 @@ def test_split_workspace_query():
              T) == 0
     assert q(gen.BF16, gen.F32, gen.ROW_MAJOR, gen.COL_MAJOR, 2560, 2048, 512, 512, 512, 2048,
              T) == 0  # 8 k-blocks: too shallow for two parts
+
+
+def _run_layouts(in_dtype, out_dtype, layout_a, layout_b, M, N, K, A, B, C, bias, lda, ldb):
+    dev = torch.device("cuda")
+    Ad, Bd, Cd = A.to(dev), B.to(dev), C.to(dev)
+    bd = bias.to(dev)
+    ws_bytes = dga.dga_gemm_general_workspace_size(in_dtype, out_dtype, layout_a, layout_b, M, N,
+                                                   K, lda, ldb, N, T)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    al, be = dga.scalar(1.0, in_dtype), dga.scalar(-1.0, in_dtype)
+    stream = torch.cuda.current_stream().cuda_stream
+    st = dga.dga_gemm_general(in_dtype, out_dtype, layout_a, layout_b, M, N, K, ctypes.byref(al),
+                              Ad.data_ptr(), lda, Bd.data_ptr(), ldb, ctypes.byref(be),
+                              Cd.data_ptr(), N, bd.data_ptr(), ws.data_ptr(), ws_bytes, T, stream)
+    assert st == dga.OK, dga.dga_status_string(st)
+    assert dga.dga_sync_status(stream) == dga.OK
+    return Cd.cpu(), dga.dga_last_launch_count()
+
+
+@pytest.mark.parametrize("in_dtype,out_dtype,layout_a,layout_b,pad,repacks", [
+    # a row-major B read in place (MN-major): the split alone
+    (gen.BF16, gen.F32, gen.ROW_MAJOR, gen.ROW_MAJOR, 0, 0),
+    # a column-major A read in place
+    (gen.F16, gen.F16, gen.COL_MAJOR, gen.COL_MAJOR, 0, 0),
+    # a leading dimension TMA cannot express (B padded by 3): B copied row by
+    # row into the front of the workspace, the partial sums behind it
+    (gen.BF16, gen.BF16, gen.ROW_MAJOR, gen.COL_MAJOR, 3, 1),
+    # TF32 with a row-major B: B transposed into the workspace, then the split
+    (gen.TF32, gen.F32, gen.ROW_MAJOR, gen.ROW_MAJOR, 0, 1),
+])
+def test_split_with_other_layouts_and_repacks(in_dtype, out_dtype, layout_a, layout_b, pad,
+                                              repacks):
+    # 80 tiles on 76 pairs (remainder 4) with K = 1024: the last wave is split,
+    # after a repack where one is needed; exact on small integers
+    nc = _clusters()
+    if _shapes(nc) == []:
+        pytest.skip("the shapes assume a device with 8k CTA pairs")
+    M, N, K = 256 * 10, 256 * 8, 1024
+    g = torch.Generator().manual_seed(11 + pad)
+    a_shape = (M, K + pad) if layout_a == gen.ROW_MAJOR else (K, M + pad)
+    b_shape = (K, N + pad) if layout_b == gen.ROW_MAJOR else (N, K + pad)
+    A = gen.small_int_matrix(a_shape, in_dtype, g, -8, 8)
+    B = gen.small_int_matrix(b_shape, in_dtype, g, -8, 8)
+    C = gen.small_int_matrix((M, N), out_dtype, g, -8, 8)
+    bias = gen.small_int_matrix((1, N), out_dtype, g, -8, 8).reshape(N)
+    got, launches = _run_layouts(in_dtype, out_dtype, layout_a, layout_b, M, N, K, A, B, C, bias,
+                                 A.shape[1], B.shape[1])
+    assert launches == repacks + 2, launches  # repack (if any), GEMM, reduce
+    ref, _ = oracle.gemm_fp_ex(in_dtype, out_dtype, layout_a, layout_b, M, N, K, 1.0, A,
+                               A.shape[1], B, B.shape[1], -1.0, C, N, bias)
+    assert_exact(got, ref, out_dtype, f"{in_dtype}->{out_dtype} A={layout_a} B={layout_b}")
