@@ -299,10 +299,13 @@ int dga_sum_rows(dga_dtype dtype, int64_t rows, int64_t cols, const void* G, int
     return e == cudaSuccess ? DGA_OK : fail_cuda(e);
 }
 
-size_t dga_gemm_general_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype,
-                                       dga_layout layout_a, dga_layout layout_b, int64_t M,
-                                       int64_t N, int64_t K, int64_t lda, int64_t ldb,
-                                       int64_t ldc, dga_path path) {
+namespace {
+
+// The workspace query, for the bytes a call would use (wanted) or only those
+// it cannot run without (required).
+size_t workspace_query(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_a,
+                       dga_layout layout_b, int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldc, dga_path path, bool required_only) {
     GemmArgs g{};
     const float one = 1.0f;
     const int32_t one_i = 1;
@@ -321,7 +324,17 @@ size_t dga_gemm_general_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype,
         probe.B = aligned16;
         chosen = choose_path(probe);
     }
-    return workspace_wanted(chosen, g);
+    return required_only ? workspace_required(chosen, g) : workspace_wanted(chosen, g);
+}
+
+}  // namespace
+
+size_t dga_gemm_general_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype,
+                                       dga_layout layout_a, dga_layout layout_b, int64_t M,
+                                       int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                                       int64_t ldc, dga_path path) {
+    return workspace_query(in_dtype, out_dtype, layout_a, layout_b, M, N, K, lda, ldb, ldc, path,
+                           false);
 }
 
 size_t dga_gemm_workspace_size(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_b,
@@ -473,6 +486,13 @@ const char* dga_status_string(int status) {
     }
 }
 
-int dga_version(void) { return 300; }  // 0.3.0: wide SIMT kernel with stream-K; naive-GEMM counter probe
+int dga_version(void) { return 310; }  // 0.3.1: split last waves on the tensor cores (INT8 included)
 
 }  // extern "C"
+
+size_t dga::workspace_required_bytes(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_a,
+                                     dga_layout layout_b, int64_t M, int64_t N, int64_t K,
+                                     int64_t lda, int64_t ldb, int64_t ldc, dga_path path) {
+    return workspace_query(in_dtype, out_dtype, layout_a, layout_b, M, N, K, lda, ldb, ldc, path,
+                           true);
+}

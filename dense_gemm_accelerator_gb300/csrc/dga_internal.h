@@ -95,6 +95,11 @@ bool tc_supports(const GemmArgs& a);
 size_t tc_workspace_size(const GemmArgs& a);
 // tc_workspace_size plus what the split last wave can use (optional)
 size_t tc_workspace_wanted(const GemmArgs& a, int sm_count);
+// The workspace a call cannot run without (dga_gemm_general_workspace_size
+// reports this plus the optional bytes); 0 for invalid arguments.
+size_t workspace_required_bytes(dga_dtype in_dtype, dga_dtype out_dtype, dga_layout layout_a,
+                                dga_layout layout_b, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                int64_t ldb, int64_t ldc, dga_path path);
 cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches);
 // Launches a kernel whose bounded wait runs out after limit_ns (self-test).
 cudaError_t tc_selftest_wait(uint64_t limit_ns, cudaStream_t stream);

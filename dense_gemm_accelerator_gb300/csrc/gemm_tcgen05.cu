@@ -106,10 +106,11 @@ struct TcParams {
     // CTA-pair kernel, floating point: the tiles after the first full_tiles
     // (the last, part-filled wave) are each cut along K into `splits` parts,
     // one work unit each, whose raw fp32 sums go to `partials` (256 x 256
-    // floats per unit) for tc_split_reduce_kernel; num_units = full_tiles +
-    // (num_tiles - full_tiles) * splits.  splits == 1: every unit is a tile.
+    // words per unit) for tc_split_reduce_kernel;
+    // num_units = full_tiles + (num_tiles - full_tiles) * splits.
+    // splits == 1: every unit is a tile.
     uint32_t full_tiles, splits, num_units;
-    float* partials;
+    uint32_t* partials;
 };
 
 // Shared-memory plan (dynamic, 1024-byte aligned): the stage ring, the
@@ -490,19 +491,18 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
 constexpr int kPairStages = 6;
 constexpr int kPairBN = 256;
 
-// A 32 x 32 block of raw fp32 sums into a split tile's partial slot (256 x
-// 256 floats, row-major, tile-relative; rows and columns past the matrix are
-// written too and never read), transposed through the staging square like
-// the stores above.
-__device__ __forceinline__ void store_block_partial(float* slot_base, uint32_t* stage, int lane,
-                                                    int row_base, int col_base,
-                                                    const uint32_t (&v)[32]) {
+// A 32 x 32 block of raw fp32 sums (as their bits) into a split tile's
+// partial slot (256 x 256 words, row-major, tile-relative; rows and columns
+// past the matrix are written too and never read), transposed through the
+// staging square like the stores above.
+__device__ __forceinline__ void store_block_partial(uint32_t* slot_base, uint32_t* stage, int lane,
+                                                    int row_base, int col_base, const uint32_t* v) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) stage[lane * 33 + j] = v[j];
     __syncwarp();
 #pragma unroll 4
     for (int i = 0; i < 32; ++i)
-        slot_base[(row_base + i) * kPairBN + col_base + lane] = __uint_as_float(stage[i * 33 + lane]);
+        slot_base[(row_base + i) * kPairBN + col_base + lane] = stage[i * 33 + lane];
     __syncwarp();
 }
 
@@ -694,7 +694,8 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
         bool ok = true;
         for (uint32_t u = cluster_id; ok && u < p.num_units; u += n_clusters) {
             // INT8 never splits (each unit a whole tile): its 64 running sums
-            // leave no registers for the unit's k-range
+            // leave no registers for a unit's k-range, and a split measured
+            // slower (the parts' epilogues cost more than the shorter wave)
             uint32_t tm, tn, kb_first = 0, kb_last = p.num_kb;
             int32_t slot = -1;
             if constexpr (kI8) tile_coords(u, p, tm, tn);
@@ -717,7 +718,7 @@ __global__ void __launch_bounds__(kI8 ? 576 : 192, 1)
                     else
                         store_block_partial(p.partials + static_cast<int64_t>(slot) * (256 * kPairBN),
                                             stage, lane, static_cast<int>(rank * 128 + quarter * 32),
-                                            c * 32, r);
+                                            c * 32, r);  // r: the fp32 sums' bits
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -806,7 +807,8 @@ __global__ void __launch_bounds__(256) tc_split_reduce_kernel(TcParams p) {
     const int64_t row = static_cast<int64_t>(tm) * 256 + r;
     if (row >= p.M) return;
     constexpr int64_t kSlot = 256 * kPairBN;
-    const float* base = p.partials + static_cast<int64_t>(j) * p.splits * kSlot + r * kPairBN + lane;
+    const float* base = reinterpret_cast<const float*>(p.partials) +
+                        static_cast<int64_t>(j) * p.splits * kSlot + r * kPairBN + lane;
     float sum[kPairBN / 32];
 #pragma unroll
     for (int q = 0; q < kPairBN / 32; ++q) sum[q] = base[q * 32];
@@ -1419,19 +1421,36 @@ int max_pair_clusters(Kern kern, int smem, int threads, const DeviceInfo& dev) {
 }
 
 // The split of the last wave: at most kMaxSplits parts per tile, none
-// shallower than kMinSplitKb k-blocks, 256 x 256 floats of workspace per part.
+// shallower than kMinSplitKb k-blocks, at most two rounds of parts (so at
+// most 2 x clusters slots of workspace, 256 x 256 32-bit words each).
 constexpr uint32_t kMaxSplits = 4;
 constexpr uint32_t kMinSplitKb = 8;
-constexpr size_t kSplitSlotBytes = size_t{256} * kPairBN * sizeof(float);
+constexpr size_t kSplitSlotBytes = size_t{256} * kPairBN * sizeof(uint32_t);
 
-// The CTA-pair GEMM, and for floating point, when split_ws holds enough and
-// the last wave is at most half full, the split of that wave's tiles along K
-// into work units of their own (one round of parts instead of a round of
-// whole tiles that leaves clusters idle) and the reduce that adds the parts
-// (*extra_launches is incremented for it).
+// Parts per tile for a last wave of `rem` tiles on `nc` clusters: the s that
+// makes that wave shortest, ceil(rem * s / nc) rounds of 1/s of a tile time
+// (the smaller s on a tie); 1 when no split shortens it.
+uint32_t split_parts(uint32_t rem, uint32_t nc, uint32_t num_kb) {
+    uint32_t best = 1, best_rounds = 1;  // one round of whole tiles
+    const uint32_t s_max = std::min(kMaxSplits, num_kb / kMinSplitKb);
+    for (uint32_t sp = 2; sp <= s_max; ++sp) {
+        if (rem * sp > 2 * nc) break;
+        const uint32_t rounds = (rem * sp + nc - 1) / nc;
+        if (rounds * best < best_rounds * sp) {  // rounds / sp < best_rounds / best
+            best = sp;
+            best_rounds = rounds;
+        }
+    }
+    return best;
+}
+
+// The CTA-pair GEMM, and for floating point, when split_ws holds enough and a
+// split shortens the last, part-filled wave (split_parts), the split of that
+// wave's tiles along K into work units of their own and the reduce that adds
+// the parts (*extra_launches is incremented for it).
 template <uint32_t kFmt, bool kI8, typename TOut>
 cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p0,
-                               const DeviceInfo& dev, cudaStream_t s, bool pdl, float* split_ws,
+                               const DeviceInfo& dev, cudaStream_t s, bool pdl, uint32_t* split_ws,
                                size_t split_bytes, int* extra_launches) {
     auto kern = tc_gemm_pair_kernel<kFmt, kI8, TOut>;
     const int smem = static_cast<int>(PairSmem<kI8 ? 8 : 4>::kLaunchBytes);
@@ -1449,14 +1468,12 @@ cudaError_t launch_pair_kernel(const CUtensorMap& ma, const CUtensorMap& mb, con
     const uint32_t nc = static_cast<uint32_t>(std::max(clusters, 1));
     if (!kI8 && split_ws != nullptr && p.num_tiles > nc) {
         const uint32_t rem = p.num_tiles % nc;
-        if (rem > 0 && 2 * rem <= nc) {
-            const uint32_t sp = std::min(std::min(nc / rem, kMaxSplits), p.num_kb / kMinSplitKb);
-            if (sp >= 2 && static_cast<size_t>(rem) * sp * kSplitSlotBytes <= split_bytes) {
-                p.full_tiles = p.num_tiles - rem;
-                p.splits = sp;
-                p.num_units = p.full_tiles + rem * sp;
-                p.partials = split_ws;
-            }
+        const uint32_t sp = rem > 0 ? split_parts(rem, nc, p.num_kb) : 1;
+        if (sp >= 2 && static_cast<size_t>(rem) * sp * kSplitSlotBytes <= split_bytes) {
+            p.full_tiles = p.num_tiles - rem;
+            p.splits = sp;
+            p.num_units = p.full_tiles + rem * sp;
+            p.partials = split_ws;
         }
     }
     cudaLaunchConfig_t cfg = {};
@@ -1602,15 +1619,15 @@ size_t tc_workspace_size(const GemmArgs& a) {
 
 size_t tc_workspace_wanted(const GemmArgs& a, int sm_count) {
     const size_t need = tc_workspace_size(a);
-    // the split last wave (CTA-pair kernel, floating point): at most one part
-    // per cluster, sm_count / 2 clusters; only for more tiles than clusters
-    // and K deep enough for two parts
+    // the split last wave (CTA-pair kernel, floating point): at most two
+    // rounds of parts on sm_count / 2 clusters; only for more tiles than
+    // clusters and K deep enough for two parts
     if (a.in_dtype == DGA_I8 || a.M <= BM || sm_count < 2) return need;
     const int64_t tiles = ((a.M + 255) / 256) * ((a.N + kPairBN - 1) / kPairBN);
     const int64_t kb = (a.K + k_per_stage(a.in_dtype == DGA_TF32 ? kFmtTF32 : kFmtBF16) - 1) /
                        k_per_stage(a.in_dtype == DGA_TF32 ? kFmtTF32 : kFmtBF16);
     if (tiles <= sm_count / 2 || kb < 2 * static_cast<int64_t>(kMinSplitKb)) return need;
-    return need + static_cast<size_t>(sm_count / 2) * kSplitSlotBytes;
+    return need + static_cast<size_t>(2 * (sm_count / 2)) * kSplitSlotBytes;
 }
 
 cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
@@ -1719,11 +1736,11 @@ cudaError_t tc_launch(const GemmArgs& a, const DeviceInfo& dev, int* launches) {
     p.num_units = p.num_tiles;
 
     // workspace past the repacked operands: room for the split last wave
-    float* split_ws = nullptr;
+    uint32_t* split_ws = nullptr;
     size_t split_bytes = 0;
     const size_t used = pl.a_bytes + pl.b_bytes;  // multiples of 256 bytes
     if (a.ws != nullptr && a.ws_bytes > used && aligned(static_cast<uint8_t*>(a.ws) + used, 16)) {
-        split_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + used);
+        split_ws = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(a.ws) + used);
         split_bytes = a.ws_bytes - used;
     }
     int extra = 0;  // the split's reduce

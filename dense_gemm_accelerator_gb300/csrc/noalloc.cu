@@ -139,11 +139,12 @@ extern "C" int dga_gemm_i8_noalloc(dga_layout layout_b, int64_t M, int64_t N, in
                                    const int32_t* alpha, const int8_t* A, int64_t lda,
                                    const int8_t* B, int64_t ldb, const int32_t* beta, int32_t* C,
                                    int64_t ldc, dga_stream_t stream) {
-    // A call that would not fit the fixed scratch is refused before anything
-    // is enqueued (invalid sizes make the query return 0; dga_gemm_ex then
-    // reports them).
-    const size_t need = dga_gemm_workspace_size(DGA_I8, DGA_I32, layout_b, M, N, K, lda, ldb, ldc,
-                                                DGA_PATH_TCGEN05);
+    // A call whose repacked operands would not fit the fixed scratch is
+    // refused before anything is enqueued (invalid sizes make the query return
+    // 0; dga_gemm_ex then reports them).  What is left of the scratch beyond
+    // them serves the split last wave when it holds enough.
+    const size_t need = dga::workspace_required_bytes(DGA_I8, DGA_I32, DGA_ROW_MAJOR, layout_b, M, N,
+                                                      K, lda, ldb, ldc, DGA_PATH_TCGEN05);
     if (need > kScratchBytes) return DGA_ERR_WORKSPACE;
     void* scratch = nullptr;
     if (need > 0) {

@@ -93,7 +93,8 @@ def test_workspace_size_query(lib):
     ws = dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
                                      w.N, w.N, dga.PATH_TCGEN05)
     assert ws >= 2 * (w.M + w.N) * w.K
-    # ... both K-major whatever B's layout: K padded to 8, each copy to 256 bytes
+    # ... both K-major whatever B's layout: K padded to 8, each copy to 256
+    # bytes (INT8 does not split its last wave, so nothing more)
     def ru(x, m):
         return (x + m - 1) // m * m
     for M, N, K in ((4093, 4099, 4096), (77, 91, 601), (5, 3, 1)):
@@ -103,11 +104,11 @@ def test_workspace_size_query(lib):
                                                dga.PATH_TCGEN05) == want, (M, N, K, layout)
     # column-major bf16 with aligned leading dimensions needs nothing; the
     # query reports the optional room for the split last wave of the CTA-pair
-    # kernel (one 256 x 256 fp32 slot per pair: 76 on the default 152 SMs),
-    # nothing for a single wave or a K too shallow to split
+    # kernel (two 256 x 256 32-bit slots per pair: 76 pairs on the default 152
+    # SMs), nothing for a single wave or a K too shallow to split
     w = W["bf16_8192"]
     assert dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
-                                       w.K, w.N, dga.PATH_TCGEN05) == 76 * 256 * 256 * 4
+                                       w.K, w.N, dga.PATH_TCGEN05) == 2 * 76 * 256 * 256 * 4
     assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.COL_MAJOR, 512, 512, 8192, 8192,
                                        8192, 512, dga.PATH_TCGEN05) == 0
     assert dga.dga_gemm_workspace_size(gen.BF16, gen.F32, gen.COL_MAJOR, 8192, 8192, 512, 512,
@@ -128,7 +129,7 @@ def test_workspace_size_query(lib):
     # as fp32 (4 bytes x N x K4)
     w = W["tf32_8192"]
     assert dga.dga_gemm_workspace_size(w.in_dtype, w.out_dtype, w.layout_b, w.M, w.N, w.K, w.K,
-                                       w.K, w.N, dga.PATH_TCGEN05) == 76 * 256 * 256 * 4
+                                       w.K, w.N, dga.PATH_TCGEN05) == 2 * 76 * 256 * 256 * 4
     assert dga.dga_gemm_workspace_size(gen.TF32, gen.F32, gen.ROW_MAJOR, 256, 512, 100, 100,
                                        512, 512, dga.PATH_TCGEN05) >= 512 * 100 * 4
     assert dga.dga_gemm_workspace_size(gen.TF32, gen.F32, gen.COL_MAJOR, 256, 512, 100, 102,

@@ -2,18 +2,19 @@
 the C ABI, against the CPU oracle element by element.
 
 A floating-point problem of more 256 x 256 tiles than there are CTA pairs
-(76 on a GB300) whose last wave is at most half full runs that wave's tiles
-cut along K into parts (as many as fit one round of the pairs, at most 4,
-none shallower than 8 k-blocks) when the workspace the size query reports is
-given: the parts' raw fp32 sums go to the workspace and a second launch adds
-them in part (K) order and applies alpha, beta, the bias row and the output
-type.  The shapes below split 2 and 4 ways, put the remainder at exactly
-half a wave (split) and one tile past it (not split), and leave ragged edges
-in both directions; with small-integer inputs every partial sum is exact, so
-the result must equal the oracle's exactly rounded once to the output type.
-The GEMM is the BLAS update of "AI Programming: Matrix Product", section
-"Dense matrix multiplication", with the bias row of its "Fully-connected
-layer" section.
+(76 on a GB300) runs its last, part-filled wave's tiles cut along K into s parts when that
+shortens the wave and the workspace the size query reports is given: s in
+2..4, none shallower than 8 k-blocks, at most two rounds of parts, chosen to
+make ceil(r * s / 76) / s smallest for r last-wave tiles.  The parts' raw
+fp32 sums go to the workspace and a second launch adds them in part (K)
+order and applies alpha, beta, the bias row and the output type (INT8 does
+not split).  The shapes below split 2, 3 and 4 ways, put the remainder at half a
+wave and one tile past it, leave a remainder no split shortens (52 tiles),
+and leave ragged edges in both directions; with small-integer inputs every
+partial sum is exact, so the result must equal the oracle's exactly rounded
+once to the output type.  The GEMM is the BLAS update of "AI Programming:
+Matrix Product", section "Dense matrix multiplication", with the bias row of
+its "Fully-connected layer" section.
 """
 import ctypes
 
@@ -39,16 +40,23 @@ def _tiles(M, N):
 
 
 def _splits(M, N, K, in_dtype):
-    """The split the rule gives (1: none) for a device with _clusters() pairs."""
+    """The split the rule gives (1: none) for a device with _clusters() pairs,
+    restated from the rule: the s in 2..min(4, k-blocks / 8) with r * s <= 2
+    pairs-count whose ceil(r * s / pairs) / s is smallest, if below 1."""
     nc = _clusters()
     tiles = _tiles(M, N)
-    if tiles <= nc:
+    if tiles <= nc or tiles % nc == 0:
         return 1
     rem = tiles % nc
-    if rem == 0 or 2 * rem > nc:
-        return 1
     kb = (K + (31 if in_dtype == gen.TF32 else 63)) // (32 if in_dtype == gen.TF32 else 64)
-    return max(1, min(nc // rem, 4, kb // 8))
+    best, best_len = 1, 1.0
+    for sp in range(2, min(4, kb // 8) + 1):
+        if rem * sp > 2 * nc:
+            break
+        length = -(-rem * sp // nc) / sp
+        if length < best_len:
+            best, best_len = sp, length
+    return best
 
 
 def _operands(in_dtype, out_dtype, M, N, K, seed, small_ints):
@@ -65,7 +73,13 @@ def _operands(in_dtype, out_dtype, M, N, K, seed, small_ints):
     return A, B, C, bias
 
 
+def _ru(x, m):
+    return (x + m - 1) // m * m
+
+
 def _run(in_dtype, out_dtype, M, N, K, A, B, C, bias, alpha, beta, workspace=True):
+    """workspace=False: only the bytes the call cannot run without (none for
+    these aligned floating-point operands; INT8's two bf16 copies)."""
     dev = torch.device("cuda")
     Ad, Bd, Cd = A.to(dev), B.to(dev), C.to(dev)
     bd = bias.to(dev) if bias is not None else None
@@ -73,6 +87,8 @@ def _run(in_dtype, out_dtype, M, N, K, A, B, C, bias, alpha, beta, workspace=Tru
                                                    gen.COL_MAJOR, M, N, K, K, K, N, T)
     if not workspace:
         ws_bytes = 0
+        if in_dtype == gen.I8:
+            ws_bytes = _ru(M * _ru(K, 8) * 2, 256) + _ru(N * _ru(K, 8) * 2, 256)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     al, be = dga.scalar(alpha, in_dtype), dga.scalar(beta, in_dtype)
     stream = torch.cuda.current_stream().cuda_stream
@@ -100,10 +116,14 @@ def _shapes(nc):
         # short) and a partial last k-block (K = 1096: rows of 2192 or 4384
         # bytes, which TMA reads in place)
         ("ragged", 256 * 9 + 100, 256 * 7 + 70, 1096),
-        # remainder exactly half a wave: 76 + 38 = 114 tiles (19 x 6)
+        # remainder exactly half a wave: 76 + 38 = 114 tiles (19 x 6), 2 parts
         ("half_wave", 256 * 19, 256 * 6, 1024),
-        # one tile past half: 76 + 39 = 115 tiles (23 x 5), not split
-        ("past_half", 256 * 23, 256 * 5, 1024),
+        # one tile past half: 76 + 39 = 115 tiles (23 x 5), 3 parts (K = 1536:
+        # 24 k-blocks, enough for three parts of at least 8)
+        ("past_half", 256 * 23, 256 * 5, 1536),
+        # 76 + 52 = 128 tiles (16 x 8): two parts would take two rounds, three
+        # more than two rounds of parts: not split
+        ("no_gain", 256 * 16, 256 * 8, 1024),
     ] if rows_one * 8 <= nc else []
 
 
@@ -111,7 +131,7 @@ CASES = [(gen.BF16, gen.F32), (gen.BF16, gen.BF16), (gen.F16, gen.F32), (gen.F16
          (gen.TF32, gen.F32)]
 
 
-@pytest.mark.parametrize("case", range(5))
+@pytest.mark.parametrize("case", range(6))
 @pytest.mark.parametrize("dtypes", CASES, ids=["bf16_f32", "bf16_bf16", "f16_f32", "f16_f16",
                                                 "tf32_f32"])
 def test_split_last_wave_exact(case, dtypes):
@@ -130,8 +150,7 @@ def test_split_last_wave_exact(case, dtypes):
     got, launches = _run(in_dtype, out_dtype, M, N, K, A, B, C, bias, 1.0, -1.0)
     sp = _splits(M, N, K, in_dtype)
     assert launches == (2 if sp > 1 else 1), (name, launches, sp)
-    if name != "past_half":
-        assert sp > 1, name
+    assert (sp > 1) == (name != "no_gain"), (name, sp)
     ref, _ = oracle.gemm_fp_ex(in_dtype, out_dtype, gen.ROW_MAJOR, gen.COL_MAJOR, M, N, K, 1.0,
                                A, K, B, K, -1.0, C, N, bias)
     assert_exact(got, ref, out_dtype, f"{name} {in_dtype}->{out_dtype}")
@@ -181,13 +200,13 @@ def test_split_last_wave_repeats_bit_for_bit():
 
 
 def test_split_workspace_query():
-    # the query adds one 256 x 256 fp32 slot per CTA pair when a split is
-    # possible; INT8 and single-wave problems get none
+    # the query adds two 256 x 256 32-bit slots per CTA pair when a split is
+    # possible (at most two rounds of parts); single-wave problems get none
     nc = _clusters()
     slot = 256 * 256 * 4
     q = dga.dga_gemm_general_workspace_size
     assert q(gen.BF16, gen.F32, gen.ROW_MAJOR, gen.COL_MAJOR, 2560, 2048, 1024, 1024, 1024, 2048,
-             T) == nc * slot
+             T) == 2 * nc * slot
     assert q(gen.BF16, gen.F32, gen.ROW_MAJOR, gen.COL_MAJOR, 512, 512, 1024, 1024, 1024, 512,
              T) == 0
     assert q(gen.BF16, gen.F32, gen.ROW_MAJOR, gen.COL_MAJOR, 2560, 2048, 512, 512, 512, 2048,
@@ -243,3 +262,27 @@ def test_split_with_other_layouts_and_repacks(in_dtype, out_dtype, layout_a, lay
     ref, _ = oracle.gemm_fp_ex(in_dtype, out_dtype, layout_a, layout_b, M, N, K, 1.0, A,
                                A.shape[1], B, B.shape[1], -1.0, C, N, bias)
     assert_exact(got, ref, out_dtype, f"{in_dtype}->{out_dtype} A={layout_a} B={layout_b}")
+
+
+@pytest.mark.parametrize("case", [0, 3, 4, 5])
+def test_int8_last_wave_not_split(case):
+    # INT8 never splits its last wave (three parts measured slower on the
+    # 4093 x 4099 x 4096 shape: each part pays a whole INT8 epilogue): the
+    # repack and the GEMM, whatever workspace is given, the same exact bits
+    nc = _clusters()
+    shapes = _shapes(nc)
+    if not shapes:
+        pytest.skip("the shapes assume a device with 8k CTA pairs")
+    name, M, N, K = shapes[case]
+    g = torch.Generator().manual_seed(90 + case)
+    A = gen.random_matrix((M, K), gen.I8, g, ("int8",))
+    B = gen.random_matrix((N, K), gen.I8, g, ("int8",))
+    C = gen.random_matrix((M, N), gen.I32, g, ("int8",))
+    bias = gen.random_matrix((1, N), gen.I32, g, ("int8",)).reshape(N)
+    got, launches = _run(gen.I8, gen.I32, M, N, K, A, B, C, bias, 3, -2)
+    assert launches == 2, (name, launches)  # repack, GEMM
+    ref = oracle.gemm_i8_ex(gen.ROW_MAJOR, gen.COL_MAJOR, M, N, K, 3, A, K, B, K, -2, C, N, bias)
+    assert_exact(got, ref, gen.I32, f"int8 {name}")
+    got0, launches0 = _run(gen.I8, gen.I32, M, N, K, A, B, C, bias, 3, -2, workspace=False)
+    assert launches0 == 2
+    assert torch.equal(got0, got), name
