@@ -2,17 +2,17 @@
 the C ABI, against the CPU oracle element by element.
 
 A floating-point problem of more 256 x 256 tiles than there are CTA pairs
-(76 on a GB300) runs its last, part-filled wave's tiles cut along K into s parts when that
-shortens the wave and the workspace the size query reports is given: s in
-2..4, none shallower than 8 k-blocks, at most two rounds of parts, chosen to
-make ceil(r * s / 76) / s smallest for r last-wave tiles.  The parts' raw
-fp32 sums go to the workspace and a second launch adds them in part (K)
-order and applies alpha, beta, the bias row and the output type (INT8 does
-not split).  The shapes below split 2, 3 and 4 ways, put the remainder at half a
-wave and one tile past it, leave a remainder no split shortens (52 tiles),
-and leave ragged edges in both directions; with small-integer inputs every
-partial sum is exact, so the result must equal the oracle's exactly rounded
-once to the output type.  The GEMM is the BLAS update of "AI Programming:
+(76 on a GB300) runs its last, part-filled wave's tiles cut along K into s
+parts when that shortens the wave and the workspace the size query reports
+is given: s in 2..4, none shallower than 8 k-blocks, at most two rounds of
+parts, chosen to make ceil(r * s / 76) / s smallest for r last-wave tiles.
+The parts' raw fp32 sums go to the workspace and a second launch adds them
+in part (K) order and applies alpha, beta, the bias row and the output type
+(INT8 does not split).  The shapes below split 2, 3 and 4 ways, put the
+remainder at half a wave and one tile past it, leave a remainder no split
+shortens (52 tiles), and leave ragged edges in both directions; with
+small-integer inputs every partial sum is exact, so the result must equal
+the oracle's exactly rounded once to the output type.  The GEMM is the BLAS update of "AI Programming:
 Matrix Product", section "Dense matrix multiplication", with the bias row of
 its "Fully-connected layer" section.
 """
