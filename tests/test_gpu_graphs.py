@@ -10,7 +10,6 @@ call bit for bit (every path sums in a fixed order), with the device status
 word clear.  Outputs are filled with a sentinel before each replay, so a
 replay that wrote nothing fails.
 """
-import ctypes
 
 import pytest
 import torch
