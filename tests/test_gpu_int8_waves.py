@@ -114,3 +114,34 @@ def test_int8_past_one_wave_repeats():
     first = _run(gen.ROW_MAJOR, gen.ROW_MAJOR, M, N, K, A, B, C, bias, 7, 3)
     for _ in range(4):
         assert torch.equal(_run(gen.ROW_MAJOR, gen.ROW_MAJOR, M, N, K, A, B, C, bias, 7, 3), first)
+
+
+@pytest.mark.parametrize("K,layout_b", [(131072, gen.COL_MAJOR), (131072, gen.ROW_MAJOR),
+                                         (139264, gen.COL_MAJOR)])
+def test_int8_at_the_largest_k(K, layout_b):
+    # K = 2^17 with every entry -128: each product is 2^14 and a full dot
+    # product 2^31, one past the int32 range, so it wraps to -2^31 (the
+    # 1024-deep chunks stay exact in fp32; their int32 sum wraps).  Beside
+    # it, sums just inside the range: row 1 has one +127 (2^31 - 2^14 -
+    # 16256), column 3 of B one +1 (2^31 - 2^14 - 128), row 2 is all +127
+    # (-16256 * 2^17).  K = 139264 (136 chunks) goes further past the range.
+    # Every element is checked against the oracle's int64 sum reduced mod
+    # 2^32.  Two tile rows on the CTA-pair kernel (M = 260, the second
+    # ragged), alpha = 1, beta = 0
+    M, N = 260, 130
+    A = torch.full((M, K), -128, dtype=torch.int8)
+    A[1, 5] = 127
+    A[2, :] = 127
+    B = torch.full((N, K) if layout_b == gen.COL_MAJOR else (K, N), -128, dtype=torch.int8)
+    if layout_b == gen.COL_MAJOR:
+        B[3, 7] = 1
+    else:
+        B[7, 3] = 1
+    C = torch.zeros(M, N, dtype=torch.int32)
+    got = _run(gen.ROW_MAJOR, layout_b, M, N, K, A, B, C, None, 1, 0)
+    ref = oracle.gemm_i8_ex(gen.ROW_MAJOR, layout_b, M, N, K, 1, A, K, B, B.shape[1], 0, C, N,
+                            None)
+    assert np.array_equal(got.numpy(), ref.astype(np.int32)), \
+        f"K={K}: mismatch at {np.argwhere(got.numpy() != ref.astype(np.int32))[:5].tolist()}"
+    if K == 131072:
+        assert int(got[0, 0]) == -(2 ** 31)  # (-128)(-128) 2^17 times = 2^31, wrapped
