@@ -141,8 +141,9 @@ extern "C" int dga_gemm_i8_noalloc(dga_layout layout_b, int64_t M, int64_t N, in
                                    int64_t ldc, dga_stream_t stream) {
     // A call whose repacked operands would not fit the fixed scratch is
     // refused before anything is enqueued (invalid sizes make the query return
-    // 0; dga_gemm_ex then reports them).  What is left of the scratch beyond
-    // them serves the split last wave when it holds enough.
+    // 0; dga_gemm_ex then reports them).  Only the bytes the call cannot run
+    // without count here, not the optional ones the public size query adds
+    // for the split last waves of other paths.
     const size_t need = dga::workspace_required_bytes(DGA_I8, DGA_I32, DGA_ROW_MAJOR, layout_b, M, N,
                                                       K, lda, ldb, ldc, DGA_PATH_TCGEN05);
     if (need > kScratchBytes) return DGA_ERR_WORKSPACE;
