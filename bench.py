@@ -22,7 +22,10 @@ the measured sustained one for `*_sustained`), `ms` per call, `traffic_mb`
 current code), `sm_mhz` (median sampled SM clock), and for the bf16-rate
 tensor rows `spec_frac_max` and `spec_frac_obs` (of the unit-count peak, SMs
 x 8192 FLOP/clk, at the maximum clock and at the sampled clock: the
-clock-normalised figure).
+clock-normalised figure); the INT8 row adds `x_probe`, its rate over that
+of the integer mma.sync instruction as the library's probe measures it
+(`peaks.int8_mma_tops`): how far the exact bf16 encoding on the tcgen05
+pipe runs past what an INT8 GEMM built on that instruction could.
 
 `--impl reference` times the CPU oracle (plain fp64 triple loop, as it
 stands) on the host cores, on a bounded sample of the same workload.
@@ -216,7 +219,39 @@ def compact_peaks(peaks):
         out["fma_probe_error"] = probe["error"][:80]
     elif probe:
         out["fma_probe"] = [sig(probe["ffma_tflops"]), sig(probe["ffma2_tflops"])]
+    if peaks.get("int8_mma_sync_tops"):
+        out["int8_mma_tops"] = sig(peaks["int8_mma_sync_tops"])
     return out
+
+
+def int8_mma_probe(device, iters=4096, reps=5):
+    """The library's INT8 instruction-rate probe: best of `reps` event-timed
+    launches of independent mma.sync m16n8k32 s8 chains, in TOP/s -- the
+    ceiling of an INT8 GEMM built on that instruction, beside which the
+    INT8 row (exact bf16 encoding on the tcgen05 pipe) is reported."""
+    import ctypes
+    import torch
+    import dense_gemm_accelerator_gb300 as dga
+    n = dga.dga_probe_fp32_fma_out_floats()
+    out = torch.empty(n, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    ops = ctypes.c_double(0.0)
+    best = 0.0
+    for i in range(reps + 1):  # the first launch is a warm-up
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st = dga.dga_probe_int8_mma(iters, out.data_ptr(), n, ctypes.byref(ops), stream.cuda_stream)
+        e1.record(stream)
+        if st != dga.OK:
+            raise RuntimeError(f"INT8 probe: {dga.dga_status_string(st)}")
+        e1.synchronize()
+        if i:
+            best = max(best, ops.value / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+    st = dga.dga_sync_status(stream.cuda_stream)
+    if st != dga.OK:
+        raise RuntimeError(f"INT8 probe: {dga.dga_status_string(st)}")
+    return best
 
 
 def fp32_fma_probe(device, iters=12000, reps=5):
@@ -837,6 +872,10 @@ def main():
     except RuntimeError as e:  # the cross-check failed: keep the unit-count peak, say why
         probe = {"error": str(e)}
     peaks["fp32_ffma_probe"] = probe
+    try:  # context for the INT8 row: the legacy integer instruction's rate
+        peaks["int8_mma_sync_tops"] = int8_mma_probe(device)
+    except RuntimeError:
+        peaks["int8_mma_sync_tops"] = None
     if "error" not in probe:
         best_probe = max(probe["ffma_tflops"], probe["ffma2_tflops"])
         if best_probe > 1.01 * peaks["fp32_ffma_tflops"]:
@@ -951,7 +990,11 @@ def main():
             if seconds is not None:
                 rf["calls"], rf["seconds"] = float(iters), iters * ms * 1e-3
             add_spec_peak(rf, peaks, rf["clocks"].get("sm_mhz"))
-            per[name if seconds is None else name + "_sustained"] = compact_row(rf)
+            row = compact_row(rf)
+            if ow.in_dtype == gen.I8 and peaks.get("int8_mma_sync_tops"):
+                # against the best rate of the integer mma.sync instruction
+                row["x_probe"] = sig(rf["achieved"] / peaks["int8_mma_sync_tops"], 3)
+            per[name if seconds is None else name + "_sustained"] = row
             del r
             torch.cuda.empty_cache()
         line["peaks"] = compact_peaks(peaks)

@@ -56,6 +56,7 @@ SIGNATURES = {
     "dga_spmv_csr_workspace_size": (_SZ, [_I64, _I64]),
     "dga_probe_fp32_fma": (_CI, [_CI, _I64, _VP, _I64, _VP, _VP]),
     "dga_probe_fp32_fma_out_floats": (_I64, []),
+    "dga_probe_int8_mma": (_CI, [_I64, _VP, _I64, _VP, _VP]),
     "dga_probe_naive_sgemm": (_CI, [_I64, _I64, _I64, _VP, _VP, _VP, _VP]),
 }
 
@@ -182,6 +183,10 @@ def dga_probe_fp32_fma(packed, iters, out, out_floats, flops, stream):
 
 def dga_probe_fp32_fma_out_floats():
     return lib().dga_probe_fp32_fma_out_floats()
+
+
+def dga_probe_int8_mma(iters, out, out_ints, ops, stream):
+    return lib().dga_probe_int8_mma(iters, out, out_ints, ops, stream)
 
 
 def dga_probe_naive_sgemm(M, N, K, A, B, C, stream):

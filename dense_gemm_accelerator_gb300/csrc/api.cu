@@ -450,6 +450,22 @@ int dga_probe_fp32_fma(int packed, int64_t iters, float* out, int64_t out_floats
     return DGA_OK;
 }
 
+int dga_probe_int8_mma(int64_t iters, int32_t* out, int64_t out_ints, double* ops,
+                       dga_stream_t stream) {
+    if (iters < 1 || iters > (int64_t{1} << 17)) return -1;
+    if (out == nullptr) return -2;
+    if (ops == nullptr) return -4;
+    DeviceInfo dev;
+    cudaError_t e = current_device_info(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev.major != 10 || dev.minor != 3) return DGA_ERR_DEVICE;
+    if (out_ints < fma_probe_out_floats(dev.sm_count)) return -3;
+    e = int8_mma_probe_launch(iters, out, dev.sm_count, ops, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e);
+    t_last_launches = 1;
+    return DGA_OK;
+}
+
 int dga_probe_naive_sgemm(int64_t M, int64_t N, int64_t K, const float* A, const float* B, float* C,
                           dga_stream_t stream) {
     constexpr int64_t kMaxElems = int64_t{1} << 31;  // every index stays below 2^31

@@ -82,7 +82,9 @@ cudaError_t spmv_status_take(int* status);
 
 // FP32 FMA-rate probe (measurement only): floats of `out` one launch writes,
 // and the launch itself (*flops receives the FLOPs it performs).
-int64_t fma_probe_out_floats(int sm_count);
+int64_t fma_probe_out_floats(int sm_count);  // also the int32s of the INT8 probe
+cudaError_t int8_mma_probe_launch(int64_t iters, int32_t* out, int sm_count, double* ops,
+                                  cudaStream_t stream);
 cudaError_t fma_probe_launch(int packed, int64_t iters, float* out, int sm_count, double* flops,
                              cudaStream_t stream);
 

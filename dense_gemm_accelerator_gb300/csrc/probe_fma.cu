@@ -1,4 +1,5 @@
-// FP32 FMA-rate probe: the denominator check for the SIMT GEMM's roofline.
+// FP32 FMA-rate probe: the denominator check for the SIMT GEMM's roofline
+// (and, below it, the INT8 instruction-rate probe).
 //
 // The roofline of "Matrix multiplication: arithmetic intensity, tiling and
 // Tensor Core" (section 5.1) bounds a compute-bound kernel by the chip's
@@ -71,7 +72,58 @@ fma2_probe_kernel(int64_t iters, float* out) {
     out[blockIdx.x * blockDim.x + threadIdx.x] = s;
 }
 
+// INT8 instruction-rate probe: the legacy integer tensor instruction that
+// an exact INT8 GEMM could be built on instead of the bf16 encoding, timed at
+// its best (independent accumulator chains, operands already in registers).
+// Every lane of warp w holds A bytes c = w % 5 + 1 and B bytes -2, so each
+// m16n8k32 step adds 32 * c * (-2) to every accumulator element whatever the
+// fragment layout, and a thread's sum over its 8 x 4 accumulators after
+// `iters` steps of all 8 chains is -2048 * c * iters: the result shows the
+// work was done.
+constexpr int kMmaChains = 8;
+
+__global__ void __launch_bounds__(kProbeThreads)
+int8_mma_probe_kernel(int64_t iters, int32_t* out) {
+    const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const uint32_t c = static_cast<uint32_t>(warp % 5) + 1;
+    uint32_t a[4], b[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = 0x01010101u * c;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) b[i] = 0xFEFEFEFEu;  // bytes -2
+    int32_t acc[kMmaChains][4];
+#pragma unroll
+    for (int j = 0; j < kMmaChains; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[j][i] = 0;
+    for (int64_t it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < kMmaChains; ++j)
+            asm volatile(
+                "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, "
+                "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                : "+r"(acc[j][0]), "+r"(acc[j][1]), "+r"(acc[j][2]), "+r"(acc[j][3])
+                : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+    }
+    int32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < kMmaChains; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) s += acc[j][i];
+    out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+}
+
 }  // namespace
+
+cudaError_t int8_mma_probe_launch(int64_t iters, int32_t* out, int sm_count, double* ops,
+                                  cudaStream_t stream) {
+    const int grid = sm_count * kProbeCtasPerSm;
+    // per warp and iteration kMmaChains m16n8k32 steps of 2 * 16 * 8 * 32 ops
+    *ops = static_cast<double>(grid) * (kProbeThreads / 32) * static_cast<double>(iters) *
+           kMmaChains * (2.0 * 16 * 8 * 32);
+    int8_mma_probe_kernel<<<grid, kProbeThreads, 0, stream>>>(iters, out);
+    return cudaGetLastError();
+}
 
 int64_t fma_probe_out_floats(int sm_count) {
     return static_cast<int64_t>(sm_count) * kProbeCtasPerSm * kProbeThreads;

@@ -251,8 +251,27 @@ int dga_probe_fp32_fma(int packed, int64_t iters, float* out, int64_t out_floats
                        dga_stream_t stream);
 
 /* Floats of `out` that dga_probe_fp32_fma writes on the current device
- * (152 SMs assumed when no device can be queried). */
+ * (152 SMs assumed when no device can be queried); also the int32 values
+ * dga_probe_int8_mma writes. */
 int64_t dga_probe_fp32_fma_out_floats(void);
+
+/*
+ * Measurement helper, not part of any GEMM: the rate of the integer tensor
+ * instruction an exact INT8 GEMM could use instead of this library's bf16
+ * encoding (mma.sync.m16n8k32 with s8 operands and s32 accumulators; the
+ * tcgen05 integer kind is not available for sm_103a).  Enqueues one kernel:
+ * 4 CTAs of 256 threads per SM, each warp running 8 independent accumulator
+ * chains of `iters` steps on operands held in registers (the instruction's
+ * best case).  Every lane of warp w holds A bytes c = w % 5 + 1 and B bytes
+ * -2, so thread t writes out[t] = -2048 * c * iters, whatever the fragment
+ * layout.  *ops (host pointer) receives the integer operations of the launch
+ * (2 * 16 * 8 * 32 per instruction); time it with events around the call.
+ * `out`: device memory of at least dga_probe_fp32_fma_out_floats() int32.
+ * Errors: -1 iters outside [1, 2^17]; -2 out null; -3 out_ints too small;
+ * -4 ops null; DGA_ERR_DEVICE, DGA_ERR_CUDA.
+ */
+int dga_probe_int8_mma(int64_t iters, int32_t* out, int64_t out_ints, double* ops,
+                       dga_stream_t stream);
 
 /*
  * Measurement helper, not part of any GEMM: the naive GEMM of "GEMM

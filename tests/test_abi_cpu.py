@@ -285,6 +285,20 @@ def test_fma_probe_argument_errors(lib):
                                   None) in (dga.ERR_CUDA, dga.ERR_DEVICE)
 
 
+def test_int8_mma_probe_argument_errors(lib):
+    import ctypes
+    ops = ctypes.c_double(0.0)
+    n = dga.dga_probe_fp32_fma_out_floats()
+    f = dga.dga_probe_int8_mma
+    assert f(0, 0x1000, n, ctypes.byref(ops), None) == -1
+    assert f((1 << 17) + 1, 0x1000, n, ctypes.byref(ops), None) == -1
+    assert f(10, None, n, ctypes.byref(ops), None) == -2
+    assert f(10, 0x1000, n, None, None) == -4
+    # valid arguments need the device, absent here (the out size is checked
+    # against the device's SM count, after the device)
+    assert f(10, 0x1000, n, ctypes.byref(ops), None) in (dga.ERR_CUDA, dga.ERR_DEVICE)
+
+
 def test_naive_probe_argument_errors_before_the_device():
     # the counter-calibration probe checks its arguments before touching a device
     f = dga.dga_probe_naive_sgemm

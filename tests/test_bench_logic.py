@@ -135,12 +135,14 @@ def test_spec_peak_fields():
 
 
 def test_per_dtype_rows_fit_a_short_tail():
-    # The driver keeps only the end of the bench's output line, so the extra
-    # keys come last and a full set of per_dtype rows -- each with the fields
-    # its kind of workload carries, a throttle reason on every tensor row --
-    # must stay well within a few thousand characters.
+    # The driver keeps only the end of the bench's output line (about 3000
+    # characters with its own framing), so the extra keys come last and a
+    # full set of per_dtype rows -- each with the fields its kind of workload
+    # carries, a throttle reason on every tensor row -- must stay well within
+    # that.
     peaks = bench.load_peaks(152)
     peaks["fp32_ffma_probe"] = {"ffma_tflops": 79.91234, "ffma2_tflops": 79.81234}
+    peaks["int8_mma_sync_tops"] = 157.91234
     per = {}
     names = [n for n in bench.PER_DTYPE] + [n + "_sustained" for n in bench.SUSTAINED]
     for i, name in enumerate(names):
@@ -159,8 +161,10 @@ def test_per_dtype_rows_fit_a_short_tail():
             rf["calls"], rf["seconds"] = 6450.0, 4.00123
         bench.add_spec_peak(rf, peaks, 1965.0)
         per[name] = bench.compact_row(rf)
+        if name.startswith("int8"):
+            per[name]["x_probe"] = bench.sig(rf["achieved"] / peaks["int8_mma_sync_tops"], 3)
     tail = json.dumps({"peaks": bench.compact_peaks(peaks), "per_dtype": per})
-    assert len(tail) < 2600, len(tail)
+    assert len(tail) < 2700, len(tail)
     assert set(per) >= {"bf16_8192", "skinny_m1", "skinny_m8", "skinny_m16", "int8_ragged"}
     row = per["bf16_8192"]
     assert row["frac"] == 0.934 and row["achieved"] == 1772.0 and row["traffic_mb"] == 1340.0

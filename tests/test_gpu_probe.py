@@ -83,3 +83,21 @@ def test_naive_probe_matches_the_oracle(M, N, K):
             assert_exact(C.cpu(), ref, gen.F32, f"naive {M}x{N}x{K} small integers")
         else:
             assert_close(C.cpu(), ref, bound, gen.F32, f"naive {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("iters", [1, 37])
+def test_int8_mma_probe_outputs_and_ops(iters):
+    # every lane of warp w holds A bytes c = w % 5 + 1 and B bytes -2: each
+    # m16n8k32 step adds 32 * c * (-2) to each of a thread's 8 x 4
+    # accumulators, whatever the fragment layout, so thread t ends at
+    # -2048 * c * iters; the op count is 8 chains x 2*16*8*32 per warp and step
+    n = dga.dga_probe_fp32_fma_out_floats()
+    out = torch.full((n,), 12345, dtype=torch.int32, device="cuda")
+    ops = ctypes.c_double(0.0)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert dga.dga_probe_int8_mma(iters, out.data_ptr(), n, ctypes.byref(ops), stream) == dga.OK
+    assert dga.dga_sync_status(stream) == dga.OK
+    warp = np.arange(n) // 32
+    want = -2048 * (warp % 5 + 1) * iters
+    assert np.array_equal(out.cpu().numpy(), want.astype(np.int32))
+    assert ops.value == (n // 32) * iters * 8 * (2 * 16 * 8 * 32)
