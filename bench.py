@@ -224,7 +224,7 @@ def compact_peaks(peaks):
     return out
 
 
-def int8_mma_probe(device, iters=4096, reps=5):
+def int8_mma_probe(device, iters=1024, reps=5):
     """The library's INT8 instruction-rate probe: best of `reps` event-timed
     launches of independent mma.sync m16n8k32 s8 chains, in TOP/s -- the
     ceiling of an INT8 GEMM built on that instruction, beside which the
